@@ -1,0 +1,337 @@
+"""Plain, slow CPU oracle for the prefix-cached flow-matching action expert.
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the benchmark's
+CPU-baseline leg may import this module.  It shares no code with the CUDA
+library (no kernels, headers, helpers or constants) and the library never
+calls it.
+
+What it computes, and where the pages define it
+(page: "vla.cpp: A Unified Inference Runtime for Vision-Language-Action Models"):
+
+* Euler flow-matching integration, §III-A Eq. (1):
+  X^{k+1} = X^k + (tau_{k+1} - tau_k) v(X^k, tau_k, C).
+* Prefix (conditioning) K/V cache and attention, §III-B Eq. (2):
+  K_C = Z W_K, V_C = Z W_V computed once per observation; attention is
+  softmax(Q K^T / sqrt(d_k) + M) V over keys, with the action (suffix) keys
+  and values appended to the cached prefix ones (joint attention, §III-B).
+* Ternary-weight / int8-activation linear layers, §III-D Eq. (4), in IEEE
+  fp32 with exact integer accumulation and round-to-nearest-even.
+* Parity metrics, §III-E Eq. (5).
+
+The block structure of the velocity network (pre-norm transformer layers with
+time-modulated RMSNorm, joint attention, a GeLU MLP and a velocity
+projection) is not printed on the pages; the readings taken here are:
+ - time embedding: d_t sinusoids sin/cos(1000 tau w_i), w_i = 10000^(-i/(d_t/2));
+ - time conditioning c = W_t2 SiLU(W_t1 e); per-layer modulation
+   W_mod^l SiLU(c) = (gamma_a, beta_a, gamma_m, beta_m); final W_mod_f SiLU(c)
+   = (gamma_f, beta_f); modulated RMSNorm n(h) (1 + gamma) + beta, eps 1e-6,
+   no learned gain, no biases anywhere;
+ - GeLU is the exact x Phi(x); the MLP is not gated;
+ - no positions in prefix or suffix; GQA query head j reads K/V head
+   floor(j / (n_q / n_kv)); key order is prefix then suffix; M = 0;
+ - schedule tau_k = k / S, integrated 0 -> 1;
+ - W2A8: the six per-layer maps W_q, W_k, W_v, W_o, W_up, W_down are ternary
+   with one fp32 scale per tensor; one activation quantisation per GEMM input
+   (shared by Q, K and V); y = bf16_rne((fp32(acc) * alpha) * beta).
+
+Precision: fp64 everywhere except Eq. (4), which is pinned to IEEE fp32 so
+that integer codes are reproducible bit for bit.
+
+Pins (tests/test_oracle_pins.py): brute-force softmax; a library attention
+routine; single-visible-key and zero-query closed forms; prefix permutation
+invariance; cache reuse == recompute (bitwise); zero velocity head returns
+the noise (bitwise); constant velocity field closed-form endpoint; one-step
+solve; suffix permutation equivariance; batch independence; GQA == replicated
+MHA; the whole velocity network against library routines (torch fp64);
+quantiser worked ties and error bound; ternary GEMM against int64 brute
+force; bf16 rounding against a library conversion; Eq. (5) special cases.
+No function here is left without a pin.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf as _erf
+
+F64 = np.float64
+
+__all__ = [
+    "sinusoidal_time_embedding", "silu", "gelu", "rmsnorm_modulate", "linear",
+    "time_conditioning", "prefix_kv", "joint_attention", "velocity", "schedule",
+    "denoise", "denoise_recompute", "quantize_rows", "pack_ternary",
+    "unpack_ternary", "bf16_rne", "ternary_linear", "velocity_w2a8",
+    "denoise_w2a8", "parity_metrics",
+]
+
+
+# ----------------------------------------------------------------------------
+# Elementwise pieces
+# ----------------------------------------------------------------------------
+
+def sinusoidal_time_embedding(tau: float, d_t: int) -> np.ndarray:
+    """e(tau) in R^{d_t}: first half sin(1000 tau w_i), second half cos(1000 tau w_i)."""
+    half = d_t // 2
+    omega = 10000.0 ** (-np.arange(half, dtype=F64) / half)
+    arg = 1000.0 * float(tau) * omega
+    return np.concatenate([np.sin(arg), np.cos(arg)])
+
+
+def silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def gelu(x):
+    """Exact GeLU x * Phi(x)."""
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def rmsnorm_modulate(h, gamma, beta, eps):
+    """h / sqrt(mean(h^2) + eps) * (1 + gamma) + beta over the last axis."""
+    ms = np.mean(h * h, axis=-1, keepdims=True)
+    return h / np.sqrt(ms + eps) * (1.0 + gamma) + beta
+
+
+def linear(x, W):
+    """x W^T for W stored [out, in]."""
+    return np.asarray(x, dtype=F64) @ np.asarray(W, dtype=F64).T
+
+
+# ----------------------------------------------------------------------------
+# Time conditioning (depends on tau and weights only)
+# ----------------------------------------------------------------------------
+
+def time_conditioning(w: dict, cfg, tau: float):
+    """Per-layer (gamma_a, beta_a, gamma_m, beta_m) and final (gamma_f, beta_f)."""
+    D = cfg.D
+    e = sinusoidal_time_embedding(tau, cfg.d_t)
+    c = linear(silu(linear(e, w["wt1"])), w["wt2"])
+    sc = silu(c)
+    per_layer = [linear(sc, w["wmod"][l]).reshape(4, D) for l in range(cfg.L)]
+    final = linear(sc, w["wmod_f"]).reshape(2, D)
+    return per_layer, final
+
+
+# ----------------------------------------------------------------------------
+# Prefix K/V cache, §III-B Eq. (2): K_C = Z W_K, V_C = Z W_V
+# ----------------------------------------------------------------------------
+
+def prefix_kv(Z, w: dict, cfg):
+    """Z [B, P, d_vlm] -> K_C, V_C [L, B, n_kv, P, d_h] (fp64).
+
+    Token-wise projection of the raw prefix hidden states: no mask, no
+    positions, so no causal structure can leak into the cache.
+    """
+    Z = np.asarray(Z, dtype=F64)
+    B, P, _ = Z.shape
+    K = np.empty((cfg.L, B, cfg.n_kv, P, cfg.d_h), dtype=F64)
+    V = np.empty_like(K)
+    for l in range(cfg.L):
+        K[l] = linear(Z, w["wk_pre"][l]).reshape(B, P, cfg.n_kv, cfg.d_h).transpose(0, 2, 1, 3)
+        V[l] = linear(Z, w["wv_pre"][l]).reshape(B, P, cfg.n_kv, cfg.d_h).transpose(0, 2, 1, 3)
+    return K, V
+
+
+def joint_attention(q, k_s, v_s, Kc, Vc, prefix_visible=None):
+    """Eq. (2) per head with suffix keys/values appended to the cached prefix.
+
+    q [B, H, n_q, d_h]; k_s, v_s [B, H, n_kv, d_h]; Kc, Vc [B, n_kv, P, d_h].
+    prefix_visible: optional bool [B, P]; a hidden prefix key gets M = -inf.
+    Suffix keys are always visible.  Two passes per query row: the row
+    maximum, then the exponentials, their sum and the weighted values.
+    """
+    B, H, n_q, d_h = q.shape
+    n_kv = k_s.shape[2]
+    group = n_q // n_kv
+    scale = 1.0 / math.sqrt(d_h)
+    o = np.empty((B, H, n_q, d_h), dtype=F64)
+    for b in range(B):
+        for j in range(n_q):
+            g = j // group
+            keys = np.concatenate([Kc[b, g], k_s[b, :, g]], axis=0)
+            vals = np.concatenate([Vc[b, g], v_s[b, :, g]], axis=0)
+            s = (q[b, :, j] @ keys.T) * scale  # [H, P + H]
+            if prefix_visible is not None:
+                M = np.zeros(keys.shape[0], dtype=F64)
+                M[: Kc.shape[2]][~np.asarray(prefix_visible[b], dtype=bool)] = -np.inf
+                s = s + M
+            m = np.max(s, axis=1, keepdims=True)
+            e = np.exp(s - m)
+            o[b, :, j] = (e @ vals) / np.sum(e, axis=1, keepdims=True)
+    return o
+
+
+# ----------------------------------------------------------------------------
+# Velocity network and Euler solver, §III-A Eq. (1)
+# ----------------------------------------------------------------------------
+
+def _expert(x, mods, Kc, Vc, w, cfg, lin, taps=None, prefix_visible=None):
+    """Shared layer walk; ``lin(u, name, l)`` applies the named per-layer map."""
+    x = np.asarray(x, dtype=F64)
+    B, H, _ = x.shape
+    per_layer, final = mods
+    h = linear(x, w["win"])  # [B, H, D]
+    for l in range(cfg.L):
+        ga, ba, gm, bm = per_layer[l]
+        u = rmsnorm_modulate(h, ga, ba, cfg.eps)
+        q = lin(u, "wq", l).reshape(B, H, cfg.n_q, cfg.d_h)
+        ks = lin(u, "wk", l).reshape(B, H, cfg.n_kv, cfg.d_h)
+        vs = lin(u, "wv", l).reshape(B, H, cfg.n_kv, cfg.d_h)
+        o = joint_attention(q, ks, vs, Kc[l], Vc[l], prefix_visible).reshape(B, H, cfg.qdim)
+        if taps is not None:
+            taps.setdefault("attn", []).append(o)
+        h = h + lin(o, "wo", l)
+        u = rmsnorm_modulate(h, gm, bm, cfg.eps)
+        h = h + lin(gelu(lin(u, "wup", l)), "wdown", l)
+        if taps is not None:
+            taps.setdefault("h", []).append(h)
+    gf, bf = final
+    return linear(rmsnorm_modulate(h, gf, bf, cfg.eps), w["wout"])
+
+
+def velocity(x, tau, Kc, Vc, w: dict, cfg, taps=None, prefix_visible=None):
+    """v_theta(X, tau, C): action chunk x [B, H, d_a] -> velocity [B, H, d_a]."""
+    mods = time_conditioning(w, cfg, tau)
+    return _expert(x, mods, Kc, Vc, w, cfg, lambda u, n, l: linear(u, w[n][l]),
+                   taps, prefix_visible)
+
+
+def schedule(S: int) -> np.ndarray:
+    """tau_0..tau_S = k / S (0 -> 1)."""
+    return np.arange(S + 1, dtype=F64) / S
+
+
+def denoise(noise, Kc, Vc, w: dict, cfg, S: int | None = None, vel=velocity):
+    """Eq. (1) over S steps from X^0 = noise; returns (X^S, [v_0 .. v_{S-1}])."""
+    S = cfg.S if S is None else S
+    tau = schedule(S)
+    x = np.asarray(noise, dtype=F64)
+    vs = []
+    for k in range(S):
+        v = vel(x, tau[k], Kc, Vc, w, cfg)
+        vs.append(v)
+        x = x + (tau[k + 1] - tau[k]) * v
+    return x, np.stack(vs)
+
+
+def denoise_recompute(noise, Z, w: dict, cfg, S: int | None = None):
+    """Eq. (1) with the conditioning K/V recomputed inside every solver step
+    (the baseline that the prefix cache removes, §III-B Eq. (3))."""
+    S = cfg.S if S is None else S
+    tau = schedule(S)
+    x = np.asarray(noise, dtype=F64)
+    vs = []
+    for k in range(S):
+        Kc, Vc = prefix_kv(Z, w, cfg)
+        v = velocity(x, tau[k], Kc, Vc, w, cfg)
+        vs.append(v)
+        x = x + (tau[k + 1] - tau[k]) * v
+    return x, np.stack(vs)
+
+
+# ----------------------------------------------------------------------------
+# Ternary weights, int8 activations, §III-D Eq. (4) (IEEE fp32, exact ints)
+# ----------------------------------------------------------------------------
+
+def quantize_rows(x):
+    """alpha_m = max(|x_m|_inf, 1e-5) / 127; a = clip(round_half_even(x / alpha), -128, 127).
+
+    fp32 throughout: the division is the correctly rounded fp32 quotient
+    (never a reciprocal multiply).  Returns (int8 codes, fp32 alpha).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1)
+    alpha = (np.maximum(amax, np.float32(1e-5)) / np.float32(127.0)).astype(np.float32)
+    idx = np.rint(x / alpha[..., None])
+    a = np.clip(idx, -128, 127).astype(np.int8)
+    return a, alpha
+
+
+def pack_ternary(q):
+    """q in {-1,0,1} [.., K] -> uint8 [.., K/4]; code q+1 at bits 2*(j mod 4)."""
+    q = np.asarray(q, dtype=np.int16)
+    K = q.shape[-1]
+    assert K % 4 == 0
+    c = (q + 1).astype(np.uint8).reshape(q.shape[:-1] + (K // 4, 4))
+    out = np.zeros(q.shape[:-1] + (K // 4,), dtype=np.uint8)
+    for i in range(4):
+        out |= (c[..., i] << np.uint8(2 * i)).astype(np.uint8)
+    return out
+
+
+def unpack_ternary(packed, K: int | None = None):
+    """uint8 [.., K/4] -> int8 q [.., K]; code 3 is not a valid ternary code."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    parts = [(packed >> np.uint8(2 * i)) & np.uint8(3) for i in range(4)]
+    codes = np.stack(parts, axis=-1).reshape(packed.shape[:-1] + (packed.shape[-1] * 4,))
+    if K is not None:
+        assert codes.shape[-1] == K
+    if np.any(codes == 3):
+        raise ValueError("invalid 2-bit ternary code 3")
+    return codes.astype(np.int8) - np.int8(1)
+
+
+def bf16_rne(x):
+    """Round fp32 to the nearest bfloat16 value, ties to even (fp32 container)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep = u >> np.uint64(16)
+    rest = u & np.uint64(0xFFFF)
+    up = (rest > 0x8000) | ((rest == 0x8000) & ((keep & np.uint64(1)) == 1))
+    keep = keep + up.astype(np.uint64)
+    return (keep << np.uint64(16)).astype(np.uint32).view(np.float32)
+
+
+def ternary_linear(a, alpha, packed, beta):
+    """y_mn = alpha_m beta sum_j a_mj q_nj; returns (bf16-rounded y as fp32, int64 acc).
+
+    a int8 [M, K], alpha fp32 [M], packed uint8 [N, K/4], beta fp32 scalar.
+    The integer dot products are formed with fp64 products and sums of
+    integers below 2^53, which are exact, then checked to be integral.
+    """
+    a = np.asarray(a)
+    q = unpack_ternary(packed, a.shape[-1])
+    acc64 = a.astype(F64) @ q.astype(F64).T
+    acc = acc64.astype(np.int64)
+    assert np.array_equal(acc.astype(F64), acc64)
+    assert np.all(np.abs(acc) < (1 << 24))
+    y = (acc.astype(np.float32) * np.asarray(alpha, dtype=np.float32)[:, None]) * np.float32(beta)
+    return bf16_rne(y), acc
+
+
+def velocity_w2a8(x, tau, Kc, Vc, w: dict, cfg, taps=None):
+    """The velocity network with the six per-layer maps replaced by Eq. (4)."""
+    mods = time_conditioning(w, cfg, tau)
+
+    def lin(u, name, l):
+        # One quantisation of the GEMM input per call; Q, K and V see the
+        # same codes because the quantiser is a deterministic function of u.
+        shp = u.shape
+        a, alpha = quantize_rows(np.asarray(u, dtype=F64).reshape(-1, shp[-1]).astype(np.float32))
+        y, _ = ternary_linear(a, alpha, w[name][l], w["beta_" + name][l])
+        return y.astype(F64).reshape(shp[:-1] + (y.shape[-1],))
+
+    return _expert(x, mods, Kc, Vc, w, cfg, lin, taps)
+
+
+def denoise_w2a8(noise, Kc, Vc, w: dict, cfg, S: int | None = None):
+    return denoise(noise, Kc, Vc, w, cfg, S, vel=velocity_w2a8)
+
+
+# ----------------------------------------------------------------------------
+# Parity metrics, §III-E Eq. (5)
+# ----------------------------------------------------------------------------
+
+def parity_metrics(A, Ahat) -> dict:
+    """e_inf = max_i |A_i - Ahat_i|; e_rel = |A - Ahat|_2 / |Ahat|_2 over the
+    flattened tensors; when |Ahat|_2 = 0 the relative error is undefined and
+    the absolute |A - Ahat|_2 is reported instead (e_rel = None)."""
+    A = np.asarray(A, dtype=F64).ravel()
+    Ahat = np.asarray(Ahat, dtype=F64).ravel()
+    d = A - Ahat
+    e_inf = float(np.max(np.abs(d))) if d.size else 0.0
+    n_ref = float(np.linalg.norm(Ahat))
+    n_d = float(np.linalg.norm(d))
+    if n_ref == 0.0:
+        return {"e_inf": e_inf, "e_rel": None, "e_abs": n_d}
+    return {"e_inf": e_inf, "e_rel": n_d / n_ref, "e_abs": n_d}
