@@ -1,0 +1,361 @@
+#!/usr/bin/env python
+"""Benchmark of the prefix-cached flow-matching action expert on GB300.
+
+One step = one whole request of the hot path over one batch of synthetic
+input: the prefix K/V cache build (Eq. 2 of "vla.cpp: A Unified Inference
+Runtime for Vision-Language-Action Models", §III-B) followed by the S-step
+Euler solve of the action chunk (Eq. 1, §III-A), i.e. L_model = P + S E of
+Eq. (3).  Metric: action chunks/s (and batch-1 ms per chunk, us per solver
+step, fraction of the HBM roofline for the solver).
+
+Default workload: the full-size bf16 expert at batch 1 (P = 816 prefix tokens
+of width 2048, 18 layers of width 1024, MLP 4096, 8 query / 1 KV heads of
+size 256, H = 50 actions x 32 dims, S = 10 steps).
+
+Multi-GPU: observations are independent, so N ranks run N replicas with no
+collective on the data path (weak scaling); the only collectives are the
+timing barrier and the max over ranks.
+
+`--impl reference` times the CPU oracle (fp64 numpy, the parity reference)
+on the host cores on the same workload, one chunk per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import CONFIGS, make_observations, make_weights  # noqa: E402
+
+METRIC = "action chunks/s & batch-1 ms per chunk; per-step µs and % of HBM/tensor roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _lib_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "prefix_cached_flow_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile(workload: str):
+    """DRAM bytes per solver launch from the committed ncu summary, if it was
+    taken on the current sources (else None)."""
+    p = os.path.join(ROOT, "profiles", f"solver_{workload}_traffic.txt")
+    try:
+        kv = {}
+        with open(p) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("library_sources_sha256_16") != _lib_hash():
+            return None
+        return float(kv["dram_bytes_per_solver_launch"])
+    except Exception:
+        return None
+
+
+def algorithmic_bytes_per_step(cfg) -> float:
+    """Bytes one Euler step must move at least: every token-dependent weight
+    once plus the K/V cache once (activations and the time table excluded)."""
+    wb = 2 if cfg.dtype == "bf16" else 4
+    if cfg.w2a8:
+        per_layer = ((cfg.qdim + 2 * cfg.kvdim) * cfg.D + cfg.D * cfg.qdim + 2 * cfg.D * cfg.F) // 4
+        weights = cfg.L * per_layer + 2 * cfg.D * cfg.d_a * 2
+    else:
+        weights = cfg.token_dependent_params() * wb
+    kv = 2 * cfg.L * cfg.B * cfg.n_kv * cfg.P * cfg.d_h * wb
+    return float(weights + kv)
+
+
+def cpu_oracle_chunk(cfg, w, Z, noise):
+    import oracle as O
+    Kc, Vc = O.prefix_kv(Z.astype(np.float64), w, cfg)
+    if cfg.w2a8:
+        return O.denoise_w2a8(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
+    return O.denoise(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
+
+
+def cpu_baseline(cfg, w, Z, noise, budget_s=10.0):
+    """Oracle throughput on the host cores on a bounded sample: whole chunks
+    of observation 0, repeated until ~budget_s of CPU work."""
+    c1 = cfg.replace(B=1)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        cpu_oracle_chunk(c1, w, Z[:1], noise[:1])
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    mean = sum(times) / len(times)
+    return {"value": 1.0 / mean, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(times)} whole chunk(s) (prefix K/V + {cfg.S} Euler steps) of observation 0 of "
+                      f"{cfg.name}, fp64 numpy/OpenBLAS, {mean * 1e3:.0f} ms per chunk"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    cfg = CONFIGS[args.workload]
+    w = make_weights(cfg)
+    if cfg.w2a8:
+        import oracle as O
+        w = O.with_unpacked(w)
+    Z, noise = make_observations(cfg, 1)
+    c1 = cfg.replace(B=1)
+    for _ in range(args.warmup):
+        cpu_oracle_chunk(c1, w, Z, noise)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_chunk(c1, w, Z, noise)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 1.0 / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "B": 1, "P": cfg.P, "S": cfg.S, "note": "one observation per step"},
+        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.steps} whole chunks of observation 0 of {cfg.name} (prefix K/V + "
+                                   f"{cfg.S} Euler steps), fp64 numpy/OpenBLAS"},
+        "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import prefix_cached_flow_gb300 as V
+
+    ws, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if not os.path.exists(V.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    cfg = CONFIGS[args.workload]
+    B = cfg.B
+    w = make_weights(cfg)
+    Z, noise = make_observations(cfg.replace(seed=cfg.seed + 1000 * rank), B)
+    ex = V.Expert(cfg, V.upload_weights(w, cfg.dtype, cfg.w2a8), max_batch=B, max_prefix=cfg.P)
+    dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    Zt = torch.from_numpy(Z).to(dt).cuda()
+    nt = torch.from_numpy(noise).cuda()
+    act = torch.empty_like(nt)
+    Kc, Vc = ex.alloc_cache(B, cfg.P)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ex.prefix_kv_build(Zt, Kc, Vc)
+        ex.denoise(Kc, Vc, nt, act)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert ex.poll_status() == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.random_(0, 255)  # L2 flush between timed steps (outside the events)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        ex.prefix_kv_build(Zt, Kc, Vc)
+        e1.record(stream)
+        ex.denoise(Kc, Vc, nt, act)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = ex.poll_status()
+    prefix_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    denoise_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    step_ms = prefix_ms + denoise_ms
+    if dist:
+        t = torch.tensor([step_ms, prefix_ms, denoise_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, prefix_ms, denoise_ms = t.tolist()
+
+    # End to end through the public host-buffer call: H2D of Z and noise, the
+    # whole request, D2H of the chunk, every step.
+    Zh = torch.from_numpy(Z).to(dt).pin_memory()
+    nh = torch.from_numpy(noise).pin_memory()
+    ah = torch.empty_like(nh).pin_memory()
+    for _ in range(3):
+        ex.policy_step_host(Zh, nh, ah)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ex.policy_step_host(Zh, nh, ah)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+
+    hbm, tflops, src = _peaks()
+    solver_bytes = cfg.S * algorithmic_bytes_per_step(cfg)
+    achieved = solver_bytes / (denoise_ms * 1e-3) / 1e9
+    traffic = _traffic_from_profile(cfg.name)
+    launches = args.steps * (1 + ex.launch_count(B, cfg.P))
+    line = {
+        "metric": METRIC,
+        "value": ws * B / (step_ms * 1e-3),
+        "unit": "chunks/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "B": B, "P": cfg.P, "S": cfg.S, "L": cfg.L, "D": cfg.D, "F": cfg.F,
+                   "heads": f"{cfg.n_q}q/{cfg.n_kv}kv x {cfg.d_h}", "H": cfg.H, "d_a": cfg.d_a,
+                   "d_vlm": cfg.d_vlm, "global_batch": ws * B, "parallelism": f"replicas x{ws}",
+                   "l2": "flushed (256 MiB write) between timed steps"},
+        "ms_per_chunk": step_ms / 1.0,
+        "prefix_build_ms": prefix_ms,
+        "denoise_ms": denoise_ms,
+        "us_per_solver_step": denoise_ms * 1e3 / cfg.S,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "solver launch (one CUDA graph of all S steps)",
+                     "algorithmic_bytes_per_launch": solver_bytes, "peak_source": src},
+        "e2e": {"value": ws * B / (e2e_ms * 1e-3), "unit": "chunks/s",
+                "h2d_bytes_per_step": int(Zh.numel() * Zh.element_size() + nh.numel() * 4),
+                "d2h_bytes_per_step": int(ah.numel() * 4)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, w, Z, noise)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ex.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full_bf16_b1", choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

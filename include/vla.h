@@ -1,0 +1,230 @@
+/*
+ * vla.h - C ABI of libvla, the GB300 (sm_103a) library for the hot path of
+ * flow-matching vision-language-action inference with a prefix K/V cache.
+ *
+ * Source of the operations: "vla.cpp: A Unified Inference Runtime for
+ * Vision-Language-Action Models":
+ *   - §III-A, Eq. (1): Euler integration of an action chunk
+ *       X^{k+1} = X^k + (tau_{k+1} - tau_k) v(X^k, tau_k, C)
+ *     from noise X^0 in R^{H x d_a} over T solver steps (here n_steps = S).
+ *   - §III-B, Eq. (2): the observation prefix Z is projected once per
+ *     observation into per-layer keys/values K_C = Z W_K, V_C = Z W_V, reused
+ *     by every solver step (cache lifecycle: refreshed per observation, reused
+ *     within a request); the action tokens attend to [K_C ; own keys] with
+ *     softmax(Q K^T / sqrt(d_k) + M) V (joint attention, M = 0 here).
+ *   - §III-D, Eq. (4): ternary weights (four 2-bit codes per byte, one fp32
+ *     scale per tensor) with per-row int8 activations, 32-bit integer
+ *     accumulation and bf16 output.
+ *   - §III-C: requests carry inputs and optional noise; responses carry the
+ *     action chunk and its dimensions, or an error.
+ *
+ * Conventions for every call:
+ *   - Pointers named *_dev are DEVICE pointers owned by the caller; the
+ *     library never frees them.  Pointers named *_host are host pointers.
+ *     Every tensor pointer must be 16-byte aligned.
+ *   - Weights are stored out-major: a map R^in -> R^out is [out][in] with
+ *     `in` contiguous (y = x W^T).  Stacked per-layer weights are [L][out][in].
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work on it and return without synchronising
+ *     unless stated otherwise.
+ *   - Argument and shape errors are returned synchronously before anything is
+ *     enqueued.  Errors raised on the device (a bounded wait that timed out)
+ *     are latched in the handle and returned by vla_expert_poll_status().
+ *   - A handle is not re-entrant: one call in flight per handle.
+ */
+#ifndef VLA_H_
+#define VLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VLA_OK = 0,
+  VLA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad enum, B or P out of range */
+  VLA_ERR_SHAPE = 2,        /* inconsistent dimensions */
+  VLA_ERR_UNSUPPORTED = 3,  /* valid but not implemented (e.g. K not a multiple of 64 for bf16) */
+  VLA_ERR_OOM = 4,          /* device allocation failed */
+  VLA_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  VLA_ERR_TIMEOUT = 6,      /* a device-side bounded wait gave up (latched) */
+  VLA_ERR_ABORTED = 7,      /* a kernel saw the handle's abort flag (latched) */
+  VLA_ERR_NO_DEVICE = 8     /* no usable sm_103 device */
+} vla_status;
+
+typedef enum { VLA_DTYPE_F32 = 0, VLA_DTYPE_BF16 = 1 } vla_dtype;
+
+/* Diagnostic flags for vla_expert_config.flags. */
+#define VLA_FLAG_SIMT_GEMM 1u  /* run bf16 GEMMs on the CUDA-core kernel instead of tcgen05 */
+#define VLA_FLAG_NO_GRAPH 2u   /* enqueue the solver kernels directly instead of one graph launch */
+
+typedef struct {
+  int n_layers;    /* L */
+  int width;       /* D, expert hidden width */
+  int mlp_width;   /* F */
+  int n_q_heads;   /* n_q */
+  int n_kv_heads;  /* n_kv; n_q % n_kv == 0, query head j reads K/V head j / (n_q / n_kv) */
+  int head_dim;    /* d_h (= d_k of Eq. 2) */
+  int vlm_hidden;  /* d_vlm, width of the prefix hidden states Z */
+  int action_dim;  /* d_a */
+  int horizon;     /* H, actions per chunk */
+  int time_dim;    /* d_t, sinusoidal time embedding width (even) */
+  int max_batch;   /* largest B any call will use; sizes the workspace */
+  int max_prefix;  /* largest P any call will use */
+  int dtype;       /* vla_dtype of weights, Z and the K/V cache (W2A8: BF16) */
+  float rms_eps;   /* RMSNorm epsilon (1e-6) */
+  unsigned flags;  /* VLA_FLAG_* (0 for normal use) */
+} vla_expert_config;
+
+/* Dense weights, device pointers of the config dtype, shapes [..][out][in]. */
+typedef struct {
+  const void* wk_pre;  /* [L][n_kv*d_h][d_vlm]  W_K of Eq. 2, per layer */
+  const void* wv_pre;  /* [L][n_kv*d_h][d_vlm]  W_V of Eq. 2, per layer */
+  const void* wq;      /* [L][n_q*d_h][D] */
+  const void* wk;      /* [L][n_kv*d_h][D]   action-token keys */
+  const void* wv;      /* [L][n_kv*d_h][D]   action-token values */
+  const void* wo;      /* [L][D][n_q*d_h] */
+  const void* wup;     /* [L][F][D] */
+  const void* wdown;   /* [L][D][F] */
+  const void* wmod;    /* [L][4D][D]  -> (gamma_a, beta_a, gamma_m, beta_m) */
+  const void* win;     /* [D][d_a]    action in-projection */
+  const void* wout;    /* [d_a][D]    velocity projection */
+  const void* wt1;     /* [D][d_t]    time MLP, first map */
+  const void* wt2;     /* [D][D]      time MLP, second map */
+  const void* wmod_f;  /* [2D][D]     -> (gamma_f, beta_f) of the final norm */
+} vla_expert_weights;
+
+/* W2A8 weights: the six per-layer maps W_q, W_k, W_v, W_o, W_up, W_down are
+ * ternary, packed uint8 [L][out][in/4] (code q+1 of input index j at bits
+ * 2*(j mod 4) of byte j/4; code 3 is invalid), each with an fp32 scale per
+ * layer (device pointer to [L] floats).  Everything else is bf16. */
+typedef struct {
+  const void* wk_pre;
+  const void* wv_pre;
+  const uint8_t* wq;
+  const uint8_t* wk;
+  const uint8_t* wv;
+  const uint8_t* wo;
+  const uint8_t* wup;
+  const uint8_t* wdown;
+  const float* beta_wq;
+  const float* beta_wk;
+  const float* beta_wv;
+  const float* beta_wo;
+  const float* beta_wup;
+  const float* beta_wdown;
+  const void* wmod;
+  const void* win;
+  const void* wout;
+  const void* wt1;
+  const void* wt2;
+  const void* wmod_f;
+} vla_expert_weights_w2a8;
+
+typedef struct vla_expert vla_expert;
+
+/* Create an expert handle for a fixed solver length n_steps = S with the
+ * uniform schedule tau_k = k / S (integration 0 -> 1, dt = 1/S).
+ * Copies and repacks the weights into handle-owned device memory (the caller
+ * may free its copies once the call returns), precomputes the time
+ * conditioning table for every tau_k, and allocates the workspace for
+ * max_batch x horizon action tokens, so that no later call allocates (except
+ * the first vla_policy_step_host, see there).  Synchronises `stream`.
+ * Returns VLA_ERR_INVALID_ARG / VLA_ERR_SHAPE / VLA_ERR_UNSUPPORTED for bad
+ * configs, VLA_ERR_OOM, VLA_ERR_CUDA, VLA_ERR_NO_DEVICE. */
+vla_status vla_expert_create(const vla_expert_config* cfg, const vla_expert_weights* w,
+                             int n_steps, void* stream, vla_expert** out);
+
+/* Same for the W2A8 variant (cfg->dtype must be VLA_DTYPE_BF16).  A packed
+ * byte holding code 3 is rejected with VLA_ERR_INVALID_ARG. */
+vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert_weights_w2a8* w,
+                                  int n_steps, void* stream, vla_expert** out);
+
+/* Synchronises the device and frees everything the handle owns.  NULL is a no-op. */
+void vla_expert_destroy(vla_expert* h);
+
+/* Bytes of ONE of the two cache tensors K_C, V_C for (B, P):
+ * L * B * n_kv * P * d_h * sizeof(dtype). */
+vla_status vla_prefix_cache_bytes(const vla_expert* h, int B, int P, size_t* bytes_per_tensor);
+
+/* Eq. 2, once per observation: K_C^l = Z W_K^l, V_C^l = Z W_V^l for every layer.
+ *   Z_dev   [B][P][d_vlm]            config dtype, read only
+ *   Kc_dev  [L][B][n_kv][P][d_h]     config dtype, written
+ *   Vc_dev  [L][B][n_kv][P][d_h]     config dtype, written
+ * 1 <= B <= max_batch, 1 <= P <= max_prefix.  No mask and no positions enter
+ * the projection.  Enqueues one kernel. */
+vla_status vla_prefix_kv_build(vla_expert* h, const void* Z_dev, int B, int P,
+                               void* Kc_dev, void* Vc_dev, void* stream);
+
+/* Eq. 1 over S solver steps, reusing the cache of vla_prefix_kv_build.
+ *   Kc_dev, Vc_dev   the cache for the same (B, P), read only
+ *   noise_dev        [B][H][d_a] fp32, X^0 (required; NULL -> VLA_ERR_INVALID_ARG)
+ *   actions_dev      [B][H][d_a] fp32, receives X^S (may alias noise_dev)
+ *   vel_tap_dev      NULL or [S][B][H][d_a] fp32, receives every v_k
+ * Every step evaluates the velocity network (time-modulated RMSNorm, joint
+ * GQA attention over [K_C ; action keys], GeLU MLP, velocity projection) and
+ * applies x <- x + dt v.  The S-step loop is one CUDA-graph launch (built on
+ * the first call for a given (B, P, pointers) and reused afterwards). */
+vla_status vla_action_denoise(vla_expert* h, const void* Kc_dev, const void* Vc_dev, int B, int P,
+                              const float* noise_dev, float* actions_dev, float* vel_tap_dev,
+                              void* stream);
+
+/* The same solver with the W2A8 maps (handle from vla_expert_create_w2a8);
+ * every ternary map quantises its input rows per Eq. 4 first. */
+vla_status vla_action_denoise_w2a8(vla_expert* h, const void* Kc_dev, const void* Vc_dev, int B,
+                                   int P, const float* noise_dev, float* actions_dev,
+                                   float* vel_tap_dev, void* stream);
+
+/* One whole request from host memory: copies Z and the noise to the device,
+ * builds the prefix cache, runs the solver and copies X^S back, then
+ * synchronises `stream`.  Z_host [B][P][d_vlm] (config dtype), noise_host and
+ * actions_host [B][H][d_a] fp32; pinned host memory gives asynchronous
+ * copies.  The first call allocates handle-owned device buffers for
+ * max_batch x max_prefix (kept until destroy); later calls allocate nothing. */
+vla_status vla_policy_step_host(vla_expert* h, const void* Z_host, int B, int P,
+                                const float* noise_host, float* actions_host, void* stream);
+
+/* Synchronises `stream` and returns the first error latched on the device
+ * since the last poll (VLA_ERR_TIMEOUT, VLA_ERR_ABORTED) or VLA_OK; clears it. */
+vla_status vla_expert_poll_status(vla_expert* h, void* stream);
+
+/* Sets (1) or clears (0) the handle's abort flag.  Kernels that see it set
+ * skip their work and latch VLA_ERR_ABORTED.  Host-mapped, takes effect for
+ * kernels that start after the write. */
+vla_status vla_expert_set_abort(vla_expert* h, int abort);
+
+/* Eq. 4, first line, as a standalone op (the same kernel the W2A8 solver uses):
+ *   x_dev     [M][K] fp32 rows
+ *   a_dev     [M][K] int8 out: clip(round_half_even(x / alpha_m), -128, 127)
+ *   alpha_dev [M] fp32 out: max(|x_m|_inf, 1e-5) / 127 (IEEE division)
+ * M >= 1, 1 <= K <= 65536. */
+vla_status vla_w2a8_quantize_rows(const float* x_dev, int M, int K, int8_t* a_dev,
+                                  float* alpha_dev, void* stream);
+
+/* Eq. 4, second line, as a standalone op:
+ *   a_dev      [M][K] int8, alpha_dev [M] fp32
+ *   q_dev      [N][K/4] packed ternary codes (as in vla_expert_weights_w2a8)
+ *   beta       per-tensor fp32 scale
+ *   y_dev      [M][N] bf16 (raw uint16 bits) out: bf16_rne((float(acc) * alpha_m) * beta)
+ *   acc_dev    NULL or [M][N] int32 out: acc_mn = sum_j a_mj q_nj (exact)
+ * K must be a multiple of 64.  Codes are assumed valid (3 is not checked here). */
+vla_status vla_w2a8_ternary_gemm(const int8_t* a_dev, const float* alpha_dev, const uint8_t* q_dev,
+                                 float beta, int M, int N, int K, uint16_t* y_dev,
+                                 int32_t* acc_dev, void* stream);
+
+/* Number of kernels one denoise call launches for batch B and prefix P
+ * (all of them inside the one graph launch).  Host-only arithmetic. */
+vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kernels);
+
+/* Human-readable name of a status. */
+const char* vla_status_string(vla_status s);
+
+/* Library version, e.g. "0.1.0". */
+const char* vla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VLA_H_ */

@@ -61,7 +61,7 @@ __all__ = [
     "sinusoidal_time_embedding", "silu", "gelu", "rmsnorm_modulate", "linear",
     "time_conditioning", "prefix_kv", "joint_attention", "velocity", "schedule",
     "denoise", "denoise_recompute", "quantize_rows", "pack_ternary",
-    "unpack_ternary", "bf16_rne", "ternary_linear", "velocity_w2a8",
+    "unpack_ternary", "bf16_rne", "ternary_linear", "velocity_w2a8", "with_unpacked",
     "denoise_w2a8", "parity_metrics",
 ]
 
@@ -282,15 +282,17 @@ def bf16_rne(x):
     return (keep << np.uint64(16)).astype(np.uint32).view(np.float32)
 
 
-def ternary_linear(a, alpha, packed, beta):
+def ternary_linear(a, alpha, packed, beta, q=None):
     """y_mn = alpha_m beta sum_j a_mj q_nj; returns (bf16-rounded y as fp32, int64 acc).
 
-    a int8 [M, K], alpha fp32 [M], packed uint8 [N, K/4], beta fp32 scalar.
+    a int8 [M, K], alpha fp32 [M], packed uint8 [N, K/4], beta fp32 scalar;
+    q optionally the already unpacked int8 [N, K] (same values, saves decoding).
     The integer dot products are formed with fp64 products and sums of
     integers below 2^53, which are exact, then checked to be integral.
     """
     a = np.asarray(a)
-    q = unpack_ternary(packed, a.shape[-1])
+    if q is None:
+        q = unpack_ternary(packed, a.shape[-1])
     acc64 = a.astype(F64) @ q.astype(F64).T
     acc = acc64.astype(np.int64)
     assert np.array_equal(acc.astype(F64), acc64)
@@ -308,10 +310,21 @@ def velocity_w2a8(x, tau, Kc, Vc, w: dict, cfg, taps=None):
         # same codes because the quantiser is a deterministic function of u.
         shp = u.shape
         a, alpha = quantize_rows(np.asarray(u, dtype=F64).reshape(-1, shp[-1]).astype(np.float32))
-        y, _ = ternary_linear(a, alpha, w[name][l], w["beta_" + name][l])
+        q = w["q_" + name][l] if ("q_" + name) in w else None
+        y, _ = ternary_linear(a, alpha, w[name][l], w["beta_" + name][l], q)
         return y.astype(F64).reshape(shp[:-1] + (y.shape[-1],))
 
     return _expert(x, mods, Kc, Vc, w, cfg, lin, taps)
+
+
+def with_unpacked(w: dict) -> dict:
+    """Copy of a W2A8 weight dict with every ternary map also stored
+    unpacked (int8, key "q_<name>") so that repeated calls skip decoding."""
+    out = dict(w)
+    for name in ("wq", "wk", "wv", "wo", "wup", "wdown"):
+        if name in w and w[name].dtype == np.uint8:
+            out["q_" + name] = unpack_ternary(w[name])
+    return out
 
 
 def denoise_w2a8(noise, Kc, Vc, w: dict, cfg, S: int | None = None):

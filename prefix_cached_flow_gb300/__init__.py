@@ -1,0 +1,7 @@
+"""GB300 (sm_103a) library for the prefix-cached flow-matching action expert.
+
+The compute lives in libvla.so (include/vla.h); this package is its thin
+Python binding plus the in-tree build step.
+"""
+from .binding import (DTYPE_BF16, DTYPE_F32, EXPORTED, FLAG_NO_GRAPH, FLAG_SIMT_GEMM, LIB_PATH, Expert,  # noqa: F401
+                      VlaError, lib, quantize_rows, ternary_gemm, upload_weights)

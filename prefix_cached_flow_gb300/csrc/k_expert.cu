@@ -1,0 +1,444 @@
+// Per-token kernels of the action expert's solver step.
+//
+// One velocity evaluation v(X^k, tau_k, C) ("vla.cpp: A Unified Inference
+// Runtime for Vision-Language-Action Models", §III-A Eq. (1)) runs, per layer:
+//   GEMM qkv -> reduce_qkv -> attention (split over key chunks) -> combine
+//   GEMM o   -> reduce_norm (residual, MLP norm)
+//   GEMM up  -> reduce_gelu
+//   GEMM down-> reduce_norm (residual, next layer's attention norm) | head
+// The GEMMs (k_gemm_tc.cu / k_gemm_simt.cu) write fp32 split-K partials; the
+// kernels here reduce them in a fixed order (deterministic), fuse the
+// epilogue (residual add, time-modulated RMSNorm, exact GeLU, the W2A8 output
+// scaling of Eq. (4)) and emit the next GEMM's input (bf16 / fp32, or the
+// Eq. (4) int8 codes for the W2A8 variant).  Attention is Eq. (2) with the
+// action tokens' own keys/values appended to the cached prefix ones.
+#include <math.h>
+
+#include "vla_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------------------
+// Time conditioning table (built once per handle; tau_k = k / S)
+// ---------------------------------------------------------------------------
+__global__ void k_time_embed(float* e, int S, int d_t) {
+  const int k = blockIdx.x;
+  const int half = d_t / 2;
+  const double tau = (double)k / (double)S;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const double omega = pow(10000.0, -(double)i / (double)half);
+    const double arg = 1000.0 * tau * omega;
+    e[(size_t)k * d_t + i] = (float)sin(arg);
+    e[(size_t)k * d_t + half + i] = (float)cos(arg);
+  }
+}
+
+__global__ void k_silu(float* x, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    x[i] = v / (1.f + expf(-v));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared epilogue: modulated RMSNorm of a row in shared memory, emitted as
+// the next GEMM's input (TU) or, for W2A8, quantised per Eq. (4).
+// ---------------------------------------------------------------------------
+template <typename TU>
+__device__ void emit_modnorm(const ExpertDims& d, const StepBufs& b, float* row, const float* gamma,
+                             const float* beta, int t, float* red) {
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) ss += row[i] * row[i];
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / (float)d.D + d.eps);
+  if (!d.w2a8) {
+    TU* out = (TU*)b.act + (size_t)t * d.D;
+    for (int i = threadIdx.x; i < d.D; i += blockDim.x) out[i] = from_f<TU>(row[i] * r * (1.f + gamma[i]) + beta[i]);
+  } else {
+    for (int i = threadIdx.x; i < d.D; i += blockDim.x) row[i] = row[i] * r * (1.f + gamma[i]) + beta[i];
+    __syncthreads();
+    const float alpha = quantize_row_block(row, d.D, b.codes + (size_t)t * d.D, nullptr, red);
+    if (threadIdx.x == 0) b.alpha[t] = alpha;
+  }
+}
+
+__device__ __forceinline__ const float* mod_ptr(const ExpertDims& d, const StepBufs& b, int step, int layer,
+                                                int which) {
+  // modtab [S][L][4][D]: which = 0 gamma_a, 1 beta_a, 2 gamma_m, 3 beta_m
+  return b.modtab + (((size_t)step * d.L + layer) * 4 + which) * d.D;
+}
+
+// h = x W_in^T; u = modnorm(h) with layer 0's attention modulation.
+template <typename TU>
+__global__ void k_embed_norm(ExpertDims d, StepBufs b, int step, const float* x_in, DevCtl ctl) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* xs = sm + d.D;
+  float* red = xs + d.d_a;
+  const int t = blockIdx.x;
+  if (t == 0 && threadIdx.x == 0 && ctl.abort && *ctl.abort) latch_error(ctl.status, VLA_DEV_ABORTED);
+  for (int j = threadIdx.x; j < d.d_a; j += blockDim.x) xs[j] = x_in[(size_t)t * d.d_a + j];
+  __syncthreads();
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+    const float* w = b.win + (size_t)i * d.d_a;
+    float acc = 0.f;
+    for (int j = 0; j < d.d_a; ++j) acc += xs[j] * w[j];
+    row[i] = acc;
+    b.h[(size_t)t * d.D + i] = acc;
+  }
+  __syncthreads();
+  emit_modnorm<TU>(d, b, row, mod_ptr(d, b, step, 0, 0), mod_ptr(d, b, step, 0, 1), t, red);
+}
+
+// Sum the QKV split-K partials and scatter q / k_s / v_s into the
+// per-(observation, head) layouts the attention kernel reads.
+template <typename TQ>
+__global__ void k_reduce_qkv(ExpertDims d, StepBufs b, int layer, int splits) {
+  const int t = blockIdx.x;
+  const int T = d.B * d.H;
+  const int bb = t / d.H, i = t - bb * d.H;
+  const int N = d.qkvdim;
+  TQ* q = (TQ*)b.q;
+  TQ* ks = (TQ*)b.ks;
+  TQ* vs = (TQ*)b.vs;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += b.part[((size_t)z * T + t) * N + n];
+    const int slot = n < d.qdim ? 0 : (n < d.qdim + d.kvdim ? 1 : 2);
+    if (d.w2a8) s = w2a8_scale(s, b.alpha[t], b.beta[layer * 6 + slot]);
+    if (slot == 0) {
+      const int j = n / d.d_h, e = n - j * d.d_h;
+      q[(((size_t)bb * d.n_q + j) * d.H + i) * d.d_h + e] = from_f<TQ>(s);
+    } else {
+      const int nn = n - d.qdim - (slot == 2 ? d.kvdim : 0);
+      const int g = nn / d.d_h, e = nn - g * d.d_h;
+      TQ* dst = slot == 1 ? ks : vs;
+      dst[(((size_t)bb * d.n_kv + g) * d.H + i) * d.d_h + e] = from_f<TQ>(s);
+    }
+  }
+}
+
+// Eq. (2) over one chunk of the joint key list [prefix P ; suffix H] for one
+// (observation, query head): unnormalised partial output, row max and sum.
+template <typename TC, typename TQ>
+__global__ void k_attn_part(ExpertDims d, StepBufs b, const TC* Kc, const TC* Vc) {
+  extern __shared__ float sm[];
+  const int H = d.H, dh = d.d_h, chunk = b.attn_chunk;
+  float* qs = sm;                     // [H][dh], pre-scaled by 1/sqrt(d_h)
+  float* Ks = qs + H * dh;            // [chunk][dh+1]
+  float* Vs = Ks + chunk * (dh + 1);  // [chunk][dh]
+  float* S = Vs + chunk * dh;         // [H][chunk]
+  const int c = blockIdx.x, j = blockIdx.y, bb = blockIdx.z;
+  const int g = j / (d.n_q / d.n_kv);
+  const int nkeys = d.P + H;
+  const int k0 = c * chunk;
+  const int nk = min(chunk, nkeys - k0);
+  const float scale = rsqrtf((float)dh);
+  const TQ* qg = (const TQ*)b.q + ((size_t)bb * d.n_q + j) * H * dh;
+  for (int idx = threadIdx.x; idx < H * dh; idx += blockDim.x) qs[idx] = to_f(qg[idx]) * scale;
+  const TQ* ksg = (const TQ*)b.ks + ((size_t)bb * d.n_kv + g) * H * dh;
+  const TQ* vsg = (const TQ*)b.vs + ((size_t)bb * d.n_kv + g) * H * dh;
+  const TC* Kg = Kc + ((size_t)bb * d.n_kv + g) * d.P * dh;
+  const TC* Vg = Vc + ((size_t)bb * d.n_kv + g) * d.P * dh;
+  for (int idx = threadIdx.x; idx < nk * dh; idx += blockDim.x) {
+    const int r = idx / dh, e = idx - r * dh;
+    const int kk = k0 + r;
+    float kv, vv;
+    if (kk < d.P) {
+      kv = to_f(Kg[(size_t)kk * dh + e]);
+      vv = to_f(Vg[(size_t)kk * dh + e]);
+    } else {
+      kv = to_f(ksg[(size_t)(kk - d.P) * dh + e]);
+      vv = to_f(vsg[(size_t)(kk - d.P) * dh + e]);
+    }
+    Ks[r * (dh + 1) + e] = kv;
+    Vs[r * dh + e] = vv;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < H * nk; idx += blockDim.x) {
+    const int t = idx / nk, r = idx - t * nk;
+    const float* qr = qs + t * dh;
+    const float* kr = Ks + r * (dh + 1);
+    float s = 0.f;
+    for (int e = 0; e < dh; ++e) s += qr[e] * kr[e];
+    S[t * chunk + r] = s;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float* ml = b.ml + (((size_t)bb * d.n_q + j) * b.n_chunks + c) * H * 2;
+  for (int t = wid; t < H; t += nw) {
+    float m = -INFINITY;
+    for (int r = lane; r < nk; r += 32) m = fmaxf(m, S[t * chunk + r]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int r = lane; r < nk; r += 32) {
+      const float p = expf(S[t * chunk + r] - m);
+      S[t * chunk + r] = p;
+      l += p;
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      ml[t * 2 + 0] = m;
+      ml[t * 2 + 1] = l;
+    }
+  }
+  __syncthreads();
+  float* op = b.opart + (((size_t)bb * d.n_q + j) * b.n_chunks + c) * H * dh;
+  for (int idx = threadIdx.x; idx < H * dh; idx += blockDim.x) {
+    const int t = idx / dh, e = idx - t * dh;
+    const float* pr = S + t * chunk;
+    float o = 0.f;
+    for (int r = 0; r < nk; ++r) o += pr[r] * Vs[r * dh + e];
+    op[idx] = o;
+  }
+}
+
+// Merge the key-chunk partials of every head for one action token and emit
+// the O-projection input row [n_q * d_h].
+template <typename TU>
+__global__ void k_attn_combine(ExpertDims d, StepBufs b) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + d.qdim;
+  const int i = blockIdx.x, bb = blockIdx.y;
+  const int t = bb * d.H + i;
+  const int nc = b.n_chunks, H = d.H, dh = d.d_h;
+  for (int idx = threadIdx.x; idx < d.qdim; idx += blockDim.x) {
+    const int j = idx / dh, e = idx - j * dh;
+    const size_t base = ((size_t)bb * d.n_q + j) * nc;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, b.ml[((base + c) * H + i) * 2]);
+    float num = 0.f, den = 0.f;
+    for (int c = 0; c < nc; ++c) {
+      const float* mlc = b.ml + ((base + c) * H + i) * 2;
+      const float w = expf(mlc[0] - M);
+      num += w * b.opart[((base + c) * H + i) * dh + e];
+      den += w * mlc[1];
+    }
+    const float o = num / den;
+    if (!d.w2a8)
+      ((TU*)b.act)[(size_t)t * d.qdim + idx] = from_f<TU>(o);
+    else
+      row[idx] = o;
+  }
+  if (d.w2a8) {
+    __syncthreads();
+    const float alpha = quantize_row_block(row, d.qdim, b.codes + (size_t)t * d.qdim, nullptr, red);
+    if (threadIdx.x == 0) b.alpha[t] = alpha;
+  }
+}
+
+// h += sum_z part (W2A8: Eq. (4) output scaling first), then the modulated
+// RMSNorm selected by (mod_layer, mod_half) emits the next GEMM input.
+template <typename TU>
+__global__ void k_reduce_norm(ExpertDims d, StepBufs b, int step, int beta_layer, int beta_slot, int mod_layer,
+                              int mod_half, int splits) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + d.D;
+  const int t = blockIdx.x;
+  const int T = d.B * d.H;
+  const float alpha = d.w2a8 ? b.alpha[t] : 0.f;
+  const float beta = d.w2a8 ? b.beta[beta_layer * 6 + beta_slot] : 0.f;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += b.part[((size_t)z * T + t) * d.D + i];
+    if (d.w2a8) s = w2a8_scale(s, alpha, beta);
+    const float hv = b.h[(size_t)t * d.D + i] + s;
+    b.h[(size_t)t * d.D + i] = hv;
+    row[i] = hv;
+  }
+  __syncthreads();
+  emit_modnorm<TU>(d, b, row, mod_ptr(d, b, step, mod_layer, 2 * mod_half),
+                   mod_ptr(d, b, step, mod_layer, 2 * mod_half + 1), t, red);
+}
+
+// g = GeLU(sum_z part) (W2A8: GeLU of the Eq. (4) bf16 output, then quantise).
+template <typename TU>
+__global__ void k_reduce_gelu(ExpertDims d, StepBufs b, int layer, int splits) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + d.F;
+  const int t = blockIdx.x;
+  const int T = d.B * d.H;
+  const float alpha = d.w2a8 ? b.alpha[t] : 0.f;
+  const float beta = d.w2a8 ? b.beta[layer * 6 + 4] : 0.f;
+  for (int n = threadIdx.x; n < d.F; n += blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += b.part[((size_t)z * T + t) * d.F + n];
+    if (d.w2a8) s = w2a8_scale(s, alpha, beta);
+    const float g = gelu_exact(s);
+    if (!d.w2a8)
+      ((TU*)b.act)[(size_t)t * d.F + n] = from_f<TU>(g);
+    else
+      row[n] = g;
+  }
+  if (d.w2a8) {
+    __syncthreads();
+    const float a = quantize_row_block(row, d.F, b.codes + (size_t)t * d.F, nullptr, red);
+    if (threadIdx.x == 0) b.alpha[t] = a;
+  }
+}
+
+// Last layer's residual, final modulated RMSNorm, velocity projection and
+// the Euler update x <- x + dt v (Eq. (1)); optional velocity tap.
+__global__ void k_head(ExpertDims d, StepBufs b, int step, int splits, float dt, const float* x_in, float* x_out,
+                       float* tap) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + d.D;
+  const int t = blockIdx.x;
+  const int T = d.B * d.H;
+  const float alpha = d.w2a8 ? b.alpha[t] : 0.f;
+  const float beta = d.w2a8 ? b.beta[(d.L - 1) * 6 + 5] : 0.f;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += b.part[((size_t)z * T + t) * d.D + i];
+    if (d.w2a8) s = w2a8_scale(s, alpha, beta);
+    const float hv = b.h[(size_t)t * d.D + i] + s;
+    row[i] = hv;
+    ss += hv * hv;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / (float)d.D + d.eps);
+  const float* gf = b.modf + (size_t)step * 2 * d.D;
+  const float* bf = gf + d.D;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) row[i] = row[i] * r * (1.f + gf[i]) + bf[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int a = wid; a < d.d_a; a += nw) {
+    const float* w = b.wout + (size_t)a * d.D;
+    float acc = 0.f;
+    for (int i = lane; i < d.D; i += 32) acc += row[i] * w[i];
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      const size_t o = (size_t)t * d.d_a + a;
+      x_out[o] = fmaf(dt, acc, x_in[o]);
+      if (tap) tap[(size_t)step * T * d.d_a + o] = acc;
+    }
+  }
+}
+
+template <typename TS>
+__global__ void k_to_f32(const TS* src, float* dst, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = to_f(src[i]);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+cudaError_t expert_kernels_init() {
+  cudaError_t e = cudaFuncSetAttribute(k_attn_part<float, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       227 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_attn_part<bf16, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_reduce_gelu<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_reduce_gelu<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_attn_combine<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_attn_combine<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, cudaStream_t st) {
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  if (src_bf16)
+    k_to_f32<bf16><<<blocks, 256, 0, st>>>((const bf16*)src, dst, n);
+  else
+    k_to_f32<float><<<blocks, 256, 0, st>>>((const float*)src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st) {
+  k_time_embed<<<S, 128, 0, st>>>(e, S, d_t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu(float* x, size_t n, cudaStream_t st) {
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  k_silu<<<blocks, 256, 0, st>>>(x, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed_norm(const ExpertDims& d, const StepBufs& b, int step, const float* x_in, DevCtl ctl,
+                              cudaStream_t st) {
+  const size_t smem = (size_t)(d.D + d.d_a + 32) * sizeof(float);
+  const int T = d.B * d.H;
+  if (d.f32)
+    k_embed_norm<float><<<T, kThreads, smem, st>>>(d, b, step, x_in, ctl);
+  else
+    k_embed_norm<bf16><<<T, kThreads, smem, st>>>(d, b, step, x_in, ctl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_qkv(const ExpertDims& d, const StepBufs& b, int layer, int splits, cudaStream_t st) {
+  const int T = d.B * d.H;
+  if (d.f32)
+    k_reduce_qkv<float><<<T, kThreads, 0, st>>>(d, b, layer, splits);
+  else
+    k_reduce_qkv<bf16><<<T, kThreads, 0, st>>>(d, b, layer, splits);
+  return cudaGetLastError();
+}
+
+size_t attention_smem_bytes(const ExpertDims& d, int chunk) {
+  return (size_t)(d.H * d.d_h + chunk * (2 * d.d_h + 1) + d.H * chunk) * sizeof(float);
+}
+
+cudaError_t launch_attention(const ExpertDims& d, const StepBufs& b, int layer, const void* kc, const void* vc,
+                             cudaStream_t st) {
+  const size_t layer_elems = (size_t)d.B * d.n_kv * d.P * d.d_h;
+  const size_t smem = attention_smem_bytes(d, b.attn_chunk);
+  dim3 grid(b.n_chunks, d.n_q, d.B);
+  if (d.f32)
+    k_attn_part<float, float><<<grid, kThreads, smem, st>>>(d, b, (const float*)kc + layer * layer_elems,
+                                                          (const float*)vc + layer * layer_elems);
+  else
+    k_attn_part<bf16, bf16><<<grid, kThreads, smem, st>>>(d, b, (const bf16*)kc + layer * layer_elems,
+                                                        (const bf16*)vc + layer * layer_elems);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem2 = (size_t)(d.qdim + 32) * sizeof(float);
+  dim3 grid2(d.H, d.B);
+  if (d.f32)
+    k_attn_combine<float><<<grid2, kThreads, smem2, st>>>(d, b);
+  else
+    k_attn_combine<bf16><<<grid2, kThreads, smem2, st>>>(d, b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_norm(const ExpertDims& d, const StepBufs& b, int step, int beta_layer, int beta_slot,
+                               int mod_layer, int mod_half, int splits, cudaStream_t st) {
+  const int T = d.B * d.H;
+  const size_t smem = (size_t)(d.D + 32) * sizeof(float);
+  if (d.f32)
+    k_reduce_norm<float><<<T, kThreads, smem, st>>>(d, b, step, beta_layer, beta_slot, mod_layer, mod_half, splits);
+  else
+    k_reduce_norm<bf16><<<T, kThreads, smem, st>>>(d, b, step, beta_layer, beta_slot, mod_layer, mod_half, splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_gelu(const ExpertDims& d, const StepBufs& b, int layer, int splits, cudaStream_t st) {
+  const int T = d.B * d.H;
+  const size_t smem = (size_t)(d.F + 32) * sizeof(float);
+  if (d.f32)
+    k_reduce_gelu<float><<<T, kThreads, smem, st>>>(d, b, layer, splits);
+  else
+    k_reduce_gelu<bf16><<<T, kThreads, smem, st>>>(d, b, layer, splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head(const ExpertDims& d, const StepBufs& b, int step, int splits, float dt, const float* x_in,
+                        float* x_out, float* tap, cudaStream_t st) {
+  const int T = d.B * d.H;
+  const size_t smem = (size_t)(d.D + 32) * sizeof(float);
+  k_head<<<T, kThreads, smem, st>>>(d, b, step, splits, dt, x_in, x_out, tap);
+  return cudaGetLastError();
+}

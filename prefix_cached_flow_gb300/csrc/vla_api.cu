@@ -1,0 +1,698 @@
+// libvla C ABI: handle life cycle, argument validation, weight repacking,
+// the per-handle time-conditioning table, split-K planning and the solver
+// loop (captured once per shape/pointer set into a CUDA graph and replayed).
+//
+// The call structure follows "vla.cpp: A Unified Inference Runtime for
+// Vision-Language-Action Models": the prefix K/V cache is built once per
+// observation (§III-B Eq. (2)) and reused by all S Euler steps of the action
+// expert (§III-A Eq. (1)); for unchanged shapes the graph and buffers persist
+// across calls (§III-B, latency model Eq. (3)).
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "vla_common.cuh"
+
+namespace {
+
+struct GraphEntry {
+  int B, P;
+  const void* kc;
+  const void* vc;
+  const float* noise;
+  float* actions;
+  float* tap;
+  cudaGraphExec_t exec;
+  uint64_t last_use;
+};
+
+constexpr int kMaxGraphs = 8;
+
+struct GemmPlan {
+  int splits = 1;
+  int kb_per_split = 1;
+  int BN = 16;
+  int tiles_n = 1;
+  int tiles_t = 1;
+  int stages = 4;
+};
+
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+int round_up(int a, int b) { return cdiv(a, b) * b; }
+
+}  // namespace
+
+struct vla_expert {
+  vla_expert_config cfg{};
+  int S = 0;
+  bool w2a8 = false;
+  bool f32 = false;
+  bool use_tc = false;
+  int num_sms = 0;
+  size_t es = 2;
+  int qdim = 0, kvdim = 0, qkvdim = 0, Kmax = 0;
+  // handle-owned weights
+  void* wkv_pre = nullptr;  // [L*2*kvdim][d_vlm]: per layer K rows then V rows
+  void* wqkv = nullptr;     // [L][qkvdim][D]  (W2A8: packed [L][qkvdim][D/4])
+  void* wo = nullptr;       // [L][D][qdim]
+  void* wup = nullptr;      // [L][F][D]
+  void* wdown = nullptr;    // [L][D][F]
+  float* beta = nullptr;    // [L][6] (W2A8)
+  float* win = nullptr;     // [D][d_a]
+  float* wout = nullptr;    // [d_a][D]
+  float* modtab = nullptr;  // [S][L][4][D]
+  float* modf = nullptr;    // [S][2][D]
+  // workspace for max_batch x H tokens
+  float* h = nullptr;
+  void* act = nullptr;
+  int8_t* codes = nullptr;
+  float* alpha = nullptr;
+  float* part = nullptr;
+  size_t part_elems = 0;
+  void* q = nullptr;
+  void* ks = nullptr;
+  void* vs = nullptr;
+  float* opart = nullptr;
+  float* ml = nullptr;
+  int attn_chunk = 0;
+  int* d_status = nullptr;
+  int* h_abort = nullptr;
+  int* d_abort = nullptr;
+  CUtensorMap tm_wkv, tm_wqkv, tm_wo, tm_wup, tm_wdown;
+  cudaStream_t cap_stream = nullptr;
+  std::vector<GraphEntry> graphs;
+  uint64_t tick = 0;
+  // request buffers (vla_policy_step_host), allocated on first use
+  void* req_z = nullptr;
+  void* req_kc = nullptr;
+  void* req_vc = nullptr;
+  float* req_noise = nullptr;
+  float* req_act = nullptr;
+};
+
+namespace {
+
+vla_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return VLA_OK;
+  if (e == cudaErrorMemoryAllocation) return VLA_ERR_OOM;
+  return VLA_ERR_CUDA;
+}
+
+#define VLA_CK(expr)                                   \
+  do {                                                 \
+    cudaError_t _e = (expr);                           \
+    if (_e != cudaSuccess) return cuda_status(_e);     \
+  } while (0)
+
+template <typename T>
+vla_status dalloc(T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc((void**)p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return VLA_ERR_OOM;
+  }
+  return VLA_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+GemmPlan plan_gemm(const vla_expert* h, int N, int K, int T) {
+  GemmPlan p;
+  if (h->use_tc && !h->w2a8) {
+    p.BN = T >= 256 ? 256 : round_up(T < 16 ? 16 : T, 16);
+    p.tiles_n = cdiv(N, 128);
+    p.tiles_t = cdiv(T, p.BN);
+    const int num_kb = K / 64;
+    const int tiles = p.tiles_n * p.tiles_t;
+    int s = h->num_sms / tiles;
+    if (s < 1) s = 1;
+    if (s > num_kb) s = num_kb;
+    p.kb_per_split = cdiv(num_kb, s);
+    p.splits = cdiv(num_kb, p.kb_per_split);
+    const int stage = 128 * 128 + p.BN * 128;
+    int st = (220 * 1024) / stage;
+    if (st > 8) st = 8;
+    if (st > p.kb_per_split) st = p.kb_per_split < 2 ? 2 : p.kb_per_split;
+    p.stages = st;
+  } else {
+    const int tiles = cdiv(T, 64) * cdiv(N, 64);
+    const int align = h->w2a8 ? 64 : 32;
+    int s = h->num_sms / tiles;
+    if (s < 1) s = 1;
+    if (s > K / align) s = K / align > 0 ? K / align : 1;
+    p.splits = simt_effective_splits(K, s, align);
+  }
+  return p;
+}
+
+void gemm_dims(const vla_expert* h, int which, int* N, int* K) {
+  const int D = h->cfg.width, F = h->cfg.mlp_width;
+  switch (which) {
+    case 0: *N = h->qkvdim; *K = D; break;
+    case 1: *N = D; *K = h->qdim; break;
+    case 2: *N = F; *K = D; break;
+    default: *N = D; *K = F; break;
+  }
+}
+
+ExpertDims make_dims(const vla_expert* h, int B, int P) {
+  ExpertDims d;
+  const vla_expert_config& c = h->cfg;
+  d.L = c.n_layers; d.D = c.width; d.F = c.mlp_width; d.n_q = c.n_q_heads; d.n_kv = c.n_kv_heads;
+  d.d_h = c.head_dim; d.d_a = c.action_dim; d.H = c.horizon; d.B = B; d.P = P; d.S = h->S; d.d_t = c.time_dim;
+  d.eps = c.rms_eps; d.qdim = h->qdim; d.kvdim = h->kvdim; d.qkvdim = h->qkvdim;
+  d.f32 = h->f32 ? 1 : 0;
+  d.w2a8 = h->w2a8 ? 1 : 0;
+  return d;
+}
+
+StepBufs make_bufs(const vla_expert* h, int P) {
+  StepBufs b;
+  b.win = h->win; b.wout = h->wout; b.modtab = h->modtab; b.modf = h->modf; b.beta = h->beta;
+  b.h = h->h; b.act = h->act; b.codes = h->codes; b.alpha = h->alpha; b.part = h->part;
+  b.q = h->q; b.ks = h->ks; b.vs = h->vs; b.opart = h->opart; b.ml = h->ml;
+  b.attn_chunk = h->attn_chunk;
+  b.n_chunks = cdiv(P + h->cfg.horizon, h->attn_chunk);
+  return b;
+}
+
+cudaError_t run_linear(vla_expert* h, int which, int layer, int T, const GemmPlan& p, const CUtensorMap* tmX,
+                       cudaStream_t st) {
+  int N, K;
+  gemm_dims(h, which, &N, &K);
+  const void* wbase = which == 0 ? h->wqkv : which == 1 ? h->wo : which == 2 ? h->wup : h->wdown;
+  const size_t sstride = (size_t)T * N;
+  if (h->w2a8) {
+    const uint8_t* q = (const uint8_t*)wbase + (size_t)layer * N * (K / 4);
+    return launch_ternary_simt(h->codes, K, q, T, N, K, p.splits, h->part, sstride, N, st);
+  }
+  if (!h->use_tc) {
+    const void* W = (const char*)wbase + (size_t)layer * N * K * h->es;
+    return launch_gemm_simt(!h->f32, h->act, K, !h->f32, W, K, T, N, K, p.splits, h->part, sstride, N, nullptr,
+                            st);
+  }
+  const CUtensorMap* tmW = which == 0 ? &h->tm_wqkv : which == 1 ? &h->tm_wo : which == 2 ? &h->tm_wup : &h->tm_wdown;
+  TcGemmArgs a{};
+  a.N = N; a.T = T; a.a_row0 = layer * N; a.num_kb = K / 64; a.kb_per_split = p.kb_per_split; a.BN = p.BN;
+  a.stages = p.stages; a.out = h->part; a.split_stride = sstride; a.ldo = N; a.mode = 0; a.status = h->d_status;
+  return launch_gemm_tc(tmW, tmX, a, p.tiles_n, p.tiles_t, p.splits, st);
+}
+
+vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B, int P, const float* noise,
+                           float* actions, float* tap, cudaStream_t st) {
+  const vla_expert_config& c = h->cfg;
+  const ExpertDims d = make_dims(h, B, P);
+  const StepBufs sb = make_bufs(h, P);
+  const int T = B * c.horizon;
+  GemmPlan pl[4];
+  for (int w = 0; w < 4; ++w) {
+    int N, K;
+    gemm_dims(h, w, &N, &K);
+    pl[w] = plan_gemm(h, N, K, T);
+  }
+  CUtensorMap tmX[3];  // activations [T][K] for K = D, qdim, F
+  if (h->use_tc && !h->w2a8) {
+    const int ks[3] = {c.width, h->qdim, c.mlp_width};
+    for (int i = 0; i < 3; ++i)
+      if (tc_encode_2d_bf16(&tmX[i], h->act, ks[i], T, 64, pl[0].BN) != 0) return VLA_ERR_CUDA;
+  }
+  const CUtensorMap* xmap[4] = {&tmX[0], &tmX[1], &tmX[0], &tmX[2]};
+  const DevCtl ctl{h->d_status, h->d_abort};
+  for (int k = 0; k < h->S; ++k) {
+    const float* x_in = k == 0 ? noise : actions;
+    const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    VLA_CK(launch_embed_norm(d, sb, k, x_in, ctl, st));
+    for (int l = 0; l < c.n_layers; ++l) {
+      VLA_CK(run_linear(h, 0, l, T, pl[0], xmap[0], st));
+      VLA_CK(launch_reduce_qkv(d, sb, l, pl[0].splits, st));
+      VLA_CK(launch_attention(d, sb, l, kc, vc, st));
+      VLA_CK(run_linear(h, 1, l, T, pl[1], xmap[1], st));
+      VLA_CK(launch_reduce_norm(d, sb, k, l, 3, l, 1, pl[1].splits, st));
+      VLA_CK(run_linear(h, 2, l, T, pl[2], xmap[2], st));
+      VLA_CK(launch_reduce_gelu(d, sb, l, pl[2].splits, st));
+      VLA_CK(run_linear(h, 3, l, T, pl[3], xmap[3], st));
+      if (l + 1 < c.n_layers)
+        VLA_CK(launch_reduce_norm(d, sb, k, l, 5, l + 1, 0, pl[3].splits, st));
+      else
+        VLA_CK(launch_head(d, sb, k, pl[3].splits, dt, x_in, actions, tap, st));
+    }
+  }
+  return VLA_OK;
+}
+
+vla_status validate_config(const vla_expert_config* c, int n_steps, bool w2a8) {
+  if (!c || n_steps < 1) return VLA_ERR_INVALID_ARG;
+  if (c->n_layers < 1 || c->width < 1 || c->mlp_width < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
+      c->head_dim < 1 || c->vlm_hidden < 1 || c->action_dim < 1 || c->horizon < 1 || c->time_dim < 2 ||
+      c->max_batch < 1 || c->max_prefix < 1 || !(c->rms_eps > 0.f))
+    return VLA_ERR_INVALID_ARG;
+  if (c->dtype != VLA_DTYPE_F32 && c->dtype != VLA_DTYPE_BF16) return VLA_ERR_INVALID_ARG;
+  if (c->n_q_heads % c->n_kv_heads != 0 || c->time_dim % 2 != 0) return VLA_ERR_SHAPE;
+  if (w2a8 && c->dtype != VLA_DTYPE_BF16) return VLA_ERR_INVALID_ARG;
+  const int qdim = c->n_q_heads * c->head_dim;
+  if (c->dtype == VLA_DTYPE_BF16 &&
+      (c->width % 64 || c->mlp_width % 64 || qdim % 64 || c->vlm_hidden % 64))
+    return VLA_ERR_UNSUPPORTED;
+  if (c->action_dim > 1024 || c->width > 16384 || c->mlp_width > 32768 || qdim > 16384) return VLA_ERR_UNSUPPORTED;
+  return VLA_OK;
+}
+
+vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, cudaStream_t st, vla_expert** out) {
+  vla_status s = validate_config(cfg, n_steps, w2a8);
+  if (s != VLA_OK) return s;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return VLA_ERR_NO_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return VLA_ERR_NO_DEVICE;
+  if (prop.major != 10 || prop.minor != 3) return VLA_ERR_NO_DEVICE;
+  vla_expert* h = new (std::nothrow) vla_expert();
+  if (!h) return VLA_ERR_OOM;
+  h->cfg = *cfg;
+  h->S = n_steps;
+  h->w2a8 = w2a8;
+  h->f32 = cfg->dtype == VLA_DTYPE_F32;
+  h->es = h->f32 ? 4 : 2;
+  h->use_tc = !h->f32 && !(cfg->flags & VLA_FLAG_SIMT_GEMM);
+  h->num_sms = prop.multiProcessorCount;
+  h->qdim = cfg->n_q_heads * cfg->head_dim;
+  h->kvdim = cfg->n_kv_heads * cfg->head_dim;
+  h->qkvdim = h->qdim + 2 * h->kvdim;
+  h->Kmax = cfg->width;
+  if (cfg->mlp_width > h->Kmax) h->Kmax = cfg->mlp_width;
+  if (h->qdim > h->Kmax) h->Kmax = h->qdim;
+  *out = h;
+  cudaError_t e = simt_kernels_init();
+  if (e == cudaSuccess) e = tc_kernels_init();
+  if (e == cudaSuccess) e = expert_kernels_init();
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  (void)st;
+  return cuda_status(e);
+}
+
+// Shared tail of create: time table, fp32 in/out maps, workspace, tensor maps.
+vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const void* wmod, const void* wmod_f,
+                         const void* win, const void* wout, cudaStream_t st) {
+  const vla_expert_config& c = h->cfg;
+  const int L = c.n_layers, D = c.width, S = h->S, d_t = c.time_dim;
+  const int wb = h->f32 ? 0 : 1;
+  vla_status s;
+  // fp32 copies of the tiny in/out projections
+  if ((s = dalloc(&h->win, (size_t)D * c.action_dim * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&h->wout, (size_t)D * c.action_dim * 4)) != VLA_OK) return s;
+  VLA_CK(launch_to_f32(win, wb, h->win, (size_t)D * c.action_dim, st));
+  VLA_CK(launch_to_f32(wout, wb, h->wout, (size_t)D * c.action_dim, st));
+  // time conditioning table for tau_k = k / S
+  float *e = nullptr, *c1 = nullptr, *cc = nullptr;
+  if ((s = dalloc(&e, (size_t)S * d_t * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&c1, (size_t)S * D * 4)) != VLA_OK) { cudaFree(e); return s; }
+  if ((s = dalloc(&cc, (size_t)S * D * 4)) != VLA_OK) { cudaFree(e); cudaFree(c1); return s; }
+  if ((s = dalloc(&h->modtab, (size_t)S * L * 4 * D * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&h->modf, (size_t)S * 2 * D * 4)) != VLA_OK) return s;
+  cudaError_t err = launch_time_embed(e, S, d_t, st);
+  if (err == cudaSuccess) err = launch_gemm_simt(0, e, d_t, wb, wt1, d_t, S, D, d_t, 1, c1, 0, D, nullptr, st);
+  if (err == cudaSuccess) err = launch_silu(c1, (size_t)S * D, st);
+  if (err == cudaSuccess) err = launch_gemm_simt(0, c1, D, wb, wt2, D, S, D, D, 1, cc, 0, D, nullptr, st);
+  if (err == cudaSuccess) err = launch_silu(cc, (size_t)S * D, st);
+  if (err == cudaSuccess)
+    err = launch_gemm_simt(0, cc, D, wb, wmod, D, S, L * 4 * D, D, 1, h->modtab, 0, L * 4 * D, nullptr, st);
+  if (err == cudaSuccess)
+    err = launch_gemm_simt(0, cc, D, wb, wmod_f, D, S, 2 * D, D, 1, h->modf, 0, 2 * D, nullptr, st);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+  cudaFree(e);
+  cudaFree(c1);
+  cudaFree(cc);
+  VLA_CK(err);
+  // workspace
+  const int Tm = c.max_batch * c.horizon;
+  const size_t ae = h->f32 ? 4 : 2;
+  if ((s = dalloc(&h->h, (size_t)Tm * D * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&h->act, (size_t)Tm * h->Kmax * ae)) != VLA_OK) return s;
+  if (h->w2a8) {
+    if ((s = dalloc(&h->codes, (size_t)Tm * h->Kmax)) != VLA_OK) return s;
+  }
+  if ((s = dalloc(&h->alpha, (size_t)Tm * 4)) != VLA_OK) return s;
+  size_t pe = 0;
+  for (int B = 1; B <= c.max_batch; ++B) {
+    const int T = B * c.horizon;
+    for (int w = 0; w < 4; ++w) {
+      int N, K;
+      gemm_dims(h, w, &N, &K);
+      const GemmPlan p = plan_gemm(h, N, K, T);
+      const size_t need = (size_t)p.splits * T * N;
+      if (need > pe) pe = need;
+    }
+  }
+  h->part_elems = pe;
+  if ((s = dalloc(&h->part, pe * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&h->q, (size_t)Tm * h->qdim * ae)) != VLA_OK) return s;
+  if ((s = dalloc(&h->ks, (size_t)Tm * h->kvdim * ae)) != VLA_OK) return s;
+  if ((s = dalloc(&h->vs, (size_t)Tm * h->kvdim * ae)) != VLA_OK) return s;
+  // attention key-chunk size: largest multiple of 16 (<= 128) whose staging fits
+  ExpertDims dd = make_dims(h, 1, c.max_prefix);
+  int chunk = 128;
+  while (chunk > 16 && attention_smem_bytes(dd, chunk) > 200 * 1024) chunk -= 16;
+  if (attention_smem_bytes(dd, chunk) > 220 * 1024) return VLA_ERR_UNSUPPORTED;
+  h->attn_chunk = chunk;
+  const int max_chunks = cdiv(c.max_prefix + c.horizon, chunk);
+  if ((s = dalloc(&h->opart, (size_t)Tm * c.n_q_heads * max_chunks * c.head_dim * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&h->ml, (size_t)Tm * c.n_q_heads * max_chunks * 2 * 4)) != VLA_OK) return s;
+  if ((s = dalloc(&h->d_status, 16)) != VLA_OK) return s;
+  VLA_CK(cudaMemset(h->d_status, 0, 16));
+  VLA_CK(cudaHostAlloc((void**)&h->h_abort, sizeof(int), cudaHostAllocMapped));
+  *h->h_abort = 0;
+  VLA_CK(cudaHostGetDevicePointer((void**)&h->d_abort, h->h_abort, 0));
+  // TMA descriptors of the bf16 weights
+  if (!h->f32) {
+    const int N_kv = L * 2 * h->kvdim;
+    if (tc_encode_2d_bf16(&h->tm_wkv, h->wkv_pre, c.vlm_hidden, N_kv, 64, 128)) return VLA_ERR_CUDA;
+    if (!h->w2a8) {
+      if (tc_encode_2d_bf16(&h->tm_wqkv, h->wqkv, D, (uint64_t)L * h->qkvdim, 64, 128)) return VLA_ERR_CUDA;
+      if (tc_encode_2d_bf16(&h->tm_wo, h->wo, h->qdim, (uint64_t)L * D, 64, 128)) return VLA_ERR_CUDA;
+      if (tc_encode_2d_bf16(&h->tm_wup, h->wup, D, (uint64_t)L * c.mlp_width, 64, 128)) return VLA_ERR_CUDA;
+      if (tc_encode_2d_bf16(&h->tm_wdown, h->wdown, c.mlp_width, (uint64_t)L * D, 64, 128)) return VLA_ERR_CUDA;
+    }
+  }
+  VLA_CK(cudaStreamSynchronize(st));
+  return VLA_OK;
+}
+
+// dst[l] = [src_a[l]; src_b[l]; (src_c[l])]: stacks per-layer row blocks.
+cudaError_t stack_rows(void* dst, size_t dst_pitch, const void* src, size_t rows_bytes, int L, size_t offset,
+                       cudaStream_t st) {
+  return cudaMemcpy2DAsync((char*)dst + offset, dst_pitch, src, rows_bytes, rows_bytes, L, cudaMemcpyDeviceToDevice,
+                           st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vla_status_string(vla_status s) {
+  switch (s) {
+    case VLA_OK: return "ok";
+    case VLA_ERR_INVALID_ARG: return "invalid argument";
+    case VLA_ERR_SHAPE: return "inconsistent shape";
+    case VLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VLA_ERR_OOM: return "out of device memory";
+    case VLA_ERR_CUDA: return "CUDA runtime error";
+    case VLA_ERR_TIMEOUT: return "device wait timed out";
+    case VLA_ERR_ABORTED: return "aborted";
+    case VLA_ERR_NO_DEVICE: return "no sm_103 device";
+  }
+  return "unknown status";
+}
+
+const char* vla_version(void) { return "0.1.0"; }
+
+void vla_expert_destroy(vla_expert* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  void* ptrs[] = {h->wkv_pre, h->wqkv, h->wo,   h->wup,   h->wdown, h->beta,  h->win,     h->wout,
+                  h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
+                  h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
+                  h->req_noise, h->req_act};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  if (h->h_abort) cudaFreeHost(h->h_abort);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  delete h;
+}
+
+vla_status vla_expert_create(const vla_expert_config* cfg, const vla_expert_weights* w, int n_steps, void* stream,
+                             vla_expert** out) {
+  if (!out || !w) return VLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  const void* ptrs[] = {w->wk_pre, w->wv_pre, w->wq, w->wk, w->wv, w->wo, w->wup, w->wdown,
+                        w->wmod,   w->win,    w->wout, w->wt1, w->wt2, w->wmod_f};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return VLA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  vla_expert* h = nullptr;
+  vla_status s = create_common(cfg, n_steps, false, st, &h);
+  if (s != VLA_OK) {
+    vla_expert_destroy(h);
+    return s;
+  }
+  const vla_expert_config& c = *cfg;
+  const int L = c.n_layers, D = c.width, F = c.mlp_width;
+  const size_t es = h->es;
+  const size_t kvb = (size_t)h->kvdim * c.vlm_hidden * es;
+  const size_t qb = (size_t)h->qdim * D * es, kb = (size_t)h->kvdim * D * es;
+  cudaError_t e = cudaSuccess;
+  if ((s = dalloc(&h->wkv_pre, 2 * kvb * L)) != VLA_OK || (s = dalloc(&h->wqkv, (qb + 2 * kb) * L)) != VLA_OK ||
+      (s = dalloc(&h->wo, (size_t)D * h->qdim * es * L)) != VLA_OK ||
+      (s = dalloc(&h->wup, (size_t)F * D * es * L)) != VLA_OK ||
+      (s = dalloc(&h->wdown, (size_t)D * F * es * L)) != VLA_OK) {
+    vla_expert_destroy(h);
+    return s;
+  }
+  e = stack_rows(h->wkv_pre, 2 * kvb, w->wk_pre, kvb, L, 0, st);
+  if (e == cudaSuccess) e = stack_rows(h->wkv_pre, 2 * kvb, w->wv_pre, kvb, L, kvb, st);
+  if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wq, qb, L, 0, st);
+  if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wk, kb, L, qb, st);
+  if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wv, kb, L, qb + kb, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->wo, w->wo, (size_t)D * h->qdim * es * L, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->wup, w->wup, (size_t)F * D * es * L, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->wdown, w->wdown, (size_t)D * F * es * L, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) {
+    vla_expert_destroy(h);
+    return cuda_status(e);
+  }
+  s = finish_create(h, w->wt1, w->wt2, w->wmod, w->wmod_f, w->win, w->wout, st);
+  if (s != VLA_OK) {
+    vla_expert_destroy(h);
+    return s;
+  }
+  *out = h;
+  return VLA_OK;
+}
+
+vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert_weights_w2a8* w, int n_steps,
+                                  void* stream, vla_expert** out) {
+  if (!out || !w) return VLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  const void* ptrs[] = {w->wk_pre, w->wv_pre, w->wq, w->wk, w->wv, w->wo, w->wup, w->wdown, w->beta_wq,
+                        w->beta_wk, w->beta_wv, w->beta_wo, w->beta_wup, w->beta_wdown, w->wmod, w->win,
+                        w->wout, w->wt1, w->wt2, w->wmod_f};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return VLA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  vla_expert* h = nullptr;
+  vla_status s = create_common(cfg, n_steps, true, st, &h);
+  if (s != VLA_OK) {
+    vla_expert_destroy(h);
+    return s;
+  }
+  const vla_expert_config& c = *cfg;
+  const int L = c.n_layers, D = c.width, F = c.mlp_width;
+  const size_t kvb = (size_t)h->kvdim * c.vlm_hidden * 2;
+  const size_t qb = (size_t)h->qdim * (D / 4), kb = (size_t)h->kvdim * (D / 4);
+  const size_t ob = (size_t)D * (h->qdim / 4), ub = (size_t)F * (D / 4), db = (size_t)D * (F / 4);
+  if ((s = dalloc(&h->wkv_pre, 2 * kvb * L)) != VLA_OK || (s = dalloc(&h->wqkv, (qb + 2 * kb) * L)) != VLA_OK ||
+      (s = dalloc(&h->wo, ob * L)) != VLA_OK || (s = dalloc(&h->wup, ub * L)) != VLA_OK ||
+      (s = dalloc(&h->wdown, db * L)) != VLA_OK || (s = dalloc(&h->beta, (size_t)L * 6 * 4)) != VLA_OK) {
+    vla_expert_destroy(h);
+    return s;
+  }
+  cudaError_t e = stack_rows(h->wkv_pre, 2 * kvb, w->wk_pre, kvb, L, 0, st);
+  if (e == cudaSuccess) e = stack_rows(h->wkv_pre, 2 * kvb, w->wv_pre, kvb, L, kvb, st);
+  if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wq, qb, L, 0, st);
+  if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wk, kb, L, qb, st);
+  if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wv, kb, L, qb + kb, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->wo, w->wo, ob * L, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->wup, w->wup, ub * L, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->wdown, w->wdown, db * L, cudaMemcpyDeviceToDevice, st);
+  const float* betas[6] = {w->beta_wq, w->beta_wk, w->beta_wv, w->beta_wo, w->beta_wup, w->beta_wdown};
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+    e = cudaMemcpy2DAsync(h->beta + i, 6 * sizeof(float), betas[i], sizeof(float), sizeof(float), L,
+                          cudaMemcpyDeviceToDevice, st);
+  // reject packed bytes that hold the invalid code 3
+  int* bad = nullptr;
+  if (e == cudaSuccess) e = cudaMalloc((void**)&bad, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), st);
+  const void* packed[4] = {h->wqkv, h->wo, h->wup, h->wdown};
+  const size_t pbytes[4] = {(qb + 2 * kb) * L, ob * L, ub * L, db * L};
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    e = launch_check_ternary_codes((const uint8_t*)packed[i], pbytes[i], bad, st);
+  int hbad = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (bad) cudaFree(bad);
+  if (e != cudaSuccess) {
+    vla_expert_destroy(h);
+    return cuda_status(e);
+  }
+  if (hbad) {
+    vla_expert_destroy(h);
+    return VLA_ERR_INVALID_ARG;
+  }
+  s = finish_create(h, w->wt1, w->wt2, w->wmod, w->wmod_f, w->win, w->wout, st);
+  if (s != VLA_OK) {
+    vla_expert_destroy(h);
+    return s;
+  }
+  *out = h;
+  return VLA_OK;
+}
+
+vla_status vla_prefix_cache_bytes(const vla_expert* h, int B, int P, size_t* bytes) {
+  if (!h || !bytes || B < 1 || P < 1) return VLA_ERR_INVALID_ARG;
+  *bytes = (size_t)h->cfg.n_layers * B * h->cfg.n_kv_heads * P * h->cfg.head_dim * h->es;
+  return VLA_OK;
+}
+
+vla_status vla_prefix_kv_build(vla_expert* h, const void* Z, int B, int P, void* Kc, void* Vc, void* stream) {
+  if (!h || !Z || !Kc || !Vc || !aligned16(Z) || !aligned16(Kc) || !aligned16(Vc)) return VLA_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
+  const vla_expert_config& c = h->cfg;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int BP = B * P, N = c.n_layers * 2 * h->kvdim, K = c.vlm_hidden;
+  KvScatter kv{Kc, Vc, c.n_layers, B, c.n_kv_heads, P, c.head_dim};
+  if (!h->use_tc) {
+    VLA_CK(launch_gemm_simt(!h->f32, Z, K, !h->f32, h->wkv_pre, K, BP, N, K, 1, nullptr, 0, 0, &kv, st));
+    return VLA_OK;
+  }
+  const int BN = BP >= 256 ? 256 : round_up(BP < 16 ? 16 : BP, 16);
+  CUtensorMap tmZ;
+  if (tc_encode_2d_bf16(&tmZ, Z, K, BP, 64, BN)) return VLA_ERR_CUDA;
+  TcGemmArgs a{};
+  a.N = N; a.T = BP; a.a_row0 = 0; a.num_kb = K / 64; a.kb_per_split = a.num_kb; a.BN = BN;
+  const int stage = 128 * 128 + BN * 128;
+  a.stages = (220 * 1024) / stage > 8 ? 8 : (220 * 1024) / stage;
+  a.mode = 1; a.kv = kv; a.status = h->d_status;
+  VLA_CK(launch_gemm_tc(&h->tm_wkv, &tmZ, a, cdiv(N, 128), cdiv(BP, BN), 1, st));
+  return VLA_OK;
+}
+
+static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const void* Vc, int B, int P,
+                               const float* noise, float* actions, float* tap, void* stream) {
+  if (!h || h->w2a8 != w2a8) return VLA_ERR_INVALID_ARG;
+  if (!Kc || !Vc || !noise || !actions || !aligned16(Kc) || !aligned16(Vc) || !aligned16(noise) ||
+      !aligned16(actions) || (tap && !aligned16(tap)))
+    return VLA_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->cfg.flags & VLA_FLAG_NO_GRAPH) return enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, st);
+  GraphEntry* hit = nullptr;
+  for (auto& g : h->graphs)
+    if (g.B == B && g.P == P && g.kc == Kc && g.vc == Vc && g.noise == noise && g.actions == actions && g.tap == tap)
+      hit = &g;
+  if (!hit) {
+    if ((int)h->graphs.size() >= kMaxGraphs) {
+      size_t lru = 0;
+      for (size_t i = 1; i < h->graphs.size(); ++i)
+        if (h->graphs[i].last_use < h->graphs[lru].last_use) lru = i;
+      cudaGraphExecDestroy(h->graphs[lru].exec);
+      h->graphs.erase(h->graphs.begin() + lru);
+    }
+    cudaGraph_t graph = nullptr;
+    VLA_CK(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+    vla_status s = enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, h->cap_stream);
+    cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+    if (s != VLA_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return s;
+    }
+    VLA_CK(e);
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    VLA_CK(e);
+    h->graphs.push_back(GraphEntry{B, P, Kc, Vc, noise, actions, tap, exec, 0});
+    hit = &h->graphs.back();
+  }
+  hit->last_use = ++h->tick;
+  VLA_CK(cudaGraphLaunch(hit->exec, st));
+  return VLA_OK;
+}
+
+vla_status vla_action_denoise(vla_expert* h, const void* Kc, const void* Vc, int B, int P, const float* noise,
+                              float* actions, float* tap, void* stream) {
+  return denoise_impl(h, false, Kc, Vc, B, P, noise, actions, tap, stream);
+}
+
+vla_status vla_action_denoise_w2a8(vla_expert* h, const void* Kc, const void* Vc, int B, int P, const float* noise,
+                                   float* actions, float* tap, void* stream) {
+  return denoise_impl(h, true, Kc, Vc, B, P, noise, actions, tap, stream);
+}
+
+vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kernels) {
+  if (!h || !kernels || B < 1 || P < 1) return VLA_ERR_INVALID_ARG;
+  // per solver step: embed+norm, then per layer 4 GEMMs, reduce_qkv,
+  // attention partials, attention combine, 2 residual/norm reductions (the
+  // last layer's second one is the velocity head) and the GeLU reduction.
+  *kernels = h->S * (1 + 10 * h->cfg.n_layers);
+  return VLA_OK;
+}
+
+vla_status vla_expert_poll_status(vla_expert* h, void* stream) {
+  if (!h) return VLA_ERR_INVALID_ARG;
+  VLA_CK(cudaStreamSynchronize((cudaStream_t)stream));
+  int v = 0;
+  VLA_CK(cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v) VLA_CK(cudaMemset(h->d_status, 0, sizeof(int)));
+  return v == 0 ? VLA_OK : (vla_status)v;
+}
+
+vla_status vla_expert_set_abort(vla_expert* h, int abort) {
+  if (!h || !h->h_abort) return VLA_ERR_INVALID_ARG;
+  *(volatile int*)h->h_abort = abort ? 1 : 0;
+  return VLA_OK;
+}
+
+vla_status vla_policy_step_host(vla_expert* h, const void* Z_host, int B, int P, const float* noise_host,
+                                float* actions_host, void* stream) {
+  if (!h || !Z_host || !noise_host || !actions_host) return VLA_ERR_INVALID_ARG;
+  const vla_expert_config& c = h->cfg;
+  if (B < 1 || B > c.max_batch || P < 1 || P > c.max_prefix) return VLA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  vla_status s;
+  if (!h->req_z) {
+    const size_t cache = (size_t)c.n_layers * c.max_batch * c.n_kv_heads * c.max_prefix * c.head_dim * h->es;
+    if ((s = dalloc(&h->req_z, (size_t)c.max_batch * c.max_prefix * c.vlm_hidden * h->es)) != VLA_OK ||
+        (s = dalloc(&h->req_kc, cache)) != VLA_OK || (s = dalloc(&h->req_vc, cache)) != VLA_OK ||
+        (s = dalloc(&h->req_noise, (size_t)c.max_batch * c.horizon * c.action_dim * 4)) != VLA_OK ||
+        (s = dalloc(&h->req_act, (size_t)c.max_batch * c.horizon * c.action_dim * 4)) != VLA_OK)
+      return s;
+  }
+  const size_t zb = (size_t)B * P * c.vlm_hidden * h->es;
+  const size_t xb = (size_t)B * c.horizon * c.action_dim * 4;
+  VLA_CK(cudaMemcpyAsync(h->req_z, Z_host, zb, cudaMemcpyHostToDevice, st));
+  VLA_CK(cudaMemcpyAsync(h->req_noise, noise_host, xb, cudaMemcpyHostToDevice, st));
+  if ((s = vla_prefix_kv_build(h, h->req_z, B, P, h->req_kc, h->req_vc, stream)) != VLA_OK) return s;
+  if ((s = denoise_impl(h, h->w2a8, h->req_kc, h->req_vc, B, P, h->req_noise, h->req_act, nullptr, stream)) != VLA_OK)
+    return s;
+  VLA_CK(cudaMemcpyAsync(actions_host, h->req_act, xb, cudaMemcpyDeviceToHost, st));
+  return vla_expert_poll_status(h, stream);
+}
+
+vla_status vla_w2a8_quantize_rows(const float* x, int M, int K, int8_t* a, float* alpha, void* stream) {
+  if (!x || !a || !alpha || M < 1 || K < 1 || K > 53248) return VLA_ERR_INVALID_ARG;
+  VLA_CK(launch_quantize_rows(x, M, K, a, alpha, (cudaStream_t)stream));
+  return VLA_OK;
+}
+
+vla_status vla_w2a8_ternary_gemm(const int8_t* a, const float* alpha, const uint8_t* q, float beta, int M, int N,
+                                 int K, uint16_t* y, int32_t* acc, void* stream) {
+  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64) return VLA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  float* part = nullptr;
+  VLA_CK(cudaMallocAsync((void**)&part, (size_t)M * N * sizeof(float), st));
+  cudaError_t e = launch_ternary_simt(a, K, q, M, N, K, 1, part, 0, N, st);
+  if (e == cudaSuccess) e = launch_ternary_finish(part, M, N, alpha, beta, y, acc, st);
+  cudaFreeAsync(part, st);
+  VLA_CK(e);
+  return VLA_OK;
+}
+
+}  // extern "C"

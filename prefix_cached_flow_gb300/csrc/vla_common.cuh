@@ -1,0 +1,373 @@
+// Internal declarations shared by the libvla translation units.
+//
+// Device-side building blocks: hand-written inline PTX for sm_103a (mbarrier,
+// TMA bulk tensor copies, tcgen05 MMA / TMEM), bounded waits that latch an
+// error word instead of spinning forever, block reductions, and the Eq. (4)
+// row quantiser ("vla.cpp: A Unified Inference Runtime for
+// Vision-Language-Action Models", §III-D) that every W2A8 producer shares.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/vla.h"
+
+typedef __nv_bfloat16 bf16;
+
+// Device error word values (the first error is latched).
+#define VLA_DEV_OK 0
+#define VLA_DEV_TIMEOUT 6
+#define VLA_DEV_ABORTED 7
+
+// A bounded wait gives up after this long (ns of %globaltimer).
+#define VLA_WAIT_LIMIT_NS 2000000000ull
+
+// ---------------------------------------------------------------------------
+// Scalar conversions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------
+// Error latch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void latch_error(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// Block reductions (blockDim.x a multiple of 32, <= 1024)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// `scratch` must hold 32 floats; all threads get the result.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  float r = (lane < nw) ? scratch[lane] : 0.f;
+  r = warp_sum(r);
+  return r;
+}
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  float r = (lane < nw) ? scratch[lane] : 0.f;
+  r = warp_max(r);
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Eq. (4), first line, for one row held in shared memory by the whole block:
+//   alpha = max(|x|_inf, 1e-5) / 127   (IEEE round-to-nearest division)
+//   a_j   = clip(rint(x_j / alpha), -128, 127)   (rint: ties to even)
+// Writes int8 codes (codes != nullptr) and/or the same integers as bf16
+// carriers (carriers != nullptr; every |a| <= 128 is exact in bf16).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float quantize_row_block(const float* row, int K, int8_t* codes,
+                                                    bf16* carriers, float* red_scratch) {
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < K; i += blockDim.x) amax = fmaxf(amax, fabsf(row[i]));
+  amax = block_max(amax, red_scratch);
+  const float alpha = __fdiv_rn(fmaxf(amax, 1e-5f), 127.0f);
+  for (int i = threadIdx.x; i < K; i += blockDim.x) {
+    float r = rintf(__fdiv_rn(row[i], alpha));
+    r = fminf(fmaxf(r, -128.f), 127.f);
+    if (codes) codes[i] = (int8_t)(int)r;
+    if (carriers) carriers[i] = __float2bfloat16_rn(r);
+  }
+  return alpha;
+}
+
+// Eq. (4), output line: bf16_rne((float(acc) * alpha) * beta), returned as fp32.
+__device__ __forceinline__ float w2a8_scale(float acc, float alpha, float beta) {
+  return __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(acc, alpha), beta)));
+}
+
+__device__ __forceinline__ float gelu_exact(float x) {
+  return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+}
+
+// ---------------------------------------------------------------------------
+// PTX: shared-memory addresses, mbarriers, TMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  On timeout latches
+// VLA_DEV_TIMEOUT and returns false; also gives up early once another thread
+// has latched an error.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > VLA_WAIT_LIMIT_NS) {
+      latch_error(status, VLA_DEV_TIMEOUT);
+      return false;
+    }
+    if (status && *(volatile int*)status != 0) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+// 2-D tiled TMA load into shared memory, completion via mbarrier tx bytes.
+// x = innermost (contiguous) element coordinate, y = row.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const void* map, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// PTX: tcgen05 (5th-generation tensor cores, accumulators in TMEM)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, cta_group::1.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+// 32 lanes x 32 bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile
+// whose rows are 128 bytes (64 bf16) with the 128-byte swizzle that TMA
+// writes; 8-row core-matrix groups are 1024 bytes apart.  The tile base must
+// be 1024-byte aligned; a K offset inside the row is added to the address.
+__device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)0 << 16;                     // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024u >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                     // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: kind::f16 with bf16 A/B, fp32 D, both K-major.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | (1u << 7)                    // A format: bf16
+         | (1u << 10)                   // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch interfaces (implemented in the kernel translation units)
+// ---------------------------------------------------------------------------
+struct KvScatter {
+  void* kc;
+  void* vc;
+  int L, B, n_kv, P, d_h;
+};
+
+struct DevCtl {
+  int* status;               // latched device error word
+  const volatile int* abort; // host-mapped abort flag (may be null)
+};
+
+// SIMT GEMM: out[z][t][n] = sum_{k in split z} X[t][k] W[n][k] (fp32 partials),
+// or, when kv != nullptr, scatter D into K_C / V_C (1 split).
+cudaError_t launch_gemm_simt(int x_bf16, const void* X, int ldx, int w_bf16, const void* W, int ldw, int T, int N,
+                             int K, int splits, float* out, size_t split_stride, int ldo, const KvScatter* kv,
+                             cudaStream_t st);
+
+// tcgen05 GEMM with both operands K-major bf16 loaded by TMA:
+// D[n][t] = sum_k W[a_row0 + n][k] * X[t][k]; A = weights (M = 128 rows per
+// tile), B = tokens (BN rows per tile, 16 <= BN <= 256, BN % 16 == 0).
+struct TcGemmArgs {
+  int N;            // valid weight rows (output features)
+  int T;            // valid token rows
+  int a_row0;       // first weight row in the A tensor map (layer offset)
+  int num_kb;       // K / 64
+  int kb_per_split; // k-blocks per split (grid.z splits)
+  int BN;           // token tile
+  int stages;       // pipeline depth
+  float* out;       // partial output [z][T][ldo] fp32 (kv == mode 0)
+  size_t split_stride;
+  int ldo;
+  int mode;         // 0: fp32 partials; 1: K/V cache scatter (bf16)
+  KvScatter kv;
+  int* status;
+};
+int tc_encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows);
+cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const TcGemmArgs& a, int tiles_n,
+                           int tiles_t, int splits, cudaStream_t st);
+size_t tc_smem_bytes(int BN, int stages);
+
+// W2A8 SIMT ternary GEMM: out[z][t][n] = (float) sum_{k in split z} a[t][k] q[n][k]
+// (exact integers), packed q [N][K/4].
+cudaError_t launch_ternary_simt(const int8_t* a, int lda, const uint8_t* q, int T, int N, int K, int splits,
+                                float* out, size_t split_stride, int ldo, cudaStream_t st);
+cudaError_t launch_quantize_rows(const float* x, int M, int K, int8_t* a, float* alpha, cudaStream_t st);
+cudaError_t launch_ternary_finish(const float* part, int M, int N, const float* alpha, float beta, uint16_t* y,
+                                  int32_t* acc, cudaStream_t st);
+cudaError_t launch_check_ternary_codes(const uint8_t* q, size_t nbytes, int* bad, cudaStream_t st);
+// Split count that launch_gemm_simt / launch_ternary_simt actually use for a
+// requested count (k range per split rounded up to `align`).
+int simt_effective_splits(int K, int splits, int align);
+// One-time kernel attribute set-up (dynamic shared memory limits); call
+// before any stream capture.
+cudaError_t simt_kernels_init();
+cudaError_t tc_kernels_init();
+cudaError_t expert_kernels_init();
+cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, cudaStream_t st);
+
+// Expert kernels (k_expert.cu).
+struct ExpertDims {
+  int L, D, F, n_q, n_kv, d_h, d_a, H, B, P, S, d_t;
+  float eps;
+  int qdim, kvdim, qkvdim;
+  int f32;   // 1 when the config dtype is fp32
+  int w2a8;  // 1 for the ternary / int8 variant
+};
+
+struct StepBufs {
+  // weights
+  const float* win;     // [D][d_a]
+  const float* wout;    // [d_a][D]
+  const float* modtab;  // [S][L][4][D]
+  const float* modf;    // [S][2][D]
+  const float* beta;    // [L][6] (W2A8)
+  // workspace
+  float* h;             // [T][D]
+  void* act;            // [T][Kmax] GEMM input (bf16 / fp32 / bf16 carriers)
+  int8_t* codes;        // [T][Kmax] W2A8 int8 codes (SIMT ternary path)
+  float* alpha;         // [T] W2A8 row scales
+  float* part;          // [splits][T][N] GEMM partials
+  void* q;              // [B][n_q][H][d_h]
+  void* ks;             // [B][n_kv][H][d_h]
+  void* vs;             // [B][n_kv][H][d_h]
+  float* opart;         // attention partial outputs
+  float* ml;            // attention partial (max, sum)
+  int attn_chunk, n_chunks;
+};
+
+cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st);
+cudaError_t launch_silu(float* x, size_t n, cudaStream_t st);
+cudaError_t launch_embed_norm(const ExpertDims& d, const StepBufs& b, int step, const float* x_in, DevCtl ctl,
+                              cudaStream_t st);
+cudaError_t launch_reduce_qkv(const ExpertDims& d, const StepBufs& b, int layer, int splits, cudaStream_t st);
+cudaError_t launch_attention(const ExpertDims& d, const StepBufs& b, int layer, const void* kc, const void* vc,
+                             cudaStream_t st);
+size_t attention_smem_bytes(const ExpertDims& d, int chunk);
+cudaError_t launch_reduce_norm(const ExpertDims& d, const StepBufs& b, int step, int layer_for_beta,
+                               int beta_slot, int mod_layer, int mod_half, int splits, cudaStream_t st);
+cudaError_t launch_reduce_gelu(const ExpertDims& d, const StepBufs& b, int layer, int splits, cudaStream_t st);
+cudaError_t launch_head(const ExpertDims& d, const StepBufs& b, int step, int splits, float dt, const float* x_in,
+                        float* x_out, float* tap, cudaStream_t st);

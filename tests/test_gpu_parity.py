@@ -1,0 +1,86 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded inputs.
+
+Gates (per action-chunk and per denoising step, as the fixed-input checks of
+"vla.cpp: A Unified Inference Runtime for Vision-Language-Action Models",
+§III-E, prescribe): bf16 paths max-abs 2e-2 on every per-step velocity
+(teacher-forced at the GPU's own x_k) and 1e-2 on the final chunk; the fp32
+instance 1e-4 on both.  The K/V cache (Eq. 2) must be within one bf16
+rounding of the oracle.
+"""
+
+import numpy as np
+import pytest
+
+from _harness import GATES, gpu_run, oracle_compare
+from workloads import CONFIGS
+
+pytestmark = pytest.mark.gpu
+
+
+def _gates(cfg):
+    return GATES["f32" if cfg.dtype == "f32" else "bf16"]
+
+
+def _kv_gate(cfg):
+    return 1e-5 if cfg.dtype == "f32" else 2.0 ** -8 + 1e-3
+
+
+def _check(run, obs, free_running=True):
+    cfg = run["cfg"]
+    assert run["status"] == 0
+    assert np.all(np.isfinite(run["act"])) and np.all(np.isfinite(run["tap"]))
+    res = oracle_compare(run, obs=obs, free_running=free_running)
+    g_v, g_x = _gates(cfg)
+    print(cfg.name, "kv", res["kv"], "v_tf", res["v_tf"], "x", res["x"])
+    assert max(res["kv"]) <= _kv_gate(cfg)
+    assert max(res["v_tf"]) <= g_v
+    for m in res["x"]:
+        assert m["e_inf"] <= g_x
+    return res
+
+
+def test_tiny_f32():
+    _check(gpu_run(CONFIGS["tiny_f32"]), obs=[0])
+
+
+def test_small_bf16():
+    _check(gpu_run(CONFIGS["small_bf16"]), obs=[0])
+
+
+def test_small_bf16_ragged_batch_and_prefix():
+    """Odd batch and a prefix that fills no tile evenly (edge of every tile loop)."""
+    cfg = CONFIGS["small_bf16"]
+    _check(gpu_run(cfg, B=3, P=77), obs=[0, 1, 2])
+
+
+def test_small_bf16_single_prefix_token():
+    cfg = CONFIGS["small_bf16"]
+    _check(gpu_run(cfg, B=1, P=1), obs=[0])
+
+
+def test_small_bf16_cuda_core_gemm_path():
+    """The diagnostic CUDA-core GEMM path must meet the same gates."""
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["small_bf16"], flags=V.FLAG_SIMT_GEMM), obs=[0])
+
+
+def test_tiny_f32_ragged():
+    cfg = CONFIGS["tiny_f32"]
+    _check(gpu_run(cfg, B=2, P=13), obs=[0, 1])
+
+
+def test_full_bf16_b1():
+    _check(gpu_run(CONFIGS["full_bf16_b1"]), obs=[0])
+
+
+def test_full_bf16_b64_sampled():
+    """64 independent observations; the oracle checks a seeded sample of them."""
+    _check(gpu_run(CONFIGS["full_bf16_b64"]), obs=[0, 63], free_running=True)
+
+
+def test_w2a8_b1():
+    _check(gpu_run(CONFIGS["w2a8_b1"]), obs=[0])
+
+
+def test_w2a8_b16_sampled():
+    _check(gpu_run(CONFIGS["w2a8_b16"]), obs=[0, 15], free_running=False)

@@ -392,3 +392,13 @@ def test_parity_metrics():
     assert abs(m["e_rel"] - 0.25 / np.linalg.norm(Ahat)) < 1e-15
     z = O.parity_metrics(np.full(4, 0.5), np.zeros(4))
     assert z["e_rel"] is None and z["e_abs"] == 1.0 and z["e_inf"] == 0.5
+
+
+def test_w2a8_unpacked_cache_is_same_function():
+    cfg = PIN.replace(w2a8=True, dtype="bf16")
+    w = make_weights(cfg)
+    Z, noise = make_observations(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    v1 = O.velocity_w2a8(noise, 0.5, Kc, Vc, w, cfg)
+    v2 = O.velocity_w2a8(noise, 0.5, Kc, Vc, O.with_unpacked(w), cfg)
+    assert np.array_equal(v1, v2)
