@@ -221,6 +221,10 @@ vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kerne
 /* Human-readable name of a status. */
 const char* vla_status_string(vla_status s);
 
+/* Text of the last CUDA failure seen by this thread (the call and the CUDA
+ * error), "" if none; valid until the next failing call on this thread. */
+const char* vla_last_error(void);
+
 /* Library version, e.g. "0.1.0". */
 const char* vla_version(void);
 

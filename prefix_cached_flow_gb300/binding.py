@@ -27,7 +27,7 @@ FLAG_SIMT_GEMM, FLAG_NO_GRAPH = 1, 2
 EXPORTED = ("vla_expert_create", "vla_expert_create_w2a8", "vla_expert_destroy", "vla_prefix_cache_bytes",
             "vla_prefix_kv_build", "vla_action_denoise", "vla_action_denoise_w2a8", "vla_policy_step_host",
             "vla_expert_poll_status", "vla_expert_set_abort", "vla_w2a8_quantize_rows",
-            "vla_w2a8_ternary_gemm", "vla_expert_launch_count", "vla_status_string", "vla_version")
+            "vla_w2a8_ternary_gemm", "vla_expert_launch_count", "vla_status_string", "vla_version", "vla_last_error")
 
 
 class VlaError(RuntimeError):
@@ -94,13 +94,16 @@ def lib() -> ctypes.CDLL:
     L.vla_status_string.restype = ctypes.c_char_p
     L.vla_version.argtypes = []
     L.vla_version.restype = ctypes.c_char_p
+    L.vla_last_error.argtypes = []
+    L.vla_last_error.restype = ctypes.c_char_p
     _lib = L
     return L
 
 
 def _check(status: int, where: str):
     if status != VLA_OK:
-        raise VlaError(status, where)
+        detail = lib().vla_last_error().decode(errors="replace")
+        raise VlaError(status, f"{where} [{detail}]" if detail else where)
 
 
 def _ptr(t):

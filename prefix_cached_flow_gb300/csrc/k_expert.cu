@@ -334,18 +334,17 @@ __global__ void k_to_f32(const TS* src, float* dst, size_t n) {
 // Host launchers
 // ---------------------------------------------------------------------------
 cudaError_t expert_kernels_init() {
-  cudaError_t e = cudaFuncSetAttribute(k_attn_part<float, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       227 * 1024);
+  cudaError_t e = set_max_dyn_smem(k_attn_part<float, float>);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_attn_part<bf16, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  e = set_max_dyn_smem(k_attn_part<bf16, bf16>);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_reduce_gelu<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  e = set_max_dyn_smem(k_reduce_gelu<float>);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_reduce_gelu<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  e = set_max_dyn_smem(k_reduce_gelu<bf16>);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_attn_combine<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  e = set_max_dyn_smem(k_attn_combine<float>);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_attn_combine<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return set_max_dyn_smem(k_attn_combine<bf16>);
 }
 
 cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, cudaStream_t st) {

@@ -224,7 +224,7 @@ int simt_effective_splits(int K, int splits, int align) {
 }
 
 cudaError_t simt_kernels_init() {
-  return cudaFuncSetAttribute(k_quantize_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return set_max_dyn_smem(k_quantize_rows);
 }
 
 cudaError_t launch_quantize_rows(const float* x, int M, int K, int8_t* a, float* alpha, cudaStream_t st) {

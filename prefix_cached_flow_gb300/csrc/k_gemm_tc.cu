@@ -182,7 +182,7 @@ int tc_encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 }
 
 cudaError_t tc_kernels_init() {
-  return cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  return set_max_dyn_smem(k_gemm_tc);
 }
 
 size_t tc_smem_bytes(int BN, int stages) {

@@ -16,6 +16,8 @@
 
 #include "vla_common.cuh"
 
+static thread_local char g_last_error[256] = "";
+
 namespace {
 
 struct GraphEntry {
@@ -44,6 +46,10 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 int round_up(int a, int b) { return cdiv(a, b) * b; }
 
 }  // namespace
+
+void vla_set_last_error(const char* where, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+}
 
 struct vla_expert {
   vla_expert_config cfg{};
@@ -97,6 +103,7 @@ namespace {
 
 vla_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return VLA_OK;
+  vla_set_last_error("CUDA", e);
   if (e == cudaErrorMemoryAllocation) return VLA_ERR_OOM;
   return VLA_ERR_CUDA;
 }
@@ -104,7 +111,10 @@ vla_status cuda_status(cudaError_t e) {
 #define VLA_CK(expr)                                   \
   do {                                                 \
     cudaError_t _e = (expr);                           \
-    if (_e != cudaSuccess) return cuda_status(_e);     \
+    if (_e != cudaSuccess) {                           \
+      vla_set_last_error(#expr, _e);                   \
+      return _e == cudaErrorMemoryAllocation ? VLA_ERR_OOM : VLA_ERR_CUDA; \
+    }                                                  \
   } while (0)
 
 template <typename T>
@@ -290,12 +300,12 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   if (cfg->mlp_width > h->Kmax) h->Kmax = cfg->mlp_width;
   if (h->qdim > h->Kmax) h->Kmax = h->qdim;
   *out = h;
-  cudaError_t e = simt_kernels_init();
-  if (e == cudaSuccess) e = tc_kernels_init();
-  if (e == cudaSuccess) e = expert_kernels_init();
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   (void)st;
-  return cuda_status(e);
+  VLA_CK(simt_kernels_init());
+  VLA_CK(tc_kernels_init());
+  VLA_CK(expert_kernels_init());
+  VLA_CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  return VLA_OK;
 }
 
 // Shared tail of create: time table, fp32 in/out maps, workspace, tensor maps.
@@ -412,6 +422,8 @@ const char* vla_status_string(vla_status s) {
 }
 
 const char* vla_version(void) { return "0.1.0"; }
+
+const char* vla_last_error(void) { return g_last_error; }
 
 void vla_expert_destroy(vla_expert* h) {
   if (!h) return;

@@ -321,6 +321,23 @@ cudaError_t launch_check_ternary_codes(const uint8_t* q, size_t nbytes, int* bad
 // Split count that launch_gemm_simt / launch_ternary_simt actually use for a
 // requested count (k range per split rounded up to `align`).
 int simt_effective_splits(int K, int splits, int align);
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in
+// maximum minus the kernel's static shared memory.
+template <typename F>
+inline cudaError_t set_max_dyn_smem(F* func) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, (const void*)func);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void*)func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+  return e;
+}
+// Records the failing CUDA call for vla_last_error().
+void vla_set_last_error(const char* where, cudaError_t e);
+
 // One-time kernel attribute set-up (dynamic shared memory limits); call
 // before any stream capture.
 cudaError_t simt_kernels_init();
