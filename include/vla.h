@@ -214,6 +214,29 @@ vla_status vla_w2a8_ternary_gemm(const int8_t* a_dev, const float* alpha_dev, co
                                  float beta, int M, int N, int K, uint16_t* y_dev,
                                  int32_t* acc_dev, void* stream);
 
+/* Allocation-free variant of vla_w2a8_ternary_gemm.  The paper has no
+ * counterpart; it exists for callers that cannot allocate device memory
+ * while they run -- a robot control loop with a hard period, where a device
+ * allocation may synchronise the device or take an unbounded time, or a host
+ * program whose device memory is reserved up front by another runtime's
+ * pool.  Same arguments, layouts and results (bit for bit) as
+ * vla_w2a8_ternary_gemm, but its fp32 partial-sum scratch is a fixed array
+ * of VLA_NOALLOC_MAX_ELEMS floats (4 MiB) inside the library, held by every
+ * GPU that loads the library until the process exits; the call itself makes
+ * no allocation.
+ *   - M * N > VLA_NOALLOC_MAX_ELEMS -> VLA_ERR_UNSUPPORTED (nothing enqueued).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the array, which keeps the last call's contents; calls
+ *     that overlap on the GPU race on it, so order them (one stream, or
+ *     explicit dependencies).  Nothing needs clearing between calls: every
+ *     call overwrites the M x N slots it reads. */
+#define VLA_NOALLOC_MAX_ELEMS 1048576
+vla_status vla_w2a8_ternary_gemm_noalloc(const int8_t* a_dev, const float* alpha_dev, const uint8_t* q_dev,
+                                         float beta, int M, int N, int K, uint16_t* y_dev,
+                                         int32_t* acc_dev, void* stream);
+
 /* Number of kernels one denoise call launches for batch B and prefix P
  * (all of them inside the one graph launch).  Host-only arithmetic. */
 vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kernels);
