@@ -145,14 +145,17 @@ vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert
 /* Synchronises the device and frees everything the handle owns.  NULL is a no-op. */
 void vla_expert_destroy(vla_expert* h);
 
-/* Bytes of ONE of the two cache tensors K_C, V_C for (B, P):
- * L * B * n_kv * P * d_h * sizeof(dtype). */
+/* Bytes to allocate for EACH of the two cache tensors for (B, P):
+ * L * B * n_kv * P8 * d_h * sizeof(dtype), P8 = P rounded up to a multiple
+ * of 8 (K_C needs only L * B * n_kv * P * d_h of it). */
 vla_status vla_prefix_cache_bytes(const vla_expert* h, int B, int P, size_t* bytes_per_tensor);
 
 /* Eq. 2, once per observation: K_C^l = Z W_K^l, V_C^l = Z W_V^l for every layer.
  *   Z_dev   [B][P][d_vlm]            config dtype, read only
  *   Kc_dev  [L][B][n_kv][P][d_h]     config dtype, written
- *   Vc_dev  [L][B][n_kv][P][d_h]     config dtype, written
+ *   Vc_dev  [L][B][n_kv][d_h][P8]    config dtype, written: V_C stored
+ *           transposed, P8 = P rounded up to a multiple of 8 (each row of
+ *           V_C^T starts 16-byte aligned; entries p >= P are not written)
  * 1 <= B <= max_batch, 1 <= P <= max_prefix.  No mask and no positions enter
  * the projection.  Enqueues one kernel. */
 vla_status vla_prefix_kv_build(vla_expert* h, const void* Z_dev, int B, int P,

@@ -169,10 +169,12 @@ class Expert:
         return n.value
 
     def alloc_cache(self, B: int, P: int):
+        """K_C [L, B, n_kv, P, d_h] and V_C stored transposed [L, B, n_kv, d_h, P8]
+        (P8 = P rounded up to a multiple of 8)."""
         c = self.cfg
-        shape = (c.L, B, c.n_kv, P, c.d_h)
-        return (torch.empty(shape, dtype=self.dtype, device="cuda"),
-                torch.empty(shape, dtype=self.dtype, device="cuda"))
+        p8 = (P + 7) // 8 * 8
+        return (torch.empty((c.L, B, c.n_kv, P, c.d_h), dtype=self.dtype, device="cuda"),
+                torch.empty((c.L, B, c.n_kv, c.d_h, p8), dtype=self.dtype, device="cuda"))
 
     def prefix_kv_build(self, Z, Kc, Vc, stream=None):
         B, P = Z.shape[0], Z.shape[1]
@@ -182,7 +184,7 @@ class Expert:
     # -- solver -----------------------------------------------------------
     def denoise(self, Kc, Vc, noise, actions=None, vel_tap=None, stream=None):
         B = noise.shape[0]
-        P = Kc.shape[3]
+        P = Kc.shape[3]  # K_C is [L, B, n_kv, P, d_h]
         if actions is None:
             actions = torch.empty_like(noise)
         fn = lib().vla_action_denoise_w2a8 if self.w2a8 else lib().vla_action_denoise

@@ -1,0 +1,357 @@
+// Joint non-causal GQA attention on tcgen05 ("vla.cpp: A Unified Inference
+// Runtime for Vision-Language-Action Models", §III-B Eq. (2)):
+//   o = softmax(Q [K_C ; K_s]^T / sqrt(d_h) + M) [V_C ; V_s],  M = 0,
+// for the action queries of every head sharing one K/V head, over the cached
+// prefix keys followed by the action tokens' own keys.
+//
+// A thread-block cluster of CS CTAs handles one 128-row query tile of one
+// (observation, K/V head); rows are (query head within the group, action
+// token).  Ranks 0..CS-2 each take KC consecutive prefix keys, rank CS-1 the
+// action keys.  Per CTA:
+//   S = Q K^T      tcgen05, A = Q [128][d_h], B = K chunk [KC][d_h]   -> TMEM
+//   P = exp2(S log2e / sqrt(d_h) - m)   one thread per query row, bf16 into
+//                                       a 128-byte-swizzled tile in smem
+//   O = P V        tcgen05, A = P [128][KC], B = V^T chunk [d_h][KC] -> TMEM
+// V is stored transposed so that both MMAs read K-major operands.  The ranks
+// then merge: row maxima and sums are exchanged through distributed shared
+// memory, every rank scales its O by exp2(m_r - M) / sum_c exp2(m_c - M) l_c
+// and publishes it in bf16 through L2 (cluster barrier with release/acquire),
+// and rank r sums a d_h/CS-column slice over the ranks in fp32 (fixed order,
+// deterministic) and writes bf16 o [B*H][n_q*d_h].
+// The prefix tiles are loaded before griddepcontrol.wait (they do not
+// depend on the previous kernel); Q and the action keys/values after it.
+#include "vla_common.cuh"
+
+namespace {
+
+struct AttnSmem {
+  uint32_t q, k, v, p, bars, slot, ml;
+  uint32_t total;
+};
+
+__host__ __device__ inline AttnSmem attn_layout(int d_h, int kc) {
+  const int nsub = d_h / 64;
+  const int ksub = (kc + 63) / 64;
+  AttnSmem s;
+  s.q = 0;                                           // nsub x [128][64] bf16
+  s.k = s.q + nsub * 16384;                          // nsub x [kc][64]  (1024-aligned slices)
+  const uint32_t kslice = ((uint32_t)kc * 128u + 1023u) & ~1023u;
+  s.v = s.k + nsub * kslice;                         // ksub x [d_h][64]
+  s.p = s.v + ksub * d_h * 128;                      // ksub x [128][64]
+  const uint32_t end = s.p + ksub * 16384;
+  s.bars = (end + 7u) & ~7u;                         // 3 mbarriers
+  s.slot = s.bars + 3 * 8;
+  s.ml = s.slot + 16;                                // [128] m, [128] l
+  s.total = s.ml + 2 * 128 * 4;
+  return s;
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(128, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmKs,
+              const __grid_constant__ CUtensorMap tmVs, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int dh = a.d_h, CS = a.cs;
+  const int nsub = dh / 64;
+  const bool suffix = (int)blockIdx.x == CS - 1;
+  const int kc = suffix ? a.kc_s : a.kc;             // keys this rank's tiles hold
+  const int ksub = (kc + 63) / 64;
+  const AttnSmem L = attn_layout(dh, a.kc > a.kc_s ? a.kc : a.kc_s);
+  const uint32_t kslice = ((uint32_t)kc * 128u + 1023u) & ~1023u;
+  uint8_t* Qs = smem + L.q;
+  uint8_t* Ks = smem + L.k;
+  uint8_t* Vt = smem + L.v;
+  uint8_t* Ps = smem + L.p;
+  uint64_t* bars = (uint64_t*)(smem + L.bars);  // 0: K/V, 1: Q, 2: MMA done
+  uint32_t* tmem_slot = (uint32_t*)(smem + L.slot);
+  float* sm_m = (float*)(smem + L.ml);
+  float* sm_l = sm_m + 128;
+  __shared__ int s_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = blockIdx.x, qt = blockIdx.y, bg = blockIdx.z;
+  const int b = bg / a.n_kv, gk = bg - b * a.n_kv;
+  const int key0 = suffix ? 0 : rank * a.kc;
+  const int avail = (suffix ? a.H : a.P) - key0;
+  const int nk = avail < 0 ? 0 : (avail < kc ? avail : kc);
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)dh || ncols < (uint32_t)kc) ncols <<= 1;
+  const uint32_t kv_bytes = (uint32_t)nsub * (uint32_t)kc * 128u + (uint32_t)ksub * (uint32_t)dh * 128u;
+  const uint32_t q_bytes = (uint32_t)nsub * 16384u;
+  VLA_TL(a.tl, 0, 0);
+
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Prefix K / V^T tiles: cache data, independent of the previous kernel.
+  if (threadIdx.x == 0 && !suffix && nk > 0) {
+    const int z = (a.layer * a.B + b) * a.n_kv + gk;
+    mbar_arrive_expect_tx(&bars[0], kv_bytes);
+    for (int s = 0; s < nsub; ++s) tma_load_3d(Ks + (size_t)s * kslice, &tmK, &bars[0], s * 64, key0, z);
+    for (int s = 0; s < ksub; ++s) tma_load_3d(Vt + (size_t)s * dh * 128, &tmVt, &bars[0], key0 + s * 64, 0, z);
+  }
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
+  VLA_TL(a.tl, 0, 1);
+  if (threadIdx.x == 0 && nk > 0) {
+    if (suffix) {
+      const int z = b * a.n_kv + gk;
+      mbar_arrive_expect_tx(&bars[0], kv_bytes);
+      for (int s = 0; s < nsub; ++s) tma_load_3d(Ks + (size_t)s * kslice, &tmKs, &bars[0], s * 64, 0, z);
+      for (int s = 0; s < ksub; ++s) tma_load_3d(Vt + (size_t)s * dh * 128, &tmVs, &bars[0], s * 64, 0, z);
+    }
+    const int qrow = (b * a.n_q + gk * a.group) * a.H + qt * 128;
+    mbar_arrive_expect_tx(&bars[1], q_bytes);
+    for (int s = 0; s < nsub; ++s) tma_load_2d(Qs + (size_t)s * 16384, &tmQ, &bars[1], s * 64, qrow);
+  }
+
+  // S = Q K^T
+  const uint32_t parity0 = 0;
+  if (nk > 0) {
+    if (warp == 1 && lane == 0) {
+      const bool okw = mbar_wait(&bars[1], 0, a.status) && mbar_wait(&bars[0], 0, a.status);
+      if (!okw) s_fail = 1;
+      VLA_TL(a.tl, 32, 2);
+      if (okw) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, kc);
+        for (int s = 0; s < nsub; ++s) {
+          const uint32_t qa = smem_u32(Qs + (size_t)s * 16384), ka = smem_u32(Ks + (size_t)s * kslice);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tmem, sdesc_k128(qa + k * 32), sdesc_k128(ka + k * 32), idesc, (s > 0 || k > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(&bars[2]);
+    }
+    __syncwarp();
+    if (!mbar_wait(&bars[2], parity0, a.status)) s_fail = 1;
+    tc_fence_after();
+  }
+  __syncthreads();
+  const bool ok = s_fail == 0;
+  VLA_TL(a.tl, 0, 3);
+
+  // Softmax over this rank's keys, one query row per thread (two passes over TMEM).
+  const int row = warp * 32 + lane;
+  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  float m = -INFINITY, l = 0.f;
+  if (ok && nk > 0) {
+    // The whole row of S (kc <= 128 columns) in registers: every TMEM load is
+    // issued back to back and waited on once.
+    uint32_t sr[128];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q * 16 < kc) tmem_ld16_nowait(taddr + (uint32_t)(q * 16), sr + q * 16);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q * 16 < kc) tmem_wait16(sr + q * 16);
+#pragma unroll
+    for (int j = 0; j < 128; ++j)
+      if (j < nk) m = fmaxf(m, __uint_as_float(sr[j]) * a.scale_log2);
+    const uint32_t pa = smem_u32(Ps);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {  // 8-key chunks
+      if (q * 8 < kc) {
+        float p[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = q * 8 + u;
+          p[u] = j < nk ? fast_exp2(__uint_as_float(sr[j]) * a.scale_log2 - m) : 0.f;
+          l += p[u];
+        }
+        uint4 pk;
+        pk.x = pack_bf16x2(p[0], p[1]);
+        pk.y = pack_bf16x2(p[2], p[3]);
+        pk.z = pack_bf16x2(p[4], p[5]);
+        pk.w = pack_bf16x2(p[6], p[7]);
+        st_shared_v4_u32(pa + (uint32_t)(q >> 3) * 16384u + sw128_offset((uint32_t)row, (uint32_t)(q & 7)), pk);
+      }
+    }
+  }
+  VLA_TL(a.tl, 0, 8);
+  sm_m[row] = m;
+  sm_l[row] = l;
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // O = P V (overwrites S's TMEM columns: every S read has completed).
+  if (nk > 0) {
+    if (warp == 1 && lane == 0) {
+      if (ok) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, dh);
+        const uint32_t pa = smem_u32(Ps), va = smem_u32(Vt);
+        for (int kk = 0; kk < kc / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+          const uint32_t voff = (uint32_t)(kk >> 2) * (uint32_t)dh * 128u + (uint32_t)(kk & 3) * 32u;
+          umma_bf16(tmem, sdesc_k128(pa + off), sdesc_k128(va + voff), idesc, kk > 0 ? 1u : 0u);
+        }
+      }
+      umma_commit(&bars[2]);
+    }
+    __syncwarp();
+    if (!mbar_wait(&bars[2], parity0 ^ 1u, a.status)) s_fail = 1;
+    tc_fence_after();
+  }
+  VLA_TL(a.tl, 0, 9);
+  cluster_sync_all();  // every rank's (m, l) is visible
+  VLA_TL(a.tl, 0, 4);
+
+  // Merge factors for this row: M = max_c m_c, den = sum_c exp2(m_c - M) l_c.
+  const uint32_t mloc = smem_u32(&sm_m[row]), lloc = smem_u32(&sm_l[row]);
+  float mc[16], lc[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    if (c < CS) {
+      mc[c] = ld_dsmem_f32(mapa_shared(mloc, (uint32_t)c));
+      lc[c] = ld_dsmem_f32(mapa_shared(lloc, (uint32_t)c));
+    }
+  float M = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    if (c < CS) M = fmaxf(M, mc[c]);
+  float den = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    if (c < CS && lc[c] > 0.f) den += fast_exp2(mc[c] - M) * lc[c];
+  const float f = (nk > 0 && l > 0.f) ? fast_exp2(m - M) / den : 0.f;
+  VLA_TL(a.tl, 0, 10);
+
+  // Publish f * O_rank (bf16; each rank holds roughly 1/CS of the sum) for the
+  // valid query rows through L2, interleaved as [d_h/8][128 rows][8] so that
+  // a warp's 32 rows form one 512-byte run.
+  const int nrows = (a.group * a.H - qt * 128) < 128 ? (a.group * a.H - qt * 128) : 128;
+  const size_t cl = (size_t)bg * a.n_qt + qt;  // this cluster's query tile
+  if (s_fail == 0 && nk > 0) {
+    uint4* dst = (uint4*)(a.xo + (cl * CS + rank) * 128 * (size_t)dh) + row;
+    for (int c0 = 0; c0 < dh; c0 += 64) {  // 64 columns per TMEM wait
+      uint32_t r[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld16_nowait(taddr + (uint32_t)(c0 + q * 16), r + q * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_wait16(r + q * 16);
+      if (row < nrows) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* w = r + q * 8;
+          uint4 u;
+          u.x = pack_bf16x2(f * __uint_as_float(w[0]), f * __uint_as_float(w[1]));
+          u.y = pack_bf16x2(f * __uint_as_float(w[2]), f * __uint_as_float(w[3]));
+          u.z = pack_bf16x2(f * __uint_as_float(w[4]), f * __uint_as_float(w[5]));
+          u.w = pack_bf16x2(f * __uint_as_float(w[6]), f * __uint_as_float(w[7]));
+          __stcg(dst + (size_t)(c0 / 8 + q) * 128, u);
+        }
+      }
+    }
+  }
+  cluster_sync_all();
+  VLA_TL(a.tl, 0, 5);
+
+  // Rank r sums columns [r*dh/CS, (r+1)*dh/CS) over the ranks that held keys
+  // (fixed order, fp32) and writes o: one query row per thread.
+  const int cols = dh / CS;
+  const int q8 = cols / 8;  // 8-column groups in this slice
+  if (s_fail == 0 && row < nrows) {
+    const int rg = qt * 128 + row;  // row within the group: (head, token)
+    const int jj = rg / a.H, i = rg - jj * a.H;
+    const int j = gk * a.group + jj;
+    bf16* out = a.o + ((size_t)b * a.H + i) * (size_t)(a.n_q * dh) + (size_t)j * dh + rank * cols;
+    for (int c8 = 0; c8 < q8; c8 += 2) {
+      uint4 v[2][16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const bool held = (c8 + h) < q8 && c < CS && (c == CS - 1 || c * a.kc < a.P);
+          v[h][c] = held ? __ldcg((const uint4*)(a.xo + (cl * CS + c) * 128 * (size_t)dh) +
+                                  (size_t)(rank * q8 + c8 + h) * 128 + row)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (c8 + h >= q8) break;
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w[4] = {v[h][c].x, v[h][c].y, v[h][c].z, v[h][c].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            sum[2 * u] += __uint_as_float(w[u] << 16);
+            sum[2 * u + 1] += __uint_as_float(w[u] & 0xFFFF0000u);
+          }
+        }
+        uint4 o4;
+        o4.x = pack_bf16x2(sum[0], sum[1]); o4.y = pack_bf16x2(sum[2], sum[3]);
+        o4.z = pack_bf16x2(sum[4], sum[5]); o4.w = pack_bf16x2(sum[6], sum[7]);
+        *(uint4*)(out + (c8 + h) * 8) = o4;
+      }
+    }
+  }
+  VLA_TL(a.tl, 0, 6);
+
+  // Drain the TMA copies (complete unless a wait timed out) and free TMEM.
+  if (threadIdx.x == 0 && nk > 0) {
+    mbar_wait(&bars[0], 0, a.status);
+    mbar_wait(&bars[1], 0, a.status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+}  // namespace
+
+size_t attn_tc_smem_bytes(int d_h, int kc) { return 1024 + attn_layout(d_h, kc).total; }
+
+cudaError_t attn_kernels_init() {
+  cudaError_t e = set_max_dyn_smem(k_attn_tc);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
+                           const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st) {
+  if (a.d_h % 64 || a.d_h > 256 || a.d_h < 64 || a.cs < 2 || a.cs > 16 || (a.cs & (a.cs - 1)) || a.kc < 16 ||
+      a.kc > 128 || a.kc % 16 || a.kc_s < 16 || a.kc_s > 128 || a.kc_s % 16 || (a.d_h / a.cs) % 8)
+    return cudaErrorInvalidValue;
+  const int kmax = a.kc > a.kc_s ? a.kc : a.kc_s;
+  const size_t smem = attn_tc_smem_bytes(a.d_h, kmax);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.cs, a.n_qt, a.B * a.n_kv);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_attn_tc, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+}

@@ -114,8 +114,10 @@ __global__ void k_reduce_qkv(ExpertDims d, StepBufs b, int layer, int splits) {
     } else {
       const int nn = n - d.qdim - (slot == 2 ? d.kvdim : 0);
       const int g = nn / d.d_h, e = nn - g * d.d_h;
-      TQ* dst = slot == 1 ? ks : vs;
-      dst[(((size_t)bb * d.n_kv + g) * d.H + i) * d.d_h + e] = from_f<TQ>(s);
+      if (slot == 1)
+        ks[(((size_t)bb * d.n_kv + g) * d.H + i) * d.d_h + e] = from_f<TQ>(s);
+      else
+        vs[(((size_t)bb * d.n_kv + g) * d.d_h + e) * d.Hp + i] = from_f<TQ>(s);
     }
   }
 }
@@ -139,19 +141,19 @@ __global__ void k_attn_part(ExpertDims d, StepBufs b, const TC* Kc, const TC* Vc
   const TQ* qg = (const TQ*)b.q + ((size_t)bb * d.n_q + j) * H * dh;
   for (int idx = threadIdx.x; idx < H * dh; idx += blockDim.x) qs[idx] = to_f(qg[idx]) * scale;
   const TQ* ksg = (const TQ*)b.ks + ((size_t)bb * d.n_kv + g) * H * dh;
-  const TQ* vsg = (const TQ*)b.vs + ((size_t)bb * d.n_kv + g) * H * dh;
+  const TQ* vsg = (const TQ*)b.vs + ((size_t)bb * d.n_kv + g) * dh * d.Hp;  // [d_h][Hp]
   const TC* Kg = Kc + ((size_t)bb * d.n_kv + g) * d.P * dh;
-  const TC* Vg = Vc + ((size_t)bb * d.n_kv + g) * d.P * dh;
+  const TC* Vg = Vc + ((size_t)bb * d.n_kv + g) * dh * d.P8;  // [d_h][P8]
   for (int idx = threadIdx.x; idx < nk * dh; idx += blockDim.x) {
     const int r = idx / dh, e = idx - r * dh;
     const int kk = k0 + r;
     float kv, vv;
     if (kk < d.P) {
       kv = to_f(Kg[(size_t)kk * dh + e]);
-      vv = to_f(Vg[(size_t)kk * dh + e]);
+      vv = to_f(Vg[(size_t)e * d.P8 + kk]);
     } else {
       kv = to_f(ksg[(size_t)(kk - d.P) * dh + e]);
-      vv = to_f(vsg[(size_t)(kk - d.P) * dh + e]);
+      vv = to_f(vsg[(size_t)e * d.Hp + (kk - d.P)]);
     }
     Ks[r * (dh + 1) + e] = kv;
     Vs[r * dh + e] = vv;
@@ -322,6 +324,83 @@ __global__ void k_head(ExpertDims d, StepBufs b, int step, int splits, float dt,
   }
 }
 
+// h = x W_in^T and its row sum of squares (one slot) for the first layer's
+// in-GEMM modulated RMSNorm; also latches the abort flag once per step.
+__global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  extern __shared__ float sm[];
+  float* xs = sm;
+  float* red = sm + d.d_a;
+  const int t = blockIdx.x;
+  if (t == 0 && threadIdx.x == 0 && ctl.abort && *ctl.abort) latch_error(ctl.status, VLA_DEV_ABORTED);
+  for (int j = threadIdx.x; j < d.d_a; j += blockDim.x) xs[j] = x_in[(size_t)t * d.d_a + j];
+  __syncthreads();
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+    const float* w = b.win + (size_t)i * d.d_a;
+    float acc = 0.f;
+    for (int j = 0; j < d.d_a; ++j) acc += xs[j] * w[j];
+    b.h[(size_t)t * d.D + i] = acc;
+    ss += acc * acc;
+  }
+  ss = block_sum(ss, red);
+  if (threadIdx.x == 0) ss_out[t] = ss;
+}
+
+// u = h / rms(h) * (1 + gamma) + beta as bf16 [T][D], rms from n_ss slots.
+__global__ void k_modnorm(int T, int D, float eps, const float* h, const float* ss, int n_ss, const float* gamma,
+                          const float* beta, bf16* u) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int t = blockIdx.x;
+  float s = 0.f;
+  for (int k = 0; k < n_ss; ++k) s += ss[(size_t)k * T + t];
+  const float r = rsqrtf(s / (float)D + eps);
+  for (int i = threadIdx.x * 2; i < D; i += blockDim.x * 2) {
+    const float2 hv = *(const float2*)(h + (size_t)t * D + i);
+    const float v0 = hv.x * r * (1.f + gamma[i]) + beta[i];
+    const float v1 = hv.y * r * (1.f + gamma[i + 1]) + beta[i + 1];
+    *(uint32_t*)(u + (size_t)t * D + i) = pack_bf16x2(v0, v1);
+  }
+}
+
+// Velocity head on the final residual stream + Euler update (Eq. (1)).
+__global__ void k_head_fused(ExpertDims d, StepBufs b, int step, float dt, const float* x_in, float* x_out,
+                             float* tap) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + d.D;
+  const int t = blockIdx.x;
+  const int T = d.B * d.H;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+    const float hv = b.h[(size_t)t * d.D + i];
+    row[i] = hv;
+    ss += hv * hv;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / (float)d.D + d.eps);
+  const float* gf = b.modf + (size_t)step * 2 * d.D;
+  const float* bf = gf + d.D;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) row[i] = row[i] * r * (1.f + gf[i]) + bf[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int a = wid; a < d.d_a; a += nw) {
+    const float* w = b.wout + (size_t)a * d.D;
+    float acc = 0.f;
+    for (int i = lane; i < d.D; i += 32) acc += row[i] * w[i];
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      const size_t o = (size_t)t * d.d_a + a;
+      x_out[o] = fmaf(dt, acc, x_in[o]);
+      if (tap) tap[(size_t)step * T * d.d_a + o] = acc;
+    }
+  }
+}
+
 template <typename TS>
 __global__ void k_to_f32(const TS* src, float* dst, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
@@ -354,6 +433,46 @@ cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, c
   else
     k_to_f32<float><<<blocks, 256, 0, st>>>((const float*)src, dst, n);
   return cudaGetLastError();
+}
+
+static cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float* x_in, float* ss_out, DevCtl ctl,
+                            cudaStream_t st) {
+  ExpertDims dd = d;
+  StepBufs bb = b;
+  void* args[] = {&dd, &bb, (void*)&x_in, &ss_out, &ctl};
+  return launch_pdl((const void*)k_embed_ss, dim3(d.B * d.H), dim3(kThreads), (size_t)(d.d_a + 32) * sizeof(float),
+                    st, args);
+}
+
+cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss, int n_ss, const float* gamma,
+                           const float* beta, bf16* u, cudaStream_t st) {
+  int T = d.B * d.H, D = d.D;
+  float eps = d.eps;
+  void* args[] = {&T, &D, &eps, (void*)&h, (void*)&ss, &n_ss, (void*)&gamma, (void*)&beta, &u};
+  return launch_pdl((const void*)k_modnorm, dim3(T), dim3(kThreads), 0, st, args);
+}
+
+cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, float dt, const float* x_in,
+                              float* x_out, float* tap, cudaStream_t st) {
+  ExpertDims dd = d;
+  StepBufs bb = b;
+  void* args[] = {&dd, &bb, &step, &dt, (void*)&x_in, &x_out, &tap};
+  return launch_pdl((const void*)k_head_fused, dim3(d.B * d.H), dim3(kThreads), (size_t)(d.D + 32) * sizeof(float),
+                    st, args);
 }
 
 cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st) {
@@ -393,15 +512,16 @@ size_t attention_smem_bytes(const ExpertDims& d, int chunk) {
 
 cudaError_t launch_attention(const ExpertDims& d, const StepBufs& b, int layer, const void* kc, const void* vc,
                              cudaStream_t st) {
-  const size_t layer_elems = (size_t)d.B * d.n_kv * d.P * d.d_h;
+  const size_t layer_k = (size_t)d.B * d.n_kv * d.P * d.d_h;
+  const size_t layer_v = (size_t)d.B * d.n_kv * d.d_h * d.P8;
   const size_t smem = attention_smem_bytes(d, b.attn_chunk);
   dim3 grid(b.n_chunks, d.n_q, d.B);
   if (d.f32)
-    k_attn_part<float, float><<<grid, kThreads, smem, st>>>(d, b, (const float*)kc + layer * layer_elems,
-                                                          (const float*)vc + layer * layer_elems);
+    k_attn_part<float, float><<<grid, kThreads, smem, st>>>(d, b, (const float*)kc + layer * layer_k,
+                                                          (const float*)vc + layer * layer_v);
   else
-    k_attn_part<bf16, bf16><<<grid, kThreads, smem, st>>>(d, b, (const bf16*)kc + layer * layer_elems,
-                                                        (const bf16*)vc + layer * layer_elems);
+    k_attn_part<bf16, bf16><<<grid, kThreads, smem, st>>>(d, b, (const bf16*)kc + layer * layer_k,
+                                                        (const bf16*)vc + layer * layer_v);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem2 = (size_t)(d.qdim + 32) * sizeof(float);

@@ -73,9 +73,10 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const TX* __restrict__ X, int
         const int r2 = rem - which * kvdim;
         const int g = r2 / kv.d_h, e = r2 - g * kv.d_h;
         const int b = t / kv.P, p = t - b * kv.P;
-        const size_t o = ((((size_t)l * kv.B + b) * kv.n_kv + g) * kv.P + p) * kv.d_h + e;
-        TW* dst = (TW*)(which ? kv.vc : kv.kc);
-        dst[o] = from_f<TW>(acc[i][j]);
+        if (which == 0)
+          ((TW*)kv.kc)[((((size_t)l * kv.B + b) * kv.n_kv + g) * kv.P + p) * kv.d_h + e] = from_f<TW>(acc[i][j]);
+        else
+          ((TW*)kv.vc)[((((size_t)l * kv.B + b) * kv.n_kv + g) * kv.d_h + e) * kv.P8 + p] = from_f<TW>(acc[i][j]);
       }
     }
   }

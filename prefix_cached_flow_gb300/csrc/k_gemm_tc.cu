@@ -126,13 +126,38 @@ __global__ void __launch_bounds__(128, 1)
         const int which = rem / kvdim;
         const int r2 = rem - which * kvdim;
         const int gg = r2 / kv.d_h, e = r2 - gg * kv.d_h;
-        bf16* dst = (bf16*)(which ? kv.vc : kv.kc);
+        if (which == 0) {
+          bf16* dst = (bf16*)kv.kc;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = t0 + c0 + j;
-          if (t >= g.T) continue;
-          const int b = t / kv.P, p = t - b * kv.P;
-          dst[((((size_t)l * kv.B + b) * kv.n_kv + gg) * kv.P + p) * kv.d_h + e] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + c0 + j;
+            if (t >= g.T) continue;
+            const int b = t / kv.P, p = t - b * kv.P;
+            dst[((((size_t)l * kv.B + b) * kv.n_kv + gg) * kv.P + p) * kv.d_h + e] = __float2bfloat16_rn(v[j]);
+          }
+        } else {
+          // V_C^T: this thread's row (feature e) gets 16 consecutive tokens.
+          bf16* dst = (bf16*)kv.vc;
+          const int tb = t0 + c0;
+          const int b0 = tb / kv.P, p0 = tb - b0 * kv.P;
+          bf16* rowp = dst + ((((size_t)l * kv.B + b0) * kv.n_kv + gg) * kv.d_h + e) * kv.P8;
+          if (tb + 15 < g.T && p0 + 15 < kv.P && (p0 & 7) == 0) {
+            uint4 a, bq;
+            a.x = pack_bf16x2(v[0], v[1]); a.y = pack_bf16x2(v[2], v[3]);
+            a.z = pack_bf16x2(v[4], v[5]); a.w = pack_bf16x2(v[6], v[7]);
+            bq.x = pack_bf16x2(v[8], v[9]); bq.y = pack_bf16x2(v[10], v[11]);
+            bq.z = pack_bf16x2(v[12], v[13]); bq.w = pack_bf16x2(v[14], v[15]);
+            *(uint4*)(rowp + p0) = a;
+            *(uint4*)(rowp + p0 + 8) = bq;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = tb + j;
+              if (t >= g.T) continue;
+              const int b = t / kv.P, p = t - b * kv.P;
+              dst[((((size_t)l * kv.B + b) * kv.n_kv + gg) * kv.d_h + e) * kv.P8 + p] = __float2bfloat16_rn(v[j]);
+            }
+          }
         }
       }
     }
@@ -183,6 +208,34 @@ int tc_encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 cudaError_t tc_kernels_init() {
   return set_max_dyn_smem(k_gemm_tc);
+}
+
+int tc_encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                     uint32_t box_rows) {
+  PFN_encodeTiled_t fn = get_encode();
+  if (!fn) return -1;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
+int tc_encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                      uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+  PFN_encodeTiled_t fn = get_encode();
+  if (!fn) return -1;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
 size_t tc_smem_bytes(int BN, int stages) {

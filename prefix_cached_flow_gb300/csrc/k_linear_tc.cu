@@ -1,0 +1,440 @@
+// Fused linear layer of the action expert on tcgen05, with on-chip split-K.
+//
+// y[t][n] = sum_k W[n][k] X[t][k] for one weight tile of 128 output rows and
+// one token tile of BN tokens.  The K range is split over the C CTAs of a
+// thread-block cluster (grid.z = C = cluster size); each CTA accumulates its
+// slice in TMEM, stages the fp32 tile in its shared memory, and after a
+// cluster barrier CTA `rank` sums rows [rank*128/C, (rank+1)*128/C) of all C
+// tiles through distributed shared memory (fixed order: deterministic) and
+// applies the epilogue:
+//   EPI_QKV   scatter to q [B][n_q][H][d_h], k_s [B][n_kv][H][d_h] and
+//             v_s^T [B][n_kv][d_h][Hp] (bf16) for the attention kernel;
+//   EPI_RESID h[t][n] += y, and per-(128-row block, token) sums of squares of
+//             the new h for the next modulated RMSNorm (the cluster combines
+//             its ranks' partial sums on chip, rank 0 writes them);
+//   EPI_GELU  g[t][n] = bf16(GeLU(y)).
+// The B operand (tokens) is either TMA-loaded from an activation tensor
+// (bmode 0) or built in shared memory from the fp32 residual stream as the
+// time-modulated RMSNorm  h / rms(h) * (1 + gamma) + beta  (bmode 1): one
+// TMA brings the CTA's h tile while the threads fetch the sums of squares
+// and the modulation slices in parallel.
+//
+// The weights do not depend on the previous kernel, so their TMA loads are
+// issued before griddepcontrol.wait: under programmatic dependent launch the
+// weight stream of this layer overlaps the tail of the previous kernel.
+//
+// Sources: "vla.cpp: A Unified Inference Runtime for Vision-Language-Action
+// Models", §III-A Eq. (1) (the velocity network evaluated per Euler step)
+// and §III-B Eq. (2) (queries, action keys and values for joint attention).
+#include "vla_common.cuh"
+
+namespace {
+
+constexpr uint32_t kA = 128 * 128;  // bytes of one 128 x 64 bf16 weight stage
+constexpr int kMaxC = 16;           // largest cluster
+constexpr int kPre = 2;             // residual quads prefetched per thread
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+struct LinSmem {
+  uint32_t a, b, hs, region, bars, slot, rstat, gam, bet, total;
+};
+
+__host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
+  LinSmem s;
+  const uint32_t b_tile = (uint32_t)g.BN * 128u;
+  const uint32_t nkb = (uint32_t)(g.KS / 64);
+  s.a = 0;
+  s.b = (uint32_t)g.stages * kA;
+  s.hs = s.b + (g.bmode == 0 ? (uint32_t)g.stages * b_tile : nkb * b_tile);
+  uint32_t end = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
+  const uint32_t stage = 128u * (uint32_t)g.BN * 4u;  // epilogue staging [BN][128] fp32
+  s.region = end > stage ? end : stage;
+  s.bars = s.region;                                  // full[NS], empty[NS], done, hbar
+  s.slot = s.bars + (2u * (uint32_t)g.stages + 2u) * 8u;
+  s.rstat = s.slot + 16u;                             // [BN] (also the epilogue's per-token sums)
+  s.gam = s.rstat + (uint32_t)g.BN * 4u;              // [KS]
+  s.bet = s.gam + (uint32_t)g.KS * 4u;                // [KS]
+  s.total = s.bet + (uint32_t)g.KS * 4u;
+  return s;
+}
+
+__global__ void __launch_bounds__(128, 1)
+    k_linear(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmH, const LinArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const LinSmem Ls = lin_layout(g);
+  const int BN = g.BN, NS = g.stages;
+  const int nkb = g.KS / 64;
+  const uint32_t b_tile = (uint32_t)BN * 128u;
+  uint8_t* Abase = smem + Ls.a;
+  uint8_t* Bbase = smem + Ls.b;
+  float* Hs = (float*)(smem + Ls.hs);
+  uint64_t* full = (uint64_t*)(smem + Ls.bars);
+  uint64_t* empty = full + NS;
+  uint64_t* done = empty + NS;
+  uint64_t* hbar = done + 1;
+  uint32_t* tmem_slot = (uint32_t*)(smem + Ls.slot);
+  float* rstat = (float*)(smem + Ls.rstat);
+  float* gam = (float*)(smem + Ls.gam);
+  float* bet = (float*)(smem + Ls.bet);
+  __shared__ int s_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128;
+  const int t0 = blockIdx.y * BN;
+  const int C = gridDim.z;
+  const int rank = blockIdx.z;
+  const int k0 = rank * g.KS;
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)BN) ncols <<= 1;
+  VLA_TL(g.tl, 0, 0);
+
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    mbar_init(hbar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(g.bmode == 0 ? (const void*)&tmB : (const void*)&tmH);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  VLA_TL(g.tl, 0, 1);
+
+  // Weight prefetch: independent of every earlier kernel.
+  const int pre = nkb < NS ? nkb : NS;
+  const uint32_t stage_tx = kA + (g.bmode == 0 ? b_tile : 0u);
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol = l2_policy_evict_first();
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full[i], stage_tx);
+      tma_load_2d_hint(Abase + (size_t)i * kA, &tmA, &full[i], k0 + i * 64, g.a_row0 + m0, pol);
+    }
+  }
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
+  VLA_TL(g.tl, 0, 2);
+
+  int issued = pre;
+  if (warp == 0 && lane == 0) {
+    if (g.bmode == 1) {
+      mbar_arrive_expect_tx(hbar, (uint32_t)nkb * (uint32_t)BN * 256u);
+      for (int i = 0; i < nkb; ++i) tma_load_2d(Hs + (size_t)i * BN * 64, &tmH, hbar, k0 + i * 64, t0);
+    } else {
+      for (int i = 0; i < pre; ++i) tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &full[i], k0 + i * 64, t0);
+    }
+  }
+  if (g.bmode == 1) {
+    // All four warps: B slice = modulated RMSNorm of h over this rank's K
+    // range.  Thread tid always handles the same 8-column chunk kc (so its
+    // gamma / beta stay in registers) for tokens t = tid / kcs + j * (128 / kcs).
+    const int tid = threadIdx.x;
+    for (int t = tid; t < BN; t += 128) {
+      const int tt = t0 + t;
+      float r = 0.f;
+      if (tt < g.T) {
+        float v[kMaxC];
+#pragma unroll
+        for (int s = 0; s < kMaxC; ++s) v[s] = s < g.n_ss_in ? g.ss_in[(size_t)s * g.T + tt] : 0.f;
+        float ss = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMaxC; ++s) ss += v[s];
+        r = rsqrtf(ss / (float)g.D + g.eps);
+      }
+      rstat[t] = r;
+    }
+    const int kcs = g.KS / 8;  // 8-column chunks per token (divides 128: KS <= 1024, power of two)
+    const int kc = tid % kcs;
+    const int tstep = 128 / kcs;
+    const float4* gp = (const float4*)(g.gamma + k0 + kc * 8);
+    const float4* bp = (const float4*)(g.beta + k0 + kc * 8);
+    const float4 g0 = gp[0], g1 = gp[1], b0 = bp[0], b1 = bp[1];
+    __syncthreads();
+    VLA_TL(g.tl, 32, 8);
+    if (!mbar_wait(hbar, 0, g.status)) s_fail = 1;
+    VLA_TL(g.tl, 32, 9);
+    const uint32_t bb = smem_u32(Bbase) + (uint32_t)(kc >> 3) * b_tile;
+    const float* hcol = Hs + (size_t)(kc >> 3) * BN * 64 + (kc & 7) * 8;
+#pragma unroll 2
+    for (int t = tid / kcs; t < BN; t += tstep) {
+      const int tt = t0 + t;
+      uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+      if (tt < g.T) {
+        const float r = rstat[t];
+        const float4* hp = (const float4*)(hcol + (size_t)t * 64);
+        const float4 h0 = hp[0], h1 = hp[1];
+        pk.x = pack_bf16x2(h0.x * r * (1.f + g0.x) + b0.x, h0.y * r * (1.f + g0.y) + b0.y);
+        pk.y = pack_bf16x2(h0.z * r * (1.f + g0.z) + b0.z, h0.w * r * (1.f + g0.w) + b0.w);
+        pk.z = pack_bf16x2(h1.x * r * (1.f + g1.x) + b1.x, h1.y * r * (1.f + g1.y) + b1.y);
+        pk.w = pack_bf16x2(h1.z * r * (1.f + g1.z) + b1.z, h1.w * r * (1.f + g1.w) + b1.w);
+      }
+      st_shared_v4_u32(bb + sw128_offset((uint32_t)t, (uint32_t)(kc & 7)), pk);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    VLA_TL(g.tl, 32, 10);
+  }
+  if (warp == 0 && lane == 0) {
+    const uint64_t pol = l2_policy_evict_first();
+    for (int i = pre; i < nkb; ++i) {
+      const int s = i % NS;
+      if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, g.status)) {
+        s_fail = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[s], stage_tx);
+      tma_load_2d_hint(Abase + (size_t)s * kA, &tmA, &full[s], k0 + i * 64, g.a_row0 + m0, pol);
+      if (g.bmode == 0) tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &full[s], k0 + i * 64, t0);
+      issued = i + 1;
+    }
+  }
+  if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, BN);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % NS;
+      if (s_fail || !mbar_wait(&full[s], (i / NS) & 1, g.status)) {
+        s_fail = 1;
+        break;
+      }
+      if (i == 0) VLA_TL(g.tl, 32, 3);
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(Abase + (size_t)s * kA);
+      const uint32_t b_addr = smem_u32(Bbase + (size_t)(g.bmode == 0 ? s : i) * b_tile);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_bf16(tmem, sdesc_k128(a_addr + k * 32), sdesc_k128(b_addr + k * 32), idesc, (i > 0 || k > 0) ? 1u : 0u);
+      umma_commit(&empty[s]);
+    }
+    umma_commit(done);
+    VLA_TL(g.tl, 32, 4);
+  }
+  __syncwarp();
+
+  // Epilogue geometry: rank r owns rows [r*RPR, (r+1)*RPR) of the tile.
+  const int RPR = 128 / C;
+  const int qpc = RPR / 4;  // float4 quads per token column
+  const int nquads = qpc * BN;
+  const int iters = (nquads + 127) / 128;
+  // Prefetch the residual rows this thread will update (independent of the MMA).
+  float4 hpre[kPre];
+  if (g.epi == EPI_RESID) {
+#pragma unroll
+    for (int it = 0; it < kPre; ++it) {
+      const int f = threadIdx.x + it * 128;
+      hpre[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (it < iters && f < nquads) {
+        const int col = f / qpc, quad = f - col * qpc;
+        const int n = m0 + rank * RPR + quad * 4, t = t0 + col;
+        if (t < g.T && n < g.N) hpre[it] = *(const float4*)(g.h + (size_t)t * g.D + n);
+      }
+    }
+  }
+
+  // Publish the fp32 partial tile through L2, column-major [col][row]
+  // (padding token columns are skipped).
+  if (!mbar_wait(done, 0, g.status)) s_fail = 1;
+  tc_fence_after();
+  __syncthreads();
+  VLA_TL(g.tl, 0, 5);
+  const bool ok = (s_fail == 0);
+  const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+  const int tcols = (g.T - t0) < BN ? (g.T - t0) : BN;  // valid token columns
+  float* mypart = g.xpart + ((size_t)tile * C + rank) * (size_t)BN * 128;
+  if (ok) {
+    const int row = warp * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int c0 = 0; c0 < tcols; c0 += 64) {  // up to 64 columns per TMEM wait
+      uint32_t r[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c0 + q * 16 < tcols) tmem_ld16_nowait(taddr + (uint32_t)(c0 + q * 16), r + q * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c0 + q * 16 < tcols) tmem_wait16(r + q * 16);
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (c0 + j < tcols) __stcg(mypart + (size_t)(c0 + j) * 128 + row, __uint_as_float(r[j]));
+    }
+  }
+  cluster_sync_all();
+  VLA_TL(g.tl, 0, 6);
+
+  // Cluster reduction (fixed rank order) and epilogue.  The partial sums of
+  // the first kPre iterations are gathered together so their L2 loads overlap.
+  const float* tpart = g.xpart + (size_t)tile * C * (size_t)BN * 128;
+  auto geom = [&](int it, bool& live, int& col, int& quad) {
+    const int f = threadIdx.x + it * 128;
+    live = ok && f < nquads && f / qpc < tcols;
+    col = live ? f / qpc : 0;
+    quad = live ? f - col * qpc : 0;
+  };
+  auto epilogue = [&](float4 acc, bool live, int col, int quad, float4 hprev, bool have_prev) {
+    const int rloc = rank * RPR + quad * 4;
+    const int n = m0 + rloc, t = t0 + col;
+    const bool valid = live && t < g.T && n < g.N;
+    if (g.epi == EPI_RESID) {
+      float ss = 0.f;
+      if (valid) {
+        float4* hp = (float4*)(g.h + (size_t)t * g.D + n);
+        float4 hv = have_prev ? hprev : *hp;
+        hv.x += acc.x; hv.y += acc.y; hv.z += acc.z; hv.w += acc.w;
+        *hp = hv;
+        ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
+      }
+      for (int o = qpc >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (live && quad == 0) rstat[col] = ss;
+    } else if (g.epi == EPI_GELU) {
+      if (valid) {
+        uint2 pk;
+        pk.x = pack_bf16x2(gelu_exact(acc.x), gelu_exact(acc.y));
+        pk.y = pack_bf16x2(gelu_exact(acc.z), gelu_exact(acc.w));
+        *(uint2*)(g.g + (size_t)t * g.ldg + n) = pk;
+      }
+    } else {  // EPI_QKV: a 4-row quad lies inside one head of q, k or v
+      if (valid) {
+        const int b = t / g.H, i = t - b * g.H;
+        if (n < g.qdim + g.kvdim) {
+          const bool isq = n < g.qdim;
+          const int r = isq ? n : n - g.qdim;
+          const int j = r / g.d_h, d = r - j * g.d_h;
+          bf16* dst = isq ? g.q + (((size_t)b * g.n_q + j) * g.H + i) * g.d_h + d
+                          : g.ks + (((size_t)b * g.n_kv + j) * g.H + i) * g.d_h + d;
+          uint2 pk;
+          pk.x = pack_bf16x2(acc.x, acc.y);
+          pk.y = pack_bf16x2(acc.z, acc.w);
+          *(uint2*)dst = pk;
+        } else {
+          const int r = n - g.qdim - g.kvdim;
+          const int gk = r / g.d_h, d = r - gk * g.d_h;
+          bf16* dst = g.vst + (((size_t)b * g.n_kv + gk) * g.d_h + d) * g.Hp + i;
+          dst[0] = __float2bfloat16_rn(acc.x);
+          dst[g.Hp] = __float2bfloat16_rn(acc.y);
+          dst[2 * g.Hp] = __float2bfloat16_rn(acc.z);
+          dst[3 * g.Hp] = __float2bfloat16_rn(acc.w);
+        }
+      }
+    }
+  };
+  {
+    // Iterations 0 and 1 (the only ones at small token counts): issue every
+    // partial load first, then sum, so the loads overlap.
+    bool lv0, lv1;
+    int cl0, qd0, cl1, qd1;
+    geom(0, lv0, cl0, qd0);
+    geom(1, lv1, cl1, qd1);
+    if (iters < 1) lv0 = false;
+    if (iters < 2) lv1 = false;
+    const float* p0 = tpart + (size_t)cl0 * 128 + rank * RPR + qd0 * 4;
+    const float* p1 = tpart + (size_t)cl1 * 128 + rank * RPR + qd1 * 4;
+    float4 v0[kMaxC], v1[kMaxC];
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c) {
+      v0[c] = (c < C && lv0) ? __ldcg((const float4*)(p0 + (size_t)c * BN * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v1[c] = (c < C && lv1) ? __ldcg((const float4*)(p1 + (size_t)c * BN * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c) {
+      a0.x += v0[c].x; a0.y += v0[c].y; a0.z += v0[c].z; a0.w += v0[c].w;
+      a1.x += v1[c].x; a1.y += v1[c].y; a1.z += v1[c].z; a1.w += v1[c].w;
+    }
+    if (iters >= 1) epilogue(a0, lv0, cl0, qd0, hpre[0], g.epi == EPI_RESID);
+    if (iters >= 2) epilogue(a1, lv1, cl1, qd1, hpre[1], g.epi == EPI_RESID);
+  }
+  for (int it = 2; it < iters; ++it) {
+    bool live;
+    int col, quad;
+    geom(it, live, col, quad);
+    float4 v[kMaxC];
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c)
+      v[c] = (c < C && live) ? __ldcg((const float4*)(tpart + (size_t)c * BN * 128 + (size_t)col * 128 + rank * RPR +
+                                                      quad * 4))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kMaxC; ++c) {
+      acc.x += v[c].x; acc.y += v[c].y; acc.z += v[c].z; acc.w += v[c].w;
+    }
+    epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false);
+  }
+  VLA_TL(g.tl, 0, 11);
+  if (g.epi == EPI_RESID) {
+    // Rank 0 combines the ranks' per-token sums of squares (fixed order).
+    __syncthreads();
+    float* myss = g.xss + ((size_t)tile * C + rank) * BN;
+    for (int col = threadIdx.x; col < tcols; col += 128) __stcg(myss + col, rstat[col]);
+    cluster_sync_all();
+    if (rank == 0 && ok) {
+      const float* tss = g.xss + (size_t)tile * C * BN;
+      for (int col = threadIdx.x; col < tcols; col += 128) {
+        float v[kMaxC];
+#pragma unroll
+        for (int c = 0; c < kMaxC; ++c) v[c] = c < C ? __ldcg(tss + (size_t)c * BN + col) : 0.f;
+        float s2 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxC; ++c) s2 += v[c];
+        g.ss_out[(size_t)blockIdx.x * g.T + t0 + col] = s2;
+      }
+    }
+  }
+
+  // Drain own TMA copies (only relevant after a timeout) and free TMEM.
+  if (warp == 0 && lane == 0) {
+    const int first = issued > NS ? issued - NS : 0;
+    for (int i = first; i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, g.status);
+    if (g.bmode == 1) mbar_wait(hbar, 0, g.status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  VLA_TL(g.tl, 0, 7);
+  if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+}  // namespace
+
+size_t linear_smem_bytes(const LinArgs& g) { return 1024 + lin_layout(g).total; }
+
+cudaError_t linear_kernels_init() {
+  cudaError_t e = set_max_dyn_smem(k_linear);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_linear, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& g,
+                          int tiles_n, int tiles_t, int C, cudaStream_t st) {
+  if (g.BN < 16 || g.BN > 256 || g.BN % 16 || g.KS % 64 || g.KS < 64 || g.stages < 1 || C < 1 || C > kMaxC ||
+      (C & (C - 1)) || g.N % 4 || (g.bmode == 1 && (g.n_ss_in < 1 || g.n_ss_in > kMaxC)))
+    return cudaErrorInvalidValue;
+  const size_t smem = linear_smem_bytes(g);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles_n, tiles_t, C);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = C;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_linear, *tmA, *tmB, *tmH, g);
+}

@@ -59,7 +59,7 @@ struct vla_expert {
   bool use_tc = false;
   int num_sms = 0;
   size_t es = 2;
-  int qdim = 0, kvdim = 0, qkvdim = 0, Kmax = 0;
+  int qdim = 0, kvdim = 0, qkvdim = 0, Kmax = 0, Hp = 0;
   // handle-owned weights
   void* wkv_pre = nullptr;  // [L*2*kvdim][d_vlm]: per layer K rows then V rows
   void* wqkv = nullptr;     // [L][qkvdim][D]  (W2A8: packed [L][qkvdim][D/4])
@@ -84,6 +84,19 @@ struct vla_expert {
   float* opart = nullptr;
   float* ml = nullptr;
   int attn_chunk = 0;
+  // fused tensor-core path (bf16): row sums of squares, tcgen05 attention partials
+  bool fused = false;
+  float* ss1 = nullptr;
+  float* ss2 = nullptr;
+  size_t ss_elems = 0;
+  float* aopart = nullptr;
+  float2* aml = nullptr;
+  void* gbuf = nullptr;  // [T][F] bf16 GeLU output (separate from act: the up GEMM may read act)
+  unsigned long long* tl = nullptr;  // event trace buffer (VLA_TIMELINE builds)
+  float* xpart = nullptr;  // split-K partial tiles exchanged through L2
+  float* xss = nullptr;    // per-rank sums of squares exchanged through L2
+  bf16* xo = nullptr;      // attention partial outputs exchanged through L2
+  size_t xpart_elems = 0, xss_elems = 0;
   int* d_status = nullptr;
   int* h_abort = nullptr;
   int* d_abort = nullptr;
@@ -179,6 +192,8 @@ ExpertDims make_dims(const vla_expert* h, int B, int P) {
   d.eps = c.rms_eps; d.qdim = h->qdim; d.kvdim = h->kvdim; d.qkvdim = h->qkvdim;
   d.f32 = h->f32 ? 1 : 0;
   d.w2a8 = h->w2a8 ? 1 : 0;
+  d.P8 = round_up(P, 8);
+  d.Hp = h->Hp;
   return d;
 }
 
@@ -256,6 +271,166 @@ vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B,
   return VLA_OK;
 }
 
+struct LinPlan {
+  int C = 1, KS = 64, BN = 16, tiles_n = 1, tiles_t = 1, stages = 1, bmode = 0;
+};
+
+// Cluster split-K plan: the smallest power-of-two cluster (<= 16) that puts
+// about one CTA on every SM, with the modulated-norm prologue fused when the
+// CTA's B slice fits in shared memory.
+LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
+  LinPlan p;
+  p.BN = T >= 256 ? 256 : round_up(T < 16 ? 16 : T, 16);
+  p.tiles_n = cdiv(N, 128);
+  p.tiles_t = cdiv(T, p.BN);
+  const int tiles = p.tiles_n * p.tiles_t;
+  p.C = 1;
+  while (p.C < 16 && tiles * p.C < h->num_sms && K % (p.C * 2 * 64) == 0) p.C *= 2;
+  p.KS = K / p.C;
+  const int nkb = p.KS / 64;
+  const int b_tile = p.BN * 128;
+  const int b_res = nkb * b_tile;
+  // the in-GEMM norm prologue maps a fixed 8-column chunk to each thread:
+  // KS / 8 must divide 128
+  const int kcs = p.KS / 8;
+  p.bmode = (want_norm && b_res <= 96 * 1024 && kcs <= 128 && 128 % kcs == 0) ? 1 : 0;
+  const int budget = 200 * 1024 - (p.bmode ? b_res : 0);
+  const int per_stage = 128 * 128 + (p.bmode ? 0 : b_tile);
+  int st = budget / per_stage;
+  if (st > 8) st = 8;
+  if (st > nkb) st = nkb;
+  if (st < 1) st = 1;
+  p.stages = st;
+  return p;
+}
+
+LinArgs lin_args(const vla_expert* h, const LinPlan& p, int N, int T, int layer) {
+  LinArgs a{};
+  a.N = N; a.T = T; a.a_row0 = layer * N; a.KS = p.KS; a.BN = p.BN; a.stages = p.stages; a.bmode = p.bmode;
+  a.eps = h->cfg.rms_eps; a.D = h->cfg.width; a.status = h->d_status;
+  a.H = h->cfg.horizon; a.n_q = h->cfg.n_q_heads; a.n_kv = h->cfg.n_kv_heads; a.d_h = h->cfg.head_dim;
+  a.qdim = h->qdim; a.kvdim = h->kvdim; a.Hp = h->Hp;
+  a.xpart = h->xpart; a.xss = h->xss;
+  return a;
+}
+
+// Attention cluster: cs - 1 ranks share the prefix keys (at most 128 each),
+// the last rank takes the action keys.
+int attn_cluster(int P) { return P <= 7 * 128 ? 8 : 16; }
+int attn_kc(int P, int cs) {
+  const int kc = round_up(cdiv(P, cs - 1), 16);
+  return kc < 16 ? 16 : kc;
+}
+
+bool fused_supported(const vla_expert_config& c, bool f32, bool w2a8, bool use_tc) {
+  if (f32 || w2a8 || !use_tc) return false;
+  if (c.head_dim % 64 || c.head_dim > 256 || c.width % 128 || c.horizon > 128) return false;
+  if (c.max_prefix > 15 * 128) return false;
+  if (c.width / 128 > 16) return false;  // sums-of-squares slots read by the norm prologue
+  const int cs = attn_cluster(c.max_prefix);
+  if ((c.head_dim / cs) % 8) return false;
+  const int kc = attn_kc(c.max_prefix, cs);
+  const int kmax = kc > round_up(c.horizon, 16) ? kc : round_up(c.horizon, 16);
+  return attn_tc_smem_bytes(c.head_dim, kmax) <= 227 * 1024;
+}
+
+// The bf16 solver on the fused tensor-core kernels: per layer one QKV GEMM
+// (norm prologue, scatter epilogue), the tcgen05 attention and its combine,
+// the O GEMM (residual epilogue), the up GEMM (norm prologue, GeLU
+// epilogue) and the down GEMM (residual epilogue); every launch uses
+// programmatic dependent launch so weight streaming overlaps the previous
+// kernel.
+vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, int B, int P, const float* noise,
+                                 float* actions, float* tap, cudaStream_t st) {
+  const vla_expert_config& c = h->cfg;
+  const ExpertDims d = make_dims(h, B, P);
+  const StepBufs sb = make_bufs(h, P);
+  const int T = B * c.horizon, D = c.width, F = c.mlp_width, L = c.n_layers;
+  const LinPlan pq = plan_linear(h, h->qkvdim, D, T, true);
+  const LinPlan po = plan_linear(h, D, h->qdim, T, false);
+  const LinPlan pu = plan_linear(h, F, D, T, true);
+  const LinPlan pd = plan_linear(h, D, F, T, false);
+  bf16* act = (bf16*)h->act;
+  CUtensorMap tm_u, tm_o, tm_g;  // activations as B operands
+  if (tc_encode_2d_bf16(&tm_u, act, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_o, act, h->qdim, T, 64, po.BN) ||
+      tc_encode_2d_bf16(&tm_g, h->gbuf, F, T, 64, pd.BN))
+    return VLA_ERR_CUDA;
+  // attention operands
+  const int dh = c.head_dim, nkv = c.n_kv_heads, P8 = d.P8;
+  AttnArgs aa{};
+  aa.B = B; aa.P = P; aa.H = c.horizon; aa.n_q = c.n_q_heads; aa.n_kv = nkv; aa.d_h = dh;
+  aa.group = c.n_q_heads / nkv;
+  aa.n_qt = cdiv(aa.group * c.horizon, 128);
+  aa.cs = attn_cluster(P);
+  aa.kc = attn_kc(P, aa.cs);
+  aa.kc_s = round_up(c.horizon, 16);
+  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
+  aa.o = act; aa.xo = h->xo; aa.status = h->d_status;
+  CUtensorMap tmQ, tmK, tmVt, tmKs, tmVs, tmH;
+  if (tc_encode_2d_bf16(&tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
+      tc_encode_3d_bf16(&tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, aa.kc) ||
+      tc_encode_3d_bf16(&tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh) ||
+      tc_encode_3d_bf16(&tmKs, h->ks, dh, c.horizon, (uint64_t)B * nkv, (uint64_t)dh * 2,
+                        (uint64_t)c.horizon * dh * 2, 64, aa.kc_s) ||
+      tc_encode_3d_bf16(&tmVs, h->vs, c.horizon, dh, (uint64_t)B * nkv, (uint64_t)h->Hp * 2,
+                        (uint64_t)dh * h->Hp * 2, 64, dh) ||
+      tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN))
+    return VLA_ERR_CUDA;
+  const DevCtl ctl{h->d_status, h->d_abort};
+  const float* modt = h->modtab;
+  for (int k = 0; k < h->S; ++k) {
+    const float* x_in = k == 0 ? noise : actions;
+    const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
+    int n_ss = 1;  // slots of ss2 currently valid
+    for (int l = 0; l < L; ++l) {
+      const float* mod = modt + ((size_t)k * L + l) * 4 * D;  // gamma_a, beta_a, gamma_m, beta_m
+#ifdef VLA_TIMELINE
+      // trace step 1, layers 1..4: slot (layer - 1) * 5 + kernel, 4096 CTAs x 16 events each
+      auto tls = [&](int kidx) -> unsigned long long* {
+        return (h->tl && k == 1 && l >= 1 && l <= 4) ? h->tl + ((size_t)((l - 1) * 5 + kidx)) * 4096 * 16 : nullptr;
+      };
+#else
+      auto tls = [&](int) -> unsigned long long* { return nullptr; };
+#endif
+      // QKV
+      LinArgs a = lin_args(h, pq, h->qkvdim, T, l);
+      a.tl = tls(0);
+      a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
+      if (pq.bmode == 1) {
+        a.h_in = h->h; a.ss_in = h->ss2; a.n_ss_in = n_ss; a.gamma = mod; a.beta = mod + D;
+      } else {
+        VLA_CK(launch_modnorm(d, h->h, h->ss2, n_ss, mod, mod + D, act, st));
+      }
+      VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
+      // attention (merged on chip)
+      aa.layer = l;
+      aa.tl = tls(1);
+      VLA_CK(launch_attn_tc(&tmQ, &tmK, &tmVt, &tmKs, &tmVs, aa, st));
+      // O projection + residual
+      a = lin_args(h, po, D, T, l);
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
+      VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
+      // MLP up + GeLU
+      a = lin_args(h, pu, F, T, l);
+      a.epi = EPI_GELU; a.g = (bf16*)h->gbuf; a.ldg = F; a.tl = tls(3);
+      if (pu.bmode == 1) {
+        a.h_in = h->h; a.ss_in = h->ss1; a.n_ss_in = po.tiles_n; a.gamma = mod + 2 * D; a.beta = mod + 3 * D;
+      } else {
+        VLA_CK(launch_modnorm(d, h->h, h->ss1, po.tiles_n, mod + 2 * D, mod + 3 * D, act, st));
+      }
+      VLA_CK(launch_linear(&h->tm_wup, &tm_u, &tmH, a, pu.tiles_n, pu.tiles_t, pu.C, st));
+      // MLP down + residual
+      a = lin_args(h, pd, D, T, l);
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.tl = tls(4);
+      VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
+      n_ss = pd.tiles_n;
+    }
+    VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));
+  }
+  return VLA_OK;
+}
+
 vla_status validate_config(const vla_expert_config* c, int n_steps, bool w2a8) {
   if (!c || n_steps < 1) return VLA_ERR_INVALID_ARG;
   if (c->n_layers < 1 || c->width < 1 || c->mlp_width < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
@@ -296,6 +471,12 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   h->qdim = cfg->n_q_heads * cfg->head_dim;
   h->kvdim = cfg->n_kv_heads * cfg->head_dim;
   h->qkvdim = h->qdim + 2 * h->kvdim;
+  h->Hp = round_up(cfg->horizon, 8);
+  h->fused = fused_supported(*cfg, h->f32, w2a8, h->use_tc);
+#ifdef VLA_TIMELINE
+  VLA_CK(cudaMalloc((void**)&h->tl, (size_t)20 * 4096 * 16 * 8));
+  VLA_CK(cudaMemset(h->tl, 0, (size_t)20 * 4096 * 16 * 8));
+#endif
   h->Kmax = cfg->width;
   if (cfg->mlp_width > h->Kmax) h->Kmax = cfg->mlp_width;
   if (h->qdim > h->Kmax) h->Kmax = h->qdim;
@@ -304,6 +485,8 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   VLA_CK(simt_kernels_init());
   VLA_CK(tc_kernels_init());
   VLA_CK(expert_kernels_init());
+  VLA_CK(linear_kernels_init());
+  VLA_CK(attn_kernels_init());
   VLA_CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
   return VLA_OK;
 }
@@ -365,7 +548,33 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
   if ((s = dalloc(&h->part, pe * 4)) != VLA_OK) return s;
   if ((s = dalloc(&h->q, (size_t)Tm * h->qdim * ae)) != VLA_OK) return s;
   if ((s = dalloc(&h->ks, (size_t)Tm * h->kvdim * ae)) != VLA_OK) return s;
-  if ((s = dalloc(&h->vs, (size_t)Tm * h->kvdim * ae)) != VLA_OK) return s;
+  if ((s = dalloc(&h->vs, (size_t)c.max_batch * h->kvdim * h->Hp * ae)) != VLA_OK) return s;
+  if (h->fused) {
+    // sums of squares: at most one slot per 128-row tile of D, or 1 (embed)
+    h->ss_elems = (size_t)(D / 128 + 1) * Tm;
+    if ((s = dalloc(&h->ss1, h->ss_elems * 4)) != VLA_OK) return s;
+    if ((s = dalloc(&h->ss2, h->ss_elems * 4)) != VLA_OK) return s;
+    if ((s = dalloc(&h->gbuf, (size_t)Tm * c.mlp_width * 2)) != VLA_OK) return s;
+    // split-K exchange buffers: the largest plan over every batch size
+    size_t xp = 0, xs = 0;
+    for (int B = 1; B <= c.max_batch; ++B) {
+      const int T = B * c.horizon;
+      const int dims[4][3] = {{h->qkvdim, D, 1}, {D, h->qdim, 0}, {c.mlp_width, D, 1}, {D, c.mlp_width, 0}};
+      for (auto& g3 : dims) {
+        const LinPlan p = plan_linear(h, g3[0], g3[1], T, g3[2] != 0);
+        const size_t tiles = (size_t)p.tiles_n * p.tiles_t * p.C;
+        if (tiles * p.BN * 128 > xp) xp = tiles * p.BN * 128;
+        if (tiles * p.BN > xs) xs = tiles * p.BN;
+      }
+    }
+    h->xpart_elems = xp;
+    h->xss_elems = xs;
+    if ((s = dalloc(&h->xpart, xp * 4)) != VLA_OK) return s;
+    if ((s = dalloc(&h->xss, xs * 4)) != VLA_OK) return s;
+    const int cs = attn_cluster(c.max_prefix);
+    const size_t qtiles = (size_t)c.max_batch * c.n_kv_heads * cdiv(c.n_q_heads / c.n_kv_heads * c.horizon, 128);
+    if ((s = dalloc(&h->xo, qtiles * cs * 128 * c.head_dim * 2)) != VLA_OK) return s;
+  }
   // attention key-chunk size: largest multiple of 16 (<= 128) whose staging fits
   ExpertDims dd = make_dims(h, 1, c.max_prefix);
   int chunk = 128;
@@ -425,6 +634,14 @@ const char* vla_version(void) { return "0.1.0"; }
 
 const char* vla_last_error(void) { return g_last_error; }
 
+#ifdef VLA_TIMELINE
+// Copies the event trace (20 slots x 4096 CTAs x 16 events, ns) to the host.
+int vla_debug_timeline(vla_expert* h, void* dst, size_t bytes) {
+  if (!h || !h->tl || bytes > (size_t)20 * 4096 * 16 * 8) return 1;
+  return cudaMemcpy(dst, h->tl, bytes, cudaMemcpyDeviceToHost) == cudaSuccess ? 0 : 5;
+}
+#endif
+
 void vla_expert_destroy(vla_expert* h) {
   if (!h) return;
   cudaDeviceSynchronize();
@@ -432,7 +649,7 @@ void vla_expert_destroy(vla_expert* h) {
   void* ptrs[] = {h->wkv_pre, h->wqkv, h->wo,   h->wup,   h->wdown, h->beta,  h->win,     h->wout,
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
-                  h->req_noise, h->req_act};
+                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -559,7 +776,8 @@ vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert
 
 vla_status vla_prefix_cache_bytes(const vla_expert* h, int B, int P, size_t* bytes) {
   if (!h || !bytes || B < 1 || P < 1) return VLA_ERR_INVALID_ARG;
-  *bytes = (size_t)h->cfg.n_layers * B * h->cfg.n_kv_heads * P * h->cfg.head_dim * h->es;
+  // K_C [L][B][n_kv][P][d_h]; V_C^T [L][B][n_kv][d_h][P8] (the larger of the two)
+  *bytes = (size_t)h->cfg.n_layers * B * h->cfg.n_kv_heads * round_up(P, 8) * h->cfg.head_dim * h->es;
   return VLA_OK;
 }
 
@@ -569,7 +787,7 @@ vla_status vla_prefix_kv_build(vla_expert* h, const void* Z, int B, int P, void*
   const vla_expert_config& c = h->cfg;
   cudaStream_t st = (cudaStream_t)stream;
   const int BP = B * P, N = c.n_layers * 2 * h->kvdim, K = c.vlm_hidden;
-  KvScatter kv{Kc, Vc, c.n_layers, B, c.n_kv_heads, P, c.head_dim};
+  KvScatter kv{Kc, Vc, c.n_layers, B, c.n_kv_heads, P, c.head_dim, round_up(P, 8)};
   if (!h->use_tc) {
     VLA_CK(launch_gemm_simt(!h->f32, Z, K, !h->f32, h->wkv_pre, K, BP, N, K, 1, nullptr, 0, 0, &kv, st));
     return VLA_OK;
@@ -594,7 +812,11 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
     return VLA_ERR_INVALID_ARG;
   if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  if (h->cfg.flags & VLA_FLAG_NO_GRAPH) return enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, st);
+  auto enqueue = [&](cudaStream_t s2) {
+    return h->fused ? enqueue_denoise_fused(h, Kc, Vc, B, P, noise, actions, tap, s2)
+                    : enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, s2);
+  };
+  if (h->cfg.flags & VLA_FLAG_NO_GRAPH) return enqueue(st);
   GraphEntry* hit = nullptr;
   for (auto& g : h->graphs)
     if (g.B == B && g.P == P && g.kc == Kc && g.vc == Vc && g.noise == noise && g.actions == actions && g.tap == tap)
@@ -609,7 +831,7 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
     }
     cudaGraph_t graph = nullptr;
     VLA_CK(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
-    vla_status s = enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, h->cap_stream);
+    vla_status s = enqueue(h->cap_stream);
     cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
     if (s != VLA_OK) {
       if (graph) cudaGraphDestroy(graph);
@@ -643,7 +865,16 @@ vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kerne
   // per solver step: embed+norm, then per layer 4 GEMMs, reduce_qkv,
   // attention partials, attention combine, 2 residual/norm reductions (the
   // last layer's second one is the velocity head) and the GeLU reduction.
-  *kernels = h->S * (1 + 10 * h->cfg.n_layers);
+  if (h->fused) {
+    const int T = B * h->cfg.horizon;
+    const int extra = (plan_linear(h, h->qkvdim, h->cfg.width, T, true).bmode == 0) +
+                      (plan_linear(h, h->cfg.mlp_width, h->cfg.width, T, true).bmode == 0);
+    // per step: embed, head; per layer: 4 GEMMs and the attention, plus the
+    // standalone norms when the in-GEMM prologue does not fit
+    *kernels = h->S * (2 + (5 + extra) * h->cfg.n_layers);
+  } else {
+    *kernels = h->S * (1 + 10 * h->cfg.n_layers);
+  }
   return VLA_OK;
 }
 
@@ -670,7 +901,7 @@ vla_status vla_policy_step_host(vla_expert* h, const void* Z_host, int B, int P,
   cudaStream_t st = (cudaStream_t)stream;
   vla_status s;
   if (!h->req_z) {
-    const size_t cache = (size_t)c.n_layers * c.max_batch * c.n_kv_heads * c.max_prefix * c.head_dim * h->es;
+    const size_t cache = (size_t)c.n_layers * c.max_batch * c.n_kv_heads * round_up(c.max_prefix, 8) * c.head_dim * h->es;
     if ((s = dalloc(&h->req_z, (size_t)c.max_batch * c.max_prefix * c.vlm_hidden * h->es)) != VLA_OK ||
         (s = dalloc(&h->req_kc, cache)) != VLA_OK || (s = dalloc(&h->req_vc, cache)) != VLA_OK ||
         (s = dalloc(&h->req_noise, (size_t)c.max_batch * c.horizon * c.action_dim * 4)) != VLA_OK ||

@@ -46,6 +46,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Optional event trace (built only with -DVLA_TIMELINE): thread `who` of each
+// CTA stores %globaltimer for event `ev` (< 16) into tl[cta * 16 + ev].
+#ifdef VLA_TIMELINE
+#define VLA_TL(tl, who, ev)                                                                          \
+  do {                                                                                               \
+    if ((tl) != nullptr && threadIdx.x == (who))                                                     \
+      (tl)[((size_t)blockIdx.x + gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z)) * 16 + (ev)] = \
+          globaltimer_ns();                                                                          \
+  } while (0)
+#else
+#define VLA_TL(tl, who, ev) \
+  do {                      \
+  } while (0)
+#endif
+
 // ---------------------------------------------------------------------------
 // Block reductions (blockDim.x a multiple of 32, <= 1024)
 // ---------------------------------------------------------------------------
@@ -196,6 +211,62 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 
 // ---------------------------------------------------------------------------
+// PTX: thread-block clusters, distributed shared memory, programmatic
+// dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA in the cluster; release/acquire orders the
+// shared-memory writes before the barrier with the reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Wait until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; a no-op without PDL.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the dependent grid start launching (its pre-wait prologue overlaps us).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4_u32(uint32_t saddr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+// Byte offset of the 16-byte chunk `j` (0..7) of row `r` inside a K-major
+// tile of 128-byte rows written with the 128-byte swizzle (the layout TMA
+// produces with CU_TENSOR_MAP_SWIZZLE_128B and sdesc_k128 describes).
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t j) {
+  return r * 128u + ((j ^ (r & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------------------
 // PTX: tcgen05 (5th-generation tensor cores, accumulators in TMEM)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
@@ -244,6 +315,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 32 bit, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tcgen05.ld of 16 columns without the wait: the raw registers must not be
+// read until tmem_wait16() has run on them (that asm takes them as in/out
+// operands, so the compiler cannot hoist a use above the wait).
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+// 2^x with the hardware approximation (relative error ~2^-22), for softmax.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Shared-memory matrix descriptor (tcgen05 format) for a K-major operand tile
 // whose rows are 128 bytes (64 bf16) with the 128-byte swizzle that TMA
 // writes; 8-row core-matrix groups are 1024 bytes apart.  The tile base must
@@ -269,10 +380,11 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
 // ---------------------------------------------------------------------------
 // Host-side launch interfaces (implemented in the kernel translation units)
 // ---------------------------------------------------------------------------
+// K_C [L][B][n_kv][P][d_h]; V_C stored transposed [L][B][n_kv][d_h][P8].
 struct KvScatter {
   void* kc;
   void* vc;
-  int L, B, n_kv, P, d_h;
+  int L, B, n_kv, P, d_h, P8;
 };
 
 struct DevCtl {
@@ -345,9 +457,83 @@ cudaError_t tc_kernels_init();
 cudaError_t expert_kernels_init();
 cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, cudaStream_t st);
 
+// Fused cluster split-K linear layer (k_linear_tc.cu).
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_GELU = 2 };
+struct LinArgs {
+  int N;        // output features (weight rows), multiple of 4
+  int T;        // tokens
+  int a_row0;   // first weight row in the A tensor map (layer offset)
+  int KS;       // K range per cluster rank (multiple of 64); K = C * KS
+  int BN;       // token tile, 16..256, multiple of 16
+  int stages;   // weight ring depth
+  int bmode;    // 0: B tiles by TMA (tmB over [T][K] bf16); 1: B = modulated RMSNorm of h
+  int epi;      // EPI_*
+  // bmode 1 inputs
+  const float* h_in;   // [T][D] residual stream
+  const float* ss_in;  // [n_ss_in][T] partial sums of squares of h rows
+  int n_ss_in;
+  const float* gamma;  // [D]
+  const float* beta;   // [D]
+  float eps;
+  int D;               // width of h (row pitch of h / h_in)
+  // EPI_RESID
+  float* h;            // [T][D]
+  float* ss_out;       // [tiles_n][T]: sums of squares of each 128-row block
+  // EPI_GELU
+  bf16* g;
+  int ldg;
+  // EPI_QKV
+  bf16* q;             // [B][n_q][H][d_h]
+  bf16* ks;            // [B][n_kv][H][d_h]
+  bf16* vst;           // [B][n_kv][d_h][Hp]
+  int H, n_q, n_kv, d_h, qdim, kvdim, Hp;
+  // split-K exchange through L2: [tile][rank][BN][128] fp32 partials and
+  // [tile][rank][BN] per-token sums of squares (tile = tile_t * tiles_n + tile_n)
+  float* xpart;
+  float* xss;
+  int* status;
+  unsigned long long* tl;  // event trace (VLA_TIMELINE builds), else unused
+};
+size_t linear_smem_bytes(const LinArgs& g);
+cudaError_t linear_kernels_init();
+// tmH: fp32 map over h [T][D] with box 64 x BN (no swizzle), used by bmode 1.
+cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& g,
+                          int tiles_n, int tiles_t, int C, cudaStream_t st);
+
+// tcgen05 joint attention (k_attn_tc.cu): a cluster of `cs` CTAs per
+// 128-row query tile of one (observation, K/V head); ranks 0..cs-2 take kc
+// prefix keys each, rank cs-1 the action keys; merged on chip into o.
+struct AttnArgs {
+  int B, P, H, n_q, n_kv, d_h, group;  // group = n_q / n_kv
+  int layer;
+  int n_qt;          // query tiles per (observation, K/V head)
+  int cs;            // cluster size (power of two, 2..16)
+  int kc;            // prefix keys per rank (multiple of 16, <= 128)
+  int kc_s;          // action-key tile (H rounded up to 16, <= 128)
+  float scale_log2;  // log2(e) / sqrt(d_h)
+  bf16* o;           // [B*H][n_q*d_h] output
+  bf16* xo;          // L2 exchange of scaled partial O: [tile][rank][d_h/8][128][8] bf16
+  int* status;
+  unsigned long long* tl;  // event trace (VLA_TIMELINE builds), else unused
+};
+size_t attn_tc_smem_bytes(int d_h, int kc);
+cudaError_t attn_kernels_init();
+// tmQ over q [B*n_q*H][d_h] (box 64 x 128); tmK over K_C {d_h, P, L*B*n_kv}
+// (box 64 x kc); tmVt over V_C^T {P, d_h, L*B*n_kv} (box 64 x d_h); tmKs over
+// k_s {d_h, H, B*n_kv} (box 64 x kc_s); tmVs over v_s^T {H, d_h, B*n_kv}
+// (box 64 x d_h); all bf16 with the 128-byte swizzle.
+cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
+                           const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st);
+int tc_encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                     uint32_t box_rows);
+int tc_encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                      uint64_t stride2_bytes, uint32_t box0, uint32_t box1);
+
 // Expert kernels (k_expert.cu).
 struct ExpertDims {
   int L, D, F, n_q, n_kv, d_h, d_a, H, B, P, S, d_t;
+  int P8;  // P rounded up to a multiple of 8: row pitch of V_C^T
+  int Hp;  // H rounded up to a multiple of 8: row pitch of v_s^T
   float eps;
   int qdim, kvdim, qkvdim;
   int f32;   // 1 when the config dtype is fp32
@@ -369,7 +555,7 @@ struct StepBufs {
   float* part;          // [splits][T][N] GEMM partials
   void* q;              // [B][n_q][H][d_h]
   void* ks;             // [B][n_kv][H][d_h]
-  void* vs;             // [B][n_kv][H][d_h]
+  void* vs;             // [B][n_kv][d_h][Hp] (transposed)
   float* opart;         // attention partial outputs
   float* ml;            // attention partial (max, sum)
   int attn_chunk, n_chunks;
@@ -388,3 +574,13 @@ cudaError_t launch_reduce_norm(const ExpertDims& d, const StepBufs& b, int step,
 cudaError_t launch_reduce_gelu(const ExpertDims& d, const StepBufs& b, int layer, int splits, cudaStream_t st);
 cudaError_t launch_head(const ExpertDims& d, const StepBufs& b, int step, int splits, float dt, const float* x_in,
                         float* x_out, float* tap, cudaStream_t st);
+// Fused-path helpers: h = x W_in^T with its row sums of squares (1 slot);
+// u = modulated RMSNorm of h as bf16 [T][D] (for token tiles too large for
+// the in-GEMM prologue); the velocity head reading h directly.
+cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float* x_in, float* ss_out, DevCtl ctl,
+                            cudaStream_t st);
+cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss, int n_ss, const float* gamma,
+                           const float* beta, bf16* u, cudaStream_t st);
+cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, float dt, const float* x_in,
+                              float* x_out, float* tap, cudaStream_t st);
+

@@ -62,7 +62,8 @@ def gpu_run(cfg, B=None, P=None, flags=0, noise=None, Z=None, max_batch=None, ma
     status = ex.poll_status()
     out = {
         "cfg": c, "w": w, "Z": Z, "noise": noise, "status": status, "expert": ex,
-        "Kc": Kc.float().cpu().numpy(), "Vc": Vc.float().cpu().numpy(),
+        # V_C is stored transposed [L, B, n_kv, d_h, P8]; compare as [.., P, d_h]
+        "Kc": Kc.float().cpu().numpy(), "Vc": Vc[..., :P].transpose(-1, -2).float().cpu().numpy(),
         "act": act.cpu().numpy(), "tap": tap.cpu().numpy(),
     }
     return out
