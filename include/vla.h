@@ -212,7 +212,10 @@ vla_status vla_w2a8_quantize_rows(const float* x_dev, int M, int K, int8_t* a_de
  *   beta       per-tensor fp32 scale
  *   y_dev      [M][N] bf16 (raw uint16 bits) out: bf16_rne((float(acc) * alpha_m) * beta)
  *   acc_dev    NULL or [M][N] int32 out: acc_mn = sum_j a_mj q_nj (exact)
- * K must be a multiple of 64.  Codes are assumed valid (3 is not checked here). */
+ * K must be a multiple of 64 and N of 4.  Codes are assumed valid (3 is not
+ * checked here).  Runs on the tensor cores: the int8 codes are carried exactly
+ * in bf16 and every partial sum is an integer below 2^24, so the fp32
+ * accumulators equal the int32 definition. */
 vla_status vla_w2a8_ternary_gemm(const int8_t* a_dev, const float* alpha_dev, const uint8_t* q_dev,
                                  float beta, int M, int N, int K, uint16_t* y_dev,
                                  int32_t* acc_dev, void* stream);

@@ -302,10 +302,17 @@ __global__ void __launch_bounds__(128, 1)
             sum[2 * u + 1] += __uint_as_float(w[u] & 0xFFFF0000u);
           }
         }
-        uint4 o4;
-        o4.x = pack_bf16x2(sum[0], sum[1]); o4.y = pack_bf16x2(sum[2], sum[3]);
-        o4.z = pack_bf16x2(sum[4], sum[5]); o4.w = pack_bf16x2(sum[6], sum[7]);
-        *(uint4*)(out + (c8 + h) * 8) = o4;
+        if (a.o32) {
+          float4* o32 = (float4*)(a.o32 + ((size_t)b * a.H + i) * (size_t)(a.n_q * dh) + (size_t)j * dh + rank * cols +
+                                  (c8 + h) * 8);
+          o32[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
+          o32[1] = make_float4(sum[4], sum[5], sum[6], sum[7]);
+        } else {
+          uint4 o4;
+          o4.x = pack_bf16x2(sum[0], sum[1]); o4.y = pack_bf16x2(sum[2], sum[3]);
+          o4.z = pack_bf16x2(sum[4], sum[5]); o4.w = pack_bf16x2(sum[6], sum[7]);
+          *(uint4*)(out + (c8 + h) * 8) = o4;
+        }
       }
     }
   }

@@ -401,6 +401,50 @@ __global__ void k_head_fused(ExpertDims d, StepBufs b, int step, float dt, const
   }
 }
 
+// Eq. (4) on the modulated RMSNorm of h: one CTA per token computes the
+// row's rms, u = h / rms * (1 + gamma) + beta, alpha = max(|u|, 1e-5) / 127
+// and the codes (as exact bf16 carriers).
+__global__ void k_quant_norm(int D, float eps, const float* h, const float* gamma, const float* beta, bf16* codes,
+                             float* alpha) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + D;
+  const int t = blockIdx.x;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    const float v = h[(size_t)t * D + i];
+    row[i] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / (float)D + eps);
+  for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = row[i] * r * (1.f + gamma[i]) + beta[i];
+  __syncthreads();
+  const float al = quantize_row_block(row, D, nullptr, codes + (size_t)t * D, red);
+  if (threadIdx.x == 0) alpha[t] = al;
+}
+
+// Eq. (4) on fp32 rows x [T][K].
+__global__ void k_quant_rows(int K, const float* x, bf16* codes, float* alpha) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + K;
+  const int t = blockIdx.x;
+  for (int i = threadIdx.x; i < K; i += blockDim.x) row[i] = x[(size_t)t * K + i];
+  __syncthreads();
+  const float al = quantize_row_block(row, K, nullptr, codes + (size_t)t * K, red);
+  if (threadIdx.x == 0) alpha[t] = al;
+}
+
+__global__ void k_i8_to_bf16(const int8_t* a, bf16* out, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    out[i] = __float2bfloat16_rn((float)a[i]);
+}
+
 template <typename TS>
 __global__ void k_to_f32(const TS* src, float* dst, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
@@ -420,6 +464,10 @@ cudaError_t expert_kernels_init() {
   e = set_max_dyn_smem(k_reduce_gelu<float>);
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_reduce_gelu<bf16>);
+  if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_quant_norm);
+  if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_quant_rows);
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_attn_combine<float>);
   if (e != cudaSuccess) return e;
@@ -464,6 +512,25 @@ cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss,
   float eps = d.eps;
   void* args[] = {&T, &D, &eps, (void*)&h, (void*)&ss, &n_ss, (void*)&gamma, (void*)&beta, &u};
   return launch_pdl((const void*)k_modnorm, dim3(T), dim3(kThreads), 0, st, args);
+}
+
+cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* gamma, const float* beta, bf16* codes,
+                              float* alpha, cudaStream_t st) {
+  int D = d.D;
+  float eps = d.eps;
+  void* args[] = {&D, &eps, (void*)&h, (void*)&gamma, (void*)&beta, &codes, &alpha};
+  return launch_pdl((const void*)k_quant_norm, dim3(d.B * d.H), dim3(512), (size_t)(D + 32) * sizeof(float), st, args);
+}
+
+cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st) {
+  void* args[] = {&K, (void*)&x, &codes, &alpha};
+  return launch_pdl((const void*)k_quant_rows, dim3(T), dim3(512), (size_t)(K + 32) * sizeof(float), st, args);
+}
+
+cudaError_t launch_i8_to_bf16(const int8_t* a, bf16* out, size_t n, cudaStream_t st) {
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  k_i8_to_bf16<<<blocks, 256, 0, st>>>(a, out, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, float dt, const float* x_in,

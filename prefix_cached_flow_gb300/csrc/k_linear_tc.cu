@@ -39,8 +39,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 
 struct LinSmem {
-  uint32_t a, b, hs, region, bars, slot, rstat, gam, bet, total;
+  uint32_t a, b, hs, pk, region, bars, slot, rstat, gam, bet, total;
 };
+constexpr uint32_t kPk = 128 * 16;  // one stage of packed ternary codes: 128 rows x 64 codes
 
 __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   LinSmem s;
@@ -49,11 +50,11 @@ __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   s.a = 0;
   s.b = (uint32_t)g.stages * kA;
   s.hs = s.b + (g.bmode == 0 ? (uint32_t)g.stages * b_tile : nkb * b_tile);
-  uint32_t end = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
-  const uint32_t stage = 128u * (uint32_t)g.BN * 4u;  // epilogue staging [BN][128] fp32
-  s.region = end > stage ? end : stage;
-  s.bars = s.region;                                  // full[NS], empty[NS], done, hbar
-  s.slot = s.bars + (2u * (uint32_t)g.stages + 2u) * 8u;
+  s.pk = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
+  const uint32_t end = s.pk + (g.amode == 1 ? (uint32_t)g.stages * kPk : 0u);
+  s.region = end;
+  s.bars = s.region;                                  // full[NS], empty[NS], done, hbar, aready[NS]
+  s.slot = s.bars + (3u * (uint32_t)g.stages + 2u) * 8u;
   s.rstat = s.slot + 16u;                             // [BN] (also the epilogue's per-token sums)
   s.gam = s.rstat + (uint32_t)g.BN * 4u;              // [KS]
   s.bet = s.gam + (uint32_t)g.KS * 4u;                // [KS]
@@ -73,10 +74,12 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* Abase = smem + Ls.a;
   uint8_t* Bbase = smem + Ls.b;
   float* Hs = (float*)(smem + Ls.hs);
+  uint8_t* Pk = smem + Ls.pk;
   uint64_t* full = (uint64_t*)(smem + Ls.bars);
   uint64_t* empty = full + NS;
   uint64_t* done = empty + NS;
   uint64_t* hbar = done + 1;
+  uint64_t* aready = hbar + 1;  // [NS]: decoded ternary A tile ready (amode 1)
   uint32_t* tmem_slot = (uint32_t*)(smem + Ls.slot);
   float* rstat = (float*)(smem + Ls.rstat);
   float* gam = (float*)(smem + Ls.gam);
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     mbar_init(done, 1);
     mbar_init(hbar, 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&aready[s], 2);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(g.bmode == 0 ? (const void*)&tmB : (const void*)&tmH);
@@ -117,12 +121,19 @@ __global__ void __launch_bounds__(128, 1)
 
   // Weight prefetch: independent of every earlier kernel.
   const int pre = nkb < NS ? nkb : NS;
-  const uint32_t stage_tx = kA + (g.bmode == 0 ? b_tile : 0u);
+  const uint32_t stage_tx = (g.amode == 1 ? kPk : kA) + (g.bmode == 0 ? b_tile : 0u);
+  // A stage i: bf16 tile by TMA, or its 2-bit codes (16 bytes per row per 64 K)
+  auto load_a = [&](int i, int s, uint64_t pol) {
+    if (g.amode == 1)
+      tma_load_2d_hint(Pk + (size_t)s * kPk, &tmA, &full[s], (k0 + i * 64) / 4, g.a_row0 + m0, pol);
+    else
+      tma_load_2d_hint(Abase + (size_t)s * kA, &tmA, &full[s], k0 + i * 64, g.a_row0 + m0, pol);
+  };
   if (warp == 0 && lane == 0) {
     const uint64_t pol = l2_policy_evict_first();
     for (int i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], stage_tx);
-      tma_load_2d_hint(Abase + (size_t)i * kA, &tmA, &full[i], k0 + i * 64, g.a_row0 + m0, pol);
+      load_a(i, i, pol);
     }
   }
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -197,16 +208,45 @@ __global__ void __launch_bounds__(128, 1)
         break;
       }
       mbar_arrive_expect_tx(&full[s], stage_tx);
-      tma_load_2d_hint(Abase + (size_t)s * kA, &tmA, &full[s], k0 + i * 64, g.a_row0 + m0, pol);
+      load_a(i, s, pol);
       if (g.bmode == 0) tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &full[s], k0 + i * 64, t0);
       issued = i + 1;
+    }
+  }
+  if (g.amode == 1 && warp >= 2) {
+    // Warps 2-3: decode each stage's 2-bit codes (code q+1, little-endian
+    // fields) into the bf16 A tile with the 128-byte swizzle the MMA reads.
+    const int dt = threadIdx.x - 64;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % NS;
+      if (!mbar_wait(&full[s], (i / NS) & 1, g.status)) {
+        s_fail = 1;
+        break;
+      }
+      const uint8_t* pk = Pk + (size_t)s * kPk;
+      const uint32_t at = smem_u32(Abase + (size_t)s * kA);
+#pragma unroll 4
+      for (int e = dt; e < 1024; e += 64) {
+        const int r = e >> 3, ch = e & 7;
+        const uint32_t two = *(const uint16_t*)(pk + r * 16 + ch * 2);  // codes of k = 8ch .. 8ch+7
+        uint4 o;
+        o.x = ternary_pair_bf16(two & 0xFu);
+        o.y = ternary_pair_bf16((two >> 4) & 0xFu);
+        o.z = ternary_pair_bf16((two >> 8) & 0xFu);
+        o.w = ternary_pair_bf16((two >> 12) & 0xFu);
+        st_shared_v4_u32(at + sw128_offset((uint32_t)r, (uint32_t)ch), o);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aready[s]);
     }
   }
   if (warp == 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16_f32(128, BN);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % NS;
-      if (s_fail || !mbar_wait(&full[s], (i / NS) & 1, g.status)) {
+      if (s_fail || !mbar_wait(&full[s], (i / NS) & 1, g.status) ||
+          (g.amode == 1 && !mbar_wait(&aready[s], (i / NS) & 1, g.status))) {
         s_fail = 1;
         break;
       }
@@ -286,6 +326,16 @@ __global__ void __launch_bounds__(128, 1)
     const int rloc = rank * RPR + quad * 4;
     const int n = m0 + rloc, t = t0 + col;
     const bool valid = live && t < g.T && n < g.N;
+    const float4 raw = acc;
+    if (g.w2a8 && valid) {
+      // Eq. (4): exact integer accumulators scaled to bf16
+      const int slot = g.epi == EPI_QKV ? (n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2)) : g.beta_slot;
+      const float al = g.alpha[t], be = g.wbeta ? g.wbeta[g.layer * 6 + slot] : g.beta_val;
+      acc.x = w2a8_scale(acc.x, al, be);
+      acc.y = w2a8_scale(acc.y, al, be);
+      acc.z = w2a8_scale(acc.z, al, be);
+      acc.w = w2a8_scale(acc.w, al, be);
+    }
     if (g.epi == EPI_RESID) {
       float ss = 0.f;
       if (valid) {
@@ -299,10 +349,24 @@ __global__ void __launch_bounds__(128, 1)
       if (live && quad == 0) rstat[col] = ss;
     } else if (g.epi == EPI_GELU) {
       if (valid) {
+        if (g.g32) {
+          *(float4*)(g.g32 + (size_t)t * g.ldg + n) =
+              make_float4(gelu_exact(acc.x), gelu_exact(acc.y), gelu_exact(acc.z), gelu_exact(acc.w));
+        } else {
+          uint2 pk;
+          pk.x = pack_bf16x2(gelu_exact(acc.x), gelu_exact(acc.y));
+          pk.y = pack_bf16x2(gelu_exact(acc.z), gelu_exact(acc.w));
+          *(uint2*)(g.g + (size_t)t * g.ldg + n) = pk;
+        }
+      }
+    } else if (g.epi == EPI_W2A8_OUT) {
+      if (valid) {
         uint2 pk;
-        pk.x = pack_bf16x2(gelu_exact(acc.x), gelu_exact(acc.y));
-        pk.y = pack_bf16x2(gelu_exact(acc.z), gelu_exact(acc.w));
-        *(uint2*)(g.g + (size_t)t * g.ldg + n) = pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        *(uint2*)(g.yout + (size_t)t * g.N + n) = pk;
+        if (g.accout)
+          *(int4*)(g.accout + (size_t)t * g.N + n) = make_int4((int)raw.x, (int)raw.y, (int)raw.z, (int)raw.w);
       }
     } else {  // EPI_QKV: a 4-row quad lies inside one head of q, k or v
       if (valid) {
@@ -418,7 +482,8 @@ cudaError_t linear_kernels_init() {
 cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& g,
                           int tiles_n, int tiles_t, int C, cudaStream_t st) {
   if (g.BN < 16 || g.BN > 256 || g.BN % 16 || g.KS % 64 || g.KS < 64 || g.stages < 1 || C < 1 || C > kMaxC ||
-      (C & (C - 1)) || g.N % 4 || (g.bmode == 1 && (g.n_ss_in < 1 || g.n_ss_in > kMaxC)))
+      (C & (C - 1)) || g.N % 4 || (g.bmode == 1 && (g.n_ss_in < 1 || g.n_ss_in > kMaxC)) ||
+      (g.amode == 1 && g.bmode != 0))
     return cudaErrorInvalidValue;
   const size_t smem = linear_smem_bytes(g);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;

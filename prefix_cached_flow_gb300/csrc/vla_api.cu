@@ -92,6 +92,7 @@ struct vla_expert {
   float* aopart = nullptr;
   float2* aml = nullptr;
   void* gbuf = nullptr;  // [T][F] bf16 GeLU output (separate from act: the up GEMM may read act)
+  float* f32buf = nullptr;  // W2A8: fp32 attention / GeLU outputs [T][max(qdim, F)] awaiting quantisation
   unsigned long long* tl = nullptr;  // event trace buffer (VLA_TIMELINE builds)
   float* xpart = nullptr;  // split-K partial tiles exchanged through L2
   float* xss = nullptr;    // per-rank sums of squares exchanged through L2
@@ -278,14 +279,14 @@ struct LinPlan {
 // Cluster split-K plan: the smallest power-of-two cluster (<= 16) that puts
 // about one CTA on every SM, with the modulated-norm prologue fused when the
 // CTA's B slice fits in shared memory.
-LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
+LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool packed) {
   LinPlan p;
   p.BN = T >= 256 ? 256 : round_up(T < 16 ? 16 : T, 16);
   p.tiles_n = cdiv(N, 128);
   p.tiles_t = cdiv(T, p.BN);
   const int tiles = p.tiles_n * p.tiles_t;
   p.C = 1;
-  while (p.C < 16 && tiles * p.C < h->num_sms && K % (p.C * 2 * 64) == 0) p.C *= 2;
+  while (p.C < 16 && tiles * p.C < num_sms && K % (p.C * 2 * 64) == 0) p.C *= 2;
   p.KS = K / p.C;
   const int nkb = p.KS / 64;
   const int b_tile = p.BN * 128;
@@ -295,13 +296,17 @@ LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
   const int kcs = p.KS / 8;
   p.bmode = (want_norm && b_res <= 96 * 1024 && kcs <= 128 && 128 % kcs == 0) ? 1 : 0;
   const int budget = 200 * 1024 - (p.bmode ? b_res : 0);
-  const int per_stage = 128 * 128 + (p.bmode ? 0 : b_tile);
+  const int per_stage = 128 * 128 + (p.bmode ? 0 : b_tile) + (packed ? 128 * 16 : 0);
   int st = budget / per_stage;
   if (st > 8) st = 8;
   if (st > nkb) st = nkb;
   if (st < 1) st = 1;
   p.stages = st;
   return p;
+}
+
+LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
+  return plan_linear_sms(h->num_sms, N, K, T, want_norm && !h->w2a8, h->w2a8);
 }
 
 LinArgs lin_args(const vla_expert* h, const LinPlan& p, int N, int T, int layer) {
@@ -311,6 +316,10 @@ LinArgs lin_args(const vla_expert* h, const LinPlan& p, int N, int T, int layer)
   a.H = h->cfg.horizon; a.n_q = h->cfg.n_q_heads; a.n_kv = h->cfg.n_kv_heads; a.d_h = h->cfg.head_dim;
   a.qdim = h->qdim; a.kvdim = h->kvdim; a.Hp = h->Hp;
   a.xpart = h->xpart; a.xss = h->xss;
+  a.layer = layer;
+  if (h->w2a8) {
+    a.amode = 1; a.w2a8 = 1; a.alpha = h->alpha; a.wbeta = h->beta;
+  }
   return a;
 }
 
@@ -323,10 +332,11 @@ int attn_kc(int P, int cs) {
 }
 
 bool fused_supported(const vla_expert_config& c, bool f32, bool w2a8, bool use_tc) {
-  if (f32 || w2a8 || !use_tc) return false;
+  if (f32 || !use_tc) return false;
+  (void)w2a8;
   if (c.head_dim % 64 || c.head_dim > 256 || c.width % 128 || c.horizon > 128) return false;
   if (c.max_prefix > 15 * 128) return false;
-  if (c.width / 128 > 16) return false;  // sums-of-squares slots read by the norm prologue
+  if (!w2a8 && c.width / 128 > 16) return false;  // sums-of-squares slots read by the norm prologue
   const int cs = attn_cluster(c.max_prefix);
   if ((c.head_dim / cs) % 8) return false;
   const int kc = attn_kc(c.max_prefix, cs);
@@ -425,6 +435,76 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.tl = tls(4);
       VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
       n_ss = pd.tiles_n;
+    }
+    VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));
+  }
+  return VLA_OK;
+}
+
+// The W2A8 solver on the tensor cores: per layer the Eq. (4) row quantiser
+// before each of the four ternary maps (norm + quantise for QKV and up,
+// quantise for the attention and GeLU outputs), the packed-ternary linear
+// kernel with the (acc * alpha) * beta scaling fused into its epilogue, and
+// the tcgen05 attention writing fp32 o for the quantiser.
+vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void* vc, int B, int P, const float* noise,
+                                      float* actions, float* tap, cudaStream_t st) {
+  const vla_expert_config& c = h->cfg;
+  const ExpertDims d = make_dims(h, B, P);
+  const StepBufs sb = make_bufs(h, P);
+  const int T = B * c.horizon, D = c.width, F = c.mlp_width, L = c.n_layers, Q = h->qdim;
+  const LinPlan pq = plan_linear(h, h->qkvdim, D, T, false);
+  const LinPlan po = plan_linear(h, D, Q, T, false);
+  const LinPlan pu = plan_linear(h, F, D, T, false);
+  const LinPlan pd = plan_linear(h, D, F, T, false);
+  bf16* act = (bf16*)h->act;
+  CUtensorMap tm_u, tm_o, tm_g, tmH;
+  if (tc_encode_2d_bf16(&tm_u, act, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_o, act, Q, T, 64, po.BN) ||
+      tc_encode_2d_bf16(&tm_g, act, F, T, 64, pd.BN) || tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN))
+    return VLA_ERR_CUDA;
+  const int dh = c.head_dim, nkv = c.n_kv_heads, P8 = d.P8;
+  AttnArgs aa{};
+  aa.B = B; aa.P = P; aa.H = c.horizon; aa.n_q = c.n_q_heads; aa.n_kv = nkv; aa.d_h = dh;
+  aa.group = c.n_q_heads / nkv;
+  aa.n_qt = cdiv(aa.group * c.horizon, 128);
+  aa.cs = attn_cluster(P);
+  aa.kc = attn_kc(P, aa.cs);
+  aa.kc_s = round_up(c.horizon, 16);
+  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
+  aa.o = act; aa.o32 = h->f32buf; aa.xo = h->xo; aa.status = h->d_status;
+  CUtensorMap tmQ, tmK, tmVt, tmKs, tmVs;
+  if (tc_encode_2d_bf16(&tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
+      tc_encode_3d_bf16(&tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, aa.kc) ||
+      tc_encode_3d_bf16(&tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh) ||
+      tc_encode_3d_bf16(&tmKs, h->ks, dh, c.horizon, (uint64_t)B * nkv, (uint64_t)dh * 2,
+                        (uint64_t)c.horizon * dh * 2, 64, aa.kc_s) ||
+      tc_encode_3d_bf16(&tmVs, h->vs, c.horizon, dh, (uint64_t)B * nkv, (uint64_t)h->Hp * 2,
+                        (uint64_t)dh * h->Hp * 2, 64, dh))
+    return VLA_ERR_CUDA;
+  const DevCtl ctl{h->d_status, h->d_abort};
+  for (int k = 0; k < h->S; ++k) {
+    const float* x_in = k == 0 ? noise : actions;
+    const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
+    for (int l = 0; l < L; ++l) {
+      const float* mod = h->modtab + ((size_t)k * L + l) * 4 * D;
+      VLA_CK(launch_quant_norm(d, h->h, mod, mod + D, act, h->alpha, st));
+      LinArgs a = lin_args(h, pq, h->qkvdim, T, l);
+      a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
+      VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
+      aa.layer = l;
+      VLA_CK(launch_attn_tc(&tmQ, &tmK, &tmVt, &tmKs, &tmVs, aa, st));
+      VLA_CK(launch_quant_rows(T, Q, h->f32buf, act, h->alpha, st));
+      a = lin_args(h, po, D, T, l);
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.beta_slot = 3;
+      VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
+      VLA_CK(launch_quant_norm(d, h->h, mod + 2 * D, mod + 3 * D, act, h->alpha, st));
+      a = lin_args(h, pu, F, T, l);
+      a.epi = EPI_GELU; a.g32 = h->f32buf; a.ldg = F; a.beta_slot = 4;
+      VLA_CK(launch_linear(&h->tm_wup, &tm_u, &tmH, a, pu.tiles_n, pu.tiles_t, pu.C, st));
+      VLA_CK(launch_quant_rows(T, F, h->f32buf, act, h->alpha, st));
+      a = lin_args(h, pd, D, T, l);
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.beta_slot = 5;
+      VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
     }
     VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));
   }
@@ -555,6 +635,8 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
     if ((s = dalloc(&h->ss1, h->ss_elems * 4)) != VLA_OK) return s;
     if ((s = dalloc(&h->ss2, h->ss_elems * 4)) != VLA_OK) return s;
     if ((s = dalloc(&h->gbuf, (size_t)Tm * c.mlp_width * 2)) != VLA_OK) return s;
+    if (h->w2a8 && (s = dalloc(&h->f32buf, (size_t)Tm * (h->qdim > c.mlp_width ? h->qdim : c.mlp_width) * 4)) != VLA_OK)
+      return s;
     // split-K exchange buffers: the largest plan over every batch size
     size_t xp = 0, xs = 0;
     for (int B = 1; B <= c.max_batch; ++B) {
@@ -593,7 +675,13 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
   if (!h->f32) {
     const int N_kv = L * 2 * h->kvdim;
     if (tc_encode_2d_bf16(&h->tm_wkv, h->wkv_pre, c.vlm_hidden, N_kv, 64, 128)) return VLA_ERR_CUDA;
-    if (!h->w2a8) {
+    if (h->w2a8) {
+      if (tc_encode_2d_u8(&h->tm_wqkv, h->wqkv, D / 4, (uint64_t)L * h->qkvdim, 16, 128) ||
+          tc_encode_2d_u8(&h->tm_wo, h->wo, h->qdim / 4, (uint64_t)L * D, 16, 128) ||
+          tc_encode_2d_u8(&h->tm_wup, h->wup, D / 4, (uint64_t)L * c.mlp_width, 16, 128) ||
+          tc_encode_2d_u8(&h->tm_wdown, h->wdown, c.mlp_width / 4, (uint64_t)L * D, 16, 128))
+        return VLA_ERR_CUDA;
+    } else {
       if (tc_encode_2d_bf16(&h->tm_wqkv, h->wqkv, D, (uint64_t)L * h->qkvdim, 64, 128)) return VLA_ERR_CUDA;
       if (tc_encode_2d_bf16(&h->tm_wo, h->wo, h->qdim, (uint64_t)L * D, 64, 128)) return VLA_ERR_CUDA;
       if (tc_encode_2d_bf16(&h->tm_wup, h->wup, D, (uint64_t)L * c.mlp_width, 64, 128)) return VLA_ERR_CUDA;
@@ -649,7 +737,7 @@ void vla_expert_destroy(vla_expert* h) {
   void* ptrs[] = {h->wkv_pre, h->wqkv, h->wo,   h->wup,   h->wdown, h->beta,  h->win,     h->wout,
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
-                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo};
+                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -813,8 +901,10 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
   if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   auto enqueue = [&](cudaStream_t s2) {
-    return h->fused ? enqueue_denoise_fused(h, Kc, Vc, B, P, noise, actions, tap, s2)
-                    : enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, s2);
+    if (h->fused)
+      return h->w2a8 ? enqueue_denoise_w2a8_fused(h, Kc, Vc, B, P, noise, actions, tap, s2)
+                     : enqueue_denoise_fused(h, Kc, Vc, B, P, noise, actions, tap, s2);
+    return enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, s2);
   };
   if (h->cfg.flags & VLA_FLAG_NO_GRAPH) return enqueue(st);
   GraphEntry* hit = nullptr;
@@ -865,7 +955,10 @@ vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kerne
   // per solver step: embed+norm, then per layer 4 GEMMs, reduce_qkv,
   // attention partials, attention combine, 2 residual/norm reductions (the
   // last layer's second one is the velocity head) and the GeLU reduction.
-  if (h->fused) {
+  if (h->fused && h->w2a8) {
+    // per step: embed, head; per layer: 4 quantisers, 4 GEMMs, attention
+    *kernels = h->S * (2 + 9 * h->cfg.n_layers);
+  } else if (h->fused) {
     const int T = B * h->cfg.horizon;
     const int extra = (plan_linear(h, h->qkvdim, h->cfg.width, T, true).bmode == 0) +
                       (plan_linear(h, h->cfg.mlp_width, h->cfg.width, T, true).bmode == 0);
@@ -927,13 +1020,38 @@ vla_status vla_w2a8_quantize_rows(const float* x, int M, int K, int8_t* a, float
 
 vla_status vla_w2a8_ternary_gemm(const int8_t* a, const float* alpha, const uint8_t* q, float beta, int M, int N,
                                  int K, uint16_t* y, int32_t* acc, void* stream) {
-  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64) return VLA_ERR_INVALID_ARG;
+  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64 || N % 4) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  float* part = nullptr;
-  VLA_CK(cudaMallocAsync((void**)&part, (size_t)M * N * sizeof(float), st));
-  cudaError_t e = launch_ternary_simt(a, K, q, M, N, K, 1, part, 0, N, st);
-  if (e == cudaSuccess) e = launch_ternary_finish(part, M, N, alpha, beta, y, acc, st);
-  cudaFreeAsync(part, st);
+  int dev = 0, sms = 0;
+  VLA_CK(cudaGetDevice(&dev));
+  VLA_CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  VLA_CK(simt_kernels_init());
+  VLA_CK(linear_kernels_init());
+  // Tensor cores: int8 codes carried exactly in bf16, ternary codes decoded
+  // to bf16 in shared memory, fp32 accumulation of integers below 2^24.
+  const LinPlan p = plan_linear_sms(sms, N, K, M, false, true);
+  const size_t tiles = (size_t)p.tiles_n * p.tiles_t * p.C;
+  bf16* carriers = nullptr;
+  float* xpart = nullptr;
+  float* xss = nullptr;
+  VLA_CK(cudaMallocAsync((void**)&carriers, (size_t)M * K * 2, st));
+  cudaError_t e = cudaMallocAsync((void**)&xpart, tiles * p.BN * 128 * 4, st);
+  if (e == cudaSuccess) e = cudaMallocAsync((void**)&xss, tiles * p.BN * 4, st);
+  if (e == cudaSuccess) e = launch_i8_to_bf16(a, carriers, (size_t)M * K, st);
+  CUtensorMap tmA, tmB;
+  if (e == cudaSuccess && (tc_encode_2d_u8(&tmA, q, K / 4, N, 16, 128) ||
+                           tc_encode_2d_bf16(&tmB, carriers, K, M, 64, p.BN)))
+    e = cudaErrorInvalidValue;
+  if (e == cudaSuccess) {
+    LinArgs g{};
+    g.N = N; g.T = M; g.a_row0 = 0; g.KS = p.KS; g.BN = p.BN; g.stages = p.stages; g.bmode = 0; g.amode = 1;
+    g.epi = EPI_W2A8_OUT; g.w2a8 = 1; g.alpha = alpha; g.wbeta = nullptr; g.beta_val = beta;
+    g.yout = y; g.accout = acc; g.xpart = xpart; g.xss = xss; g.D = K;
+    e = launch_linear(&tmA, &tmB, &tmB, g, p.tiles_n, p.tiles_t, p.C, st);
+  }
+  if (carriers) cudaFreeAsync(carriers, st);
+  if (xpart) cudaFreeAsync(xpart, st);
+  if (xss) cudaFreeAsync(xss, st);
   VLA_CK(e);
   return VLA_OK;
 }

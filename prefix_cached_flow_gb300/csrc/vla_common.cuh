@@ -123,6 +123,15 @@ __device__ __forceinline__ float w2a8_scale(float acc, float alpha, float beta) 
   return __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(acc, alpha), beta)));
 }
 
+// Two ternary 2-bit codes (c0 in bits 0-1, c1 in bits 2-3; code = q + 1) as
+// a bf16x2 word with q0 in the low half: -1 -> 0xBF80, 0 -> 0, +1 -> 0x3F80.
+__device__ __forceinline__ uint32_t ternary_pair_bf16(uint32_t nib) {
+  const uint32_t c0 = nib & 3u, c1 = nib >> 2;
+  const uint32_t v0 = (c0 == 1u) ? 0u : (0x3F80u | (c0 == 0u ? 0x8000u : 0u));
+  const uint32_t v1 = (c1 == 1u) ? 0u : (0x3F80u | (c1 == 0u ? 0x8000u : 0u));
+  return v0 | (v1 << 16);
+}
+
 __device__ __forceinline__ float gelu_exact(float x) {
   return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
 }
@@ -458,7 +467,7 @@ cudaError_t expert_kernels_init();
 cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, cudaStream_t st);
 
 // Fused cluster split-K linear layer (k_linear_tc.cu).
-enum { EPI_QKV = 0, EPI_RESID = 1, EPI_GELU = 2 };
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_GELU = 2, EPI_W2A8_OUT = 3 };
 struct LinArgs {
   int N;        // output features (weight rows), multiple of 4
   int T;        // tokens
@@ -467,7 +476,18 @@ struct LinArgs {
   int BN;       // token tile, 16..256, multiple of 16
   int stages;   // weight ring depth
   int bmode;    // 0: B tiles by TMA (tmB over [T][K] bf16); 1: B = modulated RMSNorm of h
+  int amode;    // 0: A (weights) bf16 by TMA; 1: packed 2-bit ternary codes by TMA, decoded to bf16 in smem
   int epi;      // EPI_*
+  // W2A8 (Eq. 4): the accumulators are exact integers; y = bf16((acc * alpha_t) * beta)
+  int w2a8;
+  const float* alpha;  // [T] per-token activation scales
+  const float* wbeta;  // [L][6] per-tensor weight scales (q, k, v, o, up, down); null: beta_val
+  float beta_val;
+  int layer;
+  int beta_slot;       // 3 (o), 4 (up), 5 (down); QKV picks 0/1/2 by output row
+  float* g32;          // EPI_GELU with W2A8: fp32 GeLU output [T][ldg] (quantised next)
+  uint16_t* yout;      // EPI_W2A8_OUT: bf16 bits [T][N]
+  int32_t* accout;     // EPI_W2A8_OUT: int32 accumulators [T][N] (nullable)
   // bmode 1 inputs
   const float* h_in;   // [T][D] residual stream
   const float* ss_in;  // [n_ss_in][T] partial sums of squares of h rows
@@ -513,6 +533,7 @@ struct AttnArgs {
   float scale_log2;  // log2(e) / sqrt(d_h)
   bf16* o;           // [B*H][n_q*d_h] output
   bf16* xo;          // L2 exchange of scaled partial O: [tile][rank][d_h/8][128][8] bf16
+  float* o32;        // when set, o is written in fp32 here instead of bf16 (W2A8 quantises it next)
   int* status;
   unsigned long long* tl;  // event trace (VLA_TIMELINE builds), else unused
 };
@@ -526,6 +547,9 @@ cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const
                            const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st);
 int tc_encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                      uint32_t box_rows);
+// uint8 map (no swizzle) over packed ternary codes [rows][inner bytes].
+int tc_encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows);
 int tc_encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
                       uint64_t stride2_bytes, uint32_t box0, uint32_t box1);
 
@@ -583,4 +607,11 @@ cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss,
                            const float* beta, bf16* u, cudaStream_t st);
 cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, float dt, const float* x_in,
                               float* x_out, float* tap, cudaStream_t st);
+// W2A8 row quantisers (Eq. 4): bf16 carriers of the int8 codes [T][K] and
+// alpha [T].  quant_norm quantises the modulated RMSNorm of h (computing the
+// row's rms itself); quant_rows quantises fp32 rows x [T][K].
+cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* gamma, const float* beta, bf16* codes,
+                              float* alpha, cudaStream_t st);
+cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st);
+cudaError_t launch_i8_to_bf16(const int8_t* a, bf16* out, size_t n, cudaStream_t st);
 
