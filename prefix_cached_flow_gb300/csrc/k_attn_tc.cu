@@ -54,6 +54,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+template <bool O32>
 __global__ void __launch_bounds__(128, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmKs,
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(128, 1)
             sum[2 * u + 1] += __uint_as_float(w[u] & 0xFFFF0000u);
           }
         }
-        if (a.o32) {
+        if (O32) {
           float4* o32 = (float4*)(a.o32 + ((size_t)b * a.H + i) * (size_t)(a.n_q * dh) + (size_t)j * dh + rank * cols +
                                   (c8 + h) * 8);
           o32[0] = make_float4(sum[0], sum[1], sum[2], sum[3]);
@@ -333,8 +334,10 @@ __global__ void __launch_bounds__(128, 1)
 size_t attn_tc_smem_bytes(int d_h, int kc) { return 1024 + attn_layout(d_h, kc).total; }
 
 cudaError_t attn_kernels_init() {
-  cudaError_t e = set_max_dyn_smem(k_attn_tc);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = set_max_dyn_smem(k_attn_tc<false>);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_tc<true>);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
@@ -360,5 +363,6 @@ cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_attn_tc, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_tc<true>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  return cudaLaunchKernelEx(&cfg, k_attn_tc<false>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
 }

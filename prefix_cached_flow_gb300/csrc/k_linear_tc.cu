@@ -39,7 +39,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 
 struct LinSmem {
-  uint32_t a, b, hs, pk, region, bars, slot, rstat, gam, bet, total;
+  uint32_t a, b, hs, pk, region, bars, slot, rstat, gam, bet, wss, total;
 };
 constexpr uint32_t kPk = 128 * 16;  // one stage of packed ternary codes: 128 rows x 64 codes
 
@@ -53,18 +53,23 @@ __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   s.pk = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
   const uint32_t end = s.pk + (g.amode == 1 ? (uint32_t)g.stages * kPk : 0u);
   s.region = end;
-  s.bars = s.region;                                  // full[NS], empty[NS], done, hbar, aready[NS]
-  s.slot = s.bars + (3u * (uint32_t)g.stages + 2u) * 8u;
+  s.bars = s.region;                                  // full, empty, done, hbar, aready, bfull
+  s.slot = s.bars + (4u * (uint32_t)g.stages + 2u) * 8u;
   s.rstat = s.slot + 16u;                             // [BN] (also the epilogue's per-token sums)
   s.gam = s.rstat + (uint32_t)g.BN * 4u;              // [KS]
   s.bet = s.gam + (uint32_t)g.KS * 4u;                // [KS]
-  s.total = s.bet + (uint32_t)g.KS * 4u;
+  s.wss = s.bet + (uint32_t)g.KS * 4u;                // [4][BN] per-warp sums of squares (C == 1)
+  s.total = s.wss + 4u * (uint32_t)g.BN * 4u;
   return s;
 }
 
+template <int EPI, int AMODE, int BMODE, bool SPLIT>
 __global__ void __launch_bounds__(128, 1)
     k_linear(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmH, const LinArgs g) {
+  // EPI, AMODE (1: packed ternary weights, W2A8 scaling), BMODE and SPLIT
+  // (cluster size > 1) are compile-time so that every instantiation carries
+  // only its own path.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const LinSmem Ls = lin_layout(g);
@@ -80,6 +85,7 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t* done = empty + NS;
   uint64_t* hbar = done + 1;
   uint64_t* aready = hbar + 1;  // [NS]: decoded ternary A tile ready (amode 1)
+  uint64_t* bfull = aready + NS; // [NS]: B tile landed (amode 1; amode 0 uses full[])
   uint32_t* tmem_slot = (uint32_t*)(smem + Ls.slot);
   float* rstat = (float*)(smem + Ls.rstat);
   float* gam = (float*)(smem + Ls.gam);
@@ -104,10 +110,13 @@ __global__ void __launch_bounds__(128, 1)
     }
     mbar_init(done, 1);
     mbar_init(hbar, 1);
-    for (int s = 0; s < NS; ++s) mbar_init(&aready[s], 2);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&aready[s], 2);
+      mbar_init(&bfull[s], 1);
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(g.bmode == 0 ? (const void*)&tmB : (const void*)&tmH);
+    tma_prefetch_desc(BMODE == 0 ? (const void*)&tmB : (const void*)&tmH);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, ncols);
@@ -121,10 +130,13 @@ __global__ void __launch_bounds__(128, 1)
 
   // Weight prefetch: independent of every earlier kernel.
   const int pre = nkb < NS ? nkb : NS;
-  const uint32_t stage_tx = (g.amode == 1 ? kPk : kA) + (g.bmode == 0 ? b_tile : 0u);
+  // full[s] carries the A stage (and, for bf16 weights with TMA'd tokens, the
+  // B stage); packed ternary stages put their B tile on bfull[s] instead, so
+  // the codes can be decoded before the previous kernel has finished.
+  const uint32_t stage_tx = AMODE == 1 ? kPk : kA + (BMODE == 0 ? b_tile : 0u);
   // A stage i: bf16 tile by TMA, or its 2-bit codes (16 bytes per row per 64 K)
   auto load_a = [&](int i, int s, uint64_t pol) {
-    if (g.amode == 1)
+    if (AMODE == 1)
       tma_load_2d_hint(Pk + (size_t)s * kPk, &tmA, &full[s], (k0 + i * 64) / 4, g.a_row0 + m0, pol);
     else
       tma_load_2d_hint(Abase + (size_t)s * kA, &tmA, &full[s], k0 + i * 64, g.a_row0 + m0, pol);
@@ -137,19 +149,55 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
   if (threadIdx.x == 0) griddep_launch_dependents();
-  griddep_wait();
+  const bool decoder = AMODE == 1 && warp >= 2;
+  if (decoder) {
+    // Warps 2-3: decode each stage's 2-bit codes (code q+1, little-endian
+    // fields) into the bf16 A tile with the 128-byte swizzle the MMA reads.
+    // Weights only: this starts before griddepcontrol.wait.
+    const int dt = threadIdx.x - 64;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % NS;
+      if (!mbar_wait(&full[s], (i / NS) & 1, g.status)) {
+        s_fail = 1;
+        break;
+      }
+      const uint8_t* pk = Pk + (size_t)s * kPk;
+      const uint32_t at = smem_u32(Abase + (size_t)s * kA);
+#pragma unroll 4
+      for (int e = dt; e < 1024; e += 64) {
+        const int r = e >> 3, ch = e & 7;
+        const uint32_t two = *(const uint16_t*)(pk + r * 16 + ch * 2);  // codes of k = 8ch .. 8ch+7
+        uint4 o;
+        o.x = ternary_pair_bf16(two & 0xFu);
+        o.y = ternary_pair_bf16((two >> 4) & 0xFu);
+        o.z = ternary_pair_bf16((two >> 8) & 0xFu);
+        o.w = ternary_pair_bf16((two >> 12) & 0xFu);
+        st_shared_v4_u32(at + sw128_offset((uint32_t)r, (uint32_t)ch), o);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aready[s]);
+    }
+  } else {
+    griddep_wait();
+  }
   VLA_TL(g.tl, 0, 2);
 
   int issued = pre;
   if (warp == 0 && lane == 0) {
-    if (g.bmode == 1) {
+    if (BMODE == 1) {
       mbar_arrive_expect_tx(hbar, (uint32_t)nkb * (uint32_t)BN * 256u);
       for (int i = 0; i < nkb; ++i) tma_load_2d(Hs + (size_t)i * BN * 64, &tmH, hbar, k0 + i * 64, t0);
+    } else if (AMODE == 1) {
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&bfull[i], b_tile);
+        tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &bfull[i], k0 + i * 64, t0);
+      }
     } else {
       for (int i = 0; i < pre; ++i) tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &full[i], k0 + i * 64, t0);
     }
   }
-  if (g.bmode == 1) {
+  if (BMODE == 1) {
     // All four warps: B slice = modulated RMSNorm of h over this rank's K
     // range.  Thread tid always handles the same 8-column chunk kc (so its
     // gamma / beta stay in registers) for tokens t = tid / kcs + j * (128 / kcs).
@@ -209,36 +257,13 @@ __global__ void __launch_bounds__(128, 1)
       }
       mbar_arrive_expect_tx(&full[s], stage_tx);
       load_a(i, s, pol);
-      if (g.bmode == 0) tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &full[s], k0 + i * 64, t0);
+      if (AMODE == 1) {
+        mbar_arrive_expect_tx(&bfull[s], b_tile);
+        tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &bfull[s], k0 + i * 64, t0);
+      } else if (BMODE == 0) {
+        tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &full[s], k0 + i * 64, t0);
+      }
       issued = i + 1;
-    }
-  }
-  if (g.amode == 1 && warp >= 2) {
-    // Warps 2-3: decode each stage's 2-bit codes (code q+1, little-endian
-    // fields) into the bf16 A tile with the 128-byte swizzle the MMA reads.
-    const int dt = threadIdx.x - 64;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % NS;
-      if (!mbar_wait(&full[s], (i / NS) & 1, g.status)) {
-        s_fail = 1;
-        break;
-      }
-      const uint8_t* pk = Pk + (size_t)s * kPk;
-      const uint32_t at = smem_u32(Abase + (size_t)s * kA);
-#pragma unroll 4
-      for (int e = dt; e < 1024; e += 64) {
-        const int r = e >> 3, ch = e & 7;
-        const uint32_t two = *(const uint16_t*)(pk + r * 16 + ch * 2);  // codes of k = 8ch .. 8ch+7
-        uint4 o;
-        o.x = ternary_pair_bf16(two & 0xFu);
-        o.y = ternary_pair_bf16((two >> 4) & 0xFu);
-        o.z = ternary_pair_bf16((two >> 8) & 0xFu);
-        o.w = ternary_pair_bf16((two >> 12) & 0xFu);
-        st_shared_v4_u32(at + sw128_offset((uint32_t)r, (uint32_t)ch), o);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&aready[s]);
     }
   }
   if (warp == 1 && lane == 0) {
@@ -246,14 +271,15 @@ __global__ void __launch_bounds__(128, 1)
     for (int i = 0; i < nkb; ++i) {
       const int s = i % NS;
       if (s_fail || !mbar_wait(&full[s], (i / NS) & 1, g.status) ||
-          (g.amode == 1 && !mbar_wait(&aready[s], (i / NS) & 1, g.status))) {
+          (AMODE == 1 && (!mbar_wait(&aready[s], (i / NS) & 1, g.status) ||
+                            !mbar_wait(&bfull[s], (i / NS) & 1, g.status)))) {
         s_fail = 1;
         break;
       }
       if (i == 0) VLA_TL(g.tl, 32, 3);
       tc_fence_after();
       const uint32_t a_addr = smem_u32(Abase + (size_t)s * kA);
-      const uint32_t b_addr = smem_u32(Bbase + (size_t)(g.bmode == 0 ? s : i) * b_tile);
+      const uint32_t b_addr = smem_u32(Bbase + (size_t)(BMODE == 0 ? s : i) * b_tile);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_bf16(tmem, sdesc_k128(a_addr + k * 32), sdesc_k128(b_addr + k * 32), idesc, (i > 0 || k > 0) ? 1u : 0u);
@@ -263,6 +289,7 @@ __global__ void __launch_bounds__(128, 1)
     VLA_TL(g.tl, 32, 4);
   }
   __syncwarp();
+  if (decoder) griddep_wait();  // the epilogue reads and writes activations
 
   // Epilogue geometry: rank r owns rows [r*RPR, (r+1)*RPR) of the tile.
   const int RPR = 128 / C;
@@ -271,7 +298,7 @@ __global__ void __launch_bounds__(128, 1)
   const int iters = (nquads + 127) / 128;
   // Prefetch the residual rows this thread will update (independent of the MMA).
   float4 hpre[kPre];
-  if (g.epi == EPI_RESID) {
+  if (EPI == EPI_RESID) {
 #pragma unroll
     for (int it = 0; it < kPre; ++it) {
       const int f = threadIdx.x + it * 128;
@@ -284,8 +311,6 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
 
-  // Publish the fp32 partial tile through L2, column-major [col][row]
-  // (padding token columns are skipped).
   if (!mbar_wait(done, 0, g.status)) s_fail = 1;
   tc_fence_after();
   __syncthreads();
@@ -293,6 +318,76 @@ __global__ void __launch_bounds__(128, 1)
   const bool ok = (s_fail == 0);
   const int tile = blockIdx.y * gridDim.x + blockIdx.x;
   const int tcols = (g.T - t0) < BN ? (g.T - t0) : BN;  // valid token columns
+
+  if (!SPLIT) {
+    // No split: every thread owns one output row n and applies the epilogue
+    // straight from TMEM (lanes hold consecutive rows: coalesced stores).
+    const int row = warp * 32 + lane;
+    const int n = m0 + row;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    float* wss = (float*)(smem + Ls.wss);
+    int slot = g.beta_slot;
+    if (EPI == EPI_QKV) slot = n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2);
+    const float be = AMODE == 1 ? (g.wbeta ? g.wbeta[g.layer * 6 + slot] : g.beta_val) : 0.f;
+    for (int c0 = 0; c0 < tcols; c0 += 16) {
+      float v[16];
+      if (ok) {
+        tmem_ld16(taddr + (uint32_t)c0, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int t = t0 + c0 + j;
+        const bool valid = ok && c0 + j < tcols && n < g.N;
+        float y = v[j];
+        if (AMODE == 1 && valid) y = w2a8_scale(y, g.alpha[t], be);
+        float sq = 0.f;
+        if (valid) {
+          if (EPI == EPI_RESID) {
+            float* hp = g.h + (size_t)t * g.D + n;
+            const float hv = *hp + y;
+            *hp = hv;
+            sq = hv * hv;
+          } else if (EPI == EPI_GELU) {
+            if (g.g32)
+              g.g32[(size_t)t * g.ldg + n] = gelu_exact(y);
+            else
+              g.g[(size_t)t * g.ldg + n] = __float2bfloat16_rn(gelu_exact(y));
+          } else if (EPI == EPI_W2A8_OUT) {
+            g.yout[(size_t)t * g.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            if (g.accout) g.accout[(size_t)t * g.N + n] = (int32_t)v[j];
+          } else {  // EPI_QKV
+            const int b = t / g.H, i = t - b * g.H;
+            const bf16 bv = __float2bfloat16_rn(y);
+            if (slot == 0) {
+              const int jh = n / g.d_h, d = n - jh * g.d_h;
+              g.q[(((size_t)b * g.n_q + jh) * g.H + i) * g.d_h + d] = bv;
+            } else if (slot == 1) {
+              const int r = n - g.qdim, gk = r / g.d_h, d = r - gk * g.d_h;
+              g.ks[(((size_t)b * g.n_kv + gk) * g.H + i) * g.d_h + d] = bv;
+            } else {
+              const int r = n - g.qdim - g.kvdim, gk = r / g.d_h, d = r - gk * g.d_h;
+              g.vst[(((size_t)b * g.n_kv + gk) * g.d_h + d) * g.Hp + i] = bv;
+            }
+          }
+        }
+        if (EPI == EPI_RESID) {
+          sq = warp_sum(sq);
+          if (lane == 0) wss[warp * BN + c0 + j] = sq;
+        }
+      }
+    }
+    if (EPI == EPI_RESID) {
+      __syncthreads();
+      for (int col = threadIdx.x; col < tcols; col += 128)
+        g.ss_out[(size_t)blockIdx.x * g.T + t0 + col] =
+            wss[col] + wss[BN + col] + wss[2 * BN + col] + wss[3 * BN + col];
+    }
+  } else {
+  // Publish the fp32 partial tile through L2, column-major [col][row]
+  // (padding token columns are skipped).
   float* mypart = g.xpart + ((size_t)tile * C + rank) * (size_t)BN * 128;
   if (ok) {
     const int row = warp * 32 + lane;
@@ -327,16 +422,16 @@ __global__ void __launch_bounds__(128, 1)
     const int n = m0 + rloc, t = t0 + col;
     const bool valid = live && t < g.T && n < g.N;
     const float4 raw = acc;
-    if (g.w2a8 && valid) {
+    if (AMODE == 1 && valid) {
       // Eq. (4): exact integer accumulators scaled to bf16
-      const int slot = g.epi == EPI_QKV ? (n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2)) : g.beta_slot;
+      const int slot = EPI == EPI_QKV ? (n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2)) : g.beta_slot;
       const float al = g.alpha[t], be = g.wbeta ? g.wbeta[g.layer * 6 + slot] : g.beta_val;
       acc.x = w2a8_scale(acc.x, al, be);
       acc.y = w2a8_scale(acc.y, al, be);
       acc.z = w2a8_scale(acc.z, al, be);
       acc.w = w2a8_scale(acc.w, al, be);
     }
-    if (g.epi == EPI_RESID) {
+    if (EPI == EPI_RESID) {
       float ss = 0.f;
       if (valid) {
         float4* hp = (float4*)(g.h + (size_t)t * g.D + n);
@@ -347,7 +442,7 @@ __global__ void __launch_bounds__(128, 1)
       }
       for (int o = qpc >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (live && quad == 0) rstat[col] = ss;
-    } else if (g.epi == EPI_GELU) {
+    } else if (EPI == EPI_GELU) {
       if (valid) {
         if (g.g32) {
           *(float4*)(g.g32 + (size_t)t * g.ldg + n) =
@@ -359,7 +454,7 @@ __global__ void __launch_bounds__(128, 1)
           *(uint2*)(g.g + (size_t)t * g.ldg + n) = pk;
         }
       }
-    } else if (g.epi == EPI_W2A8_OUT) {
+    } else if (EPI == EPI_W2A8_OUT) {
       if (valid) {
         uint2 pk;
         pk.x = pack_bf16x2(acc.x, acc.y);
@@ -416,8 +511,8 @@ __global__ void __launch_bounds__(128, 1)
       a0.x += v0[c].x; a0.y += v0[c].y; a0.z += v0[c].z; a0.w += v0[c].w;
       a1.x += v1[c].x; a1.y += v1[c].y; a1.z += v1[c].z; a1.w += v1[c].w;
     }
-    if (iters >= 1) epilogue(a0, lv0, cl0, qd0, hpre[0], g.epi == EPI_RESID);
-    if (iters >= 2) epilogue(a1, lv1, cl1, qd1, hpre[1], g.epi == EPI_RESID);
+    if (iters >= 1) epilogue(a0, lv0, cl0, qd0, hpre[0], EPI == EPI_RESID);
+    if (iters >= 2) epilogue(a1, lv1, cl1, qd1, hpre[1], EPI == EPI_RESID);
   }
   for (int it = 2; it < iters; ++it) {
     bool live;
@@ -437,7 +532,7 @@ __global__ void __launch_bounds__(128, 1)
     epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false);
   }
   VLA_TL(g.tl, 0, 11);
-  if (g.epi == EPI_RESID) {
+  if (EPI == EPI_RESID) {
     // Rank 0 combines the ranks' per-token sums of squares (fixed order).
     __syncthreads();
     float* myss = g.xss + ((size_t)tile * C + rank) * BN;
@@ -456,12 +551,16 @@ __global__ void __launch_bounds__(128, 1)
       }
     }
   }
+  }  // C > 1
 
   // Drain own TMA copies (only relevant after a timeout) and free TMEM.
   if (warp == 0 && lane == 0) {
     const int first = issued > NS ? issued - NS : 0;
-    for (int i = first; i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, g.status);
-    if (g.bmode == 1) mbar_wait(hbar, 0, g.status);
+    for (int i = first; i < issued; ++i) {
+      mbar_wait(&full[i % NS], (i / NS) & 1, g.status);
+      if (AMODE == 1) mbar_wait(&bfull[i % NS], (i / NS) & 1, g.status);
+    }
+    if (BMODE == 1) mbar_wait(hbar, 0, g.status);
   }
   tc_fence_before();
   __syncthreads();
@@ -473,9 +572,28 @@ __global__ void __launch_bounds__(128, 1)
 
 size_t linear_smem_bytes(const LinArgs& g) { return 1024 + lin_layout(g).total; }
 
+template <int EPI, int AMODE, int BMODE>
+cudaError_t init_one() {
+  cudaError_t e = set_max_dyn_smem(k_linear<EPI, AMODE, BMODE, false>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear<EPI, AMODE, BMODE, true>);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_linear<EPI, AMODE, BMODE, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
 cudaError_t linear_kernels_init() {
-  cudaError_t e = set_max_dyn_smem(k_linear);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_linear, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaSuccess;
+  // bf16 weights: every epilogue with TMA'd or norm-built tokens
+  if (e == cudaSuccess) e = init_one<EPI_QKV, 0, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_QKV, 0, 1>();
+  if (e == cudaSuccess) e = init_one<EPI_RESID, 0, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_GELU, 0, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_GELU, 0, 1>();
+  // packed ternary weights (W2A8)
+  if (e == cudaSuccess) e = init_one<EPI_QKV, 1, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_RESID, 1, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_GELU, 1, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_W2A8_OUT, 1, 0>();
   return e;
 }
 
@@ -483,10 +601,24 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
                           int tiles_n, int tiles_t, int C, cudaStream_t st) {
   if (g.BN < 16 || g.BN > 256 || g.BN % 16 || g.KS % 64 || g.KS < 64 || g.stages < 1 || C < 1 || C > kMaxC ||
       (C & (C - 1)) || g.N % 4 || (g.bmode == 1 && (g.n_ss_in < 1 || g.n_ss_in > kMaxC)) ||
-      (g.amode == 1 && g.bmode != 0))
+      (g.amode == 1 && g.bmode != 0) || (g.amode == 1) != (g.w2a8 == 1))
     return cudaErrorInvalidValue;
   const size_t smem = linear_smem_bytes(g);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  void (*fn)(CUtensorMap, CUtensorMap, CUtensorMap, LinArgs) = nullptr;
+#define VLA_LIN_CASE(E, A, B) \
+  if (g.epi == E && g.amode == A && g.bmode == B) fn = C > 1 ? k_linear<E, A, B, true> : k_linear<E, A, B, false>;
+  VLA_LIN_CASE(EPI_QKV, 0, 0)
+  VLA_LIN_CASE(EPI_QKV, 0, 1)
+  VLA_LIN_CASE(EPI_RESID, 0, 0)
+  VLA_LIN_CASE(EPI_GELU, 0, 0)
+  VLA_LIN_CASE(EPI_GELU, 0, 1)
+  VLA_LIN_CASE(EPI_QKV, 1, 0)
+  VLA_LIN_CASE(EPI_RESID, 1, 0)
+  VLA_LIN_CASE(EPI_GELU, 1, 0)
+  VLA_LIN_CASE(EPI_W2A8_OUT, 1, 0)
+#undef VLA_LIN_CASE
+  if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_t, C);
   cfg.blockDim = dim3(128, 1, 1);
@@ -501,5 +633,5 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_linear, *tmA, *tmB, *tmH, g);
+  return cudaLaunchKernelEx(&cfg, fn, *tmA, *tmB, *tmH, g);
 }
