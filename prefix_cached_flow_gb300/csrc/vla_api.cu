@@ -122,6 +122,12 @@ vla_status cuda_status(cudaError_t e) {
   return VLA_ERR_CUDA;
 }
 
+#define VLA_ST(expr)              \
+  do {                            \
+    const vla_status _s = (expr); \
+    if (_s != VLA_OK) return _s;  \
+  } while (0)
+
 #define VLA_CK(expr)                                   \
   do {                                                 \
     cudaError_t _e = (expr);                           \
@@ -344,6 +350,60 @@ bool fused_supported(const vla_expert_config& c, bool f32, bool w2a8, bool use_t
   return attn_tc_smem_bytes(c.head_dim, kmax) <= 227 * 1024;
 }
 
+// Attention for one solve: the kernel form, its arguments and tensor maps.
+// The streaming kernel (one CTA per query tile, all keys) is used when the
+// query tiles alone occupy a fifth of the SMs; otherwise the clustered kernel
+// spreads each tile's keys over a cluster.  VLA_FLAG_ATTN_SPLIT /
+// VLA_FLAG_ATTN_STREAM force one form.
+struct AttnPlan {
+  bool stream;
+  AttnArgs aa;
+  CUtensorMap tmQ, tmK, tmVt, tmKs, tmVs;
+};
+
+vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, const void* vc, void* o, float* o32,
+                          AttnPlan* ap) {
+  const vla_expert_config& c = h->cfg;
+  const int dh = c.head_dim, nkv = c.n_kv_heads, L = c.n_layers, P8 = round_up(P, 8);
+  AttnArgs& aa = ap->aa;
+  aa = AttnArgs{};
+  aa.B = B; aa.P = P; aa.H = c.horizon; aa.n_q = c.n_q_heads; aa.n_kv = nkv; aa.d_h = dh;
+  aa.group = c.n_q_heads / nkv;
+  aa.n_qt = cdiv(aa.group * c.horizon, 128);
+  aa.cs = attn_cluster(P);
+  aa.kc = attn_kc(P, aa.cs);
+  aa.kc_s = round_up(c.horizon, 16);
+  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
+  aa.o = (bf16*)o; aa.o32 = o32; aa.xo = h->xo; aa.status = h->d_status;
+  const unsigned fl = c.flags;
+  ap->stream = (fl & VLA_FLAG_ATTN_STREAM) ||
+               (!(fl & VLA_FLAG_ATTN_SPLIT) && B * nkv * aa.n_qt * 5 >= h->num_sms);
+  const uint32_t krows = ap->stream ? 64u : (uint32_t)aa.kc, ksrows = ap->stream ? 64u : (uint32_t)aa.kc_s;
+  if (tc_encode_2d_bf16(&ap->tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
+      tc_encode_3d_bf16(&ap->tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64,
+                        krows) ||
+      tc_encode_3d_bf16(&ap->tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64,
+                        dh) ||
+      tc_encode_3d_bf16(&ap->tmKs, h->ks, dh, c.horizon, (uint64_t)B * nkv, (uint64_t)dh * 2,
+                        (uint64_t)c.horizon * dh * 2, 64, ksrows) ||
+      tc_encode_3d_bf16(&ap->tmVs, h->vs, c.horizon, dh, (uint64_t)B * nkv, (uint64_t)h->Hp * 2,
+                        (uint64_t)dh * h->Hp * 2, 64, dh))
+    return VLA_ERR_CUDA;
+  return VLA_OK;
+}
+
+vla_status enqueue_attention(const AttnPlan& ap, int layer, unsigned long long* tl, cudaStream_t st) {
+  AttnArgs aa = ap.aa;
+  aa.layer = layer;
+  aa.tl = tl;
+  if (ap.stream) {
+    VLA_CK(launch_attn_stream(&ap.tmQ, &ap.tmK, &ap.tmVt, &ap.tmKs, &ap.tmVs, aa, st));
+  } else {
+    VLA_CK(launch_attn_tc(&ap.tmQ, &ap.tmK, &ap.tmVt, &ap.tmKs, &ap.tmVs, aa, st));
+  }
+  return VLA_OK;
+}
+
 // The bf16 solver on the fused tensor-core kernels: per layer one QKV GEMM
 // (norm prologue, scatter epilogue), the tcgen05 attention and its combine,
 // the O GEMM (residual epilogue), the up GEMM (norm prologue, GeLU
@@ -365,27 +425,10 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   if (tc_encode_2d_bf16(&tm_u, act, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_o, act, h->qdim, T, 64, po.BN) ||
       tc_encode_2d_bf16(&tm_g, h->gbuf, F, T, 64, pd.BN))
     return VLA_ERR_CUDA;
-  // attention operands
-  const int dh = c.head_dim, nkv = c.n_kv_heads, P8 = d.P8;
-  AttnArgs aa{};
-  aa.B = B; aa.P = P; aa.H = c.horizon; aa.n_q = c.n_q_heads; aa.n_kv = nkv; aa.d_h = dh;
-  aa.group = c.n_q_heads / nkv;
-  aa.n_qt = cdiv(aa.group * c.horizon, 128);
-  aa.cs = attn_cluster(P);
-  aa.kc = attn_kc(P, aa.cs);
-  aa.kc_s = round_up(c.horizon, 16);
-  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
-  aa.o = act; aa.xo = h->xo; aa.status = h->d_status;
-  CUtensorMap tmQ, tmK, tmVt, tmKs, tmVs, tmH;
-  if (tc_encode_2d_bf16(&tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
-      tc_encode_3d_bf16(&tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, aa.kc) ||
-      tc_encode_3d_bf16(&tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh) ||
-      tc_encode_3d_bf16(&tmKs, h->ks, dh, c.horizon, (uint64_t)B * nkv, (uint64_t)dh * 2,
-                        (uint64_t)c.horizon * dh * 2, 64, aa.kc_s) ||
-      tc_encode_3d_bf16(&tmVs, h->vs, c.horizon, dh, (uint64_t)B * nkv, (uint64_t)h->Hp * 2,
-                        (uint64_t)dh * h->Hp * 2, 64, dh) ||
-      tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN))
-    return VLA_ERR_CUDA;
+  AttnPlan ap;
+  VLA_ST(plan_attention(h, B, P, kc, vc, act, nullptr, &ap));
+  CUtensorMap tmH;
+  if (tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN)) return VLA_ERR_CUDA;
   const DevCtl ctl{h->d_status, h->d_abort};
   const float* modt = h->modtab;
   for (int k = 0; k < h->S; ++k) {
@@ -413,10 +456,8 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
         VLA_CK(launch_modnorm(d, h->h, h->ss2, n_ss, mod, mod + D, act, st));
       }
       VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
-      // attention (merged on chip)
-      aa.layer = l;
-      aa.tl = tls(1);
-      VLA_CK(launch_attn_tc(&tmQ, &tmK, &tmVt, &tmKs, &tmVs, aa, st));
+      // attention
+      VLA_ST(enqueue_attention(ap, l, tls(1), st));
       // O projection + residual
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
@@ -461,25 +502,8 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
   if (tc_encode_2d_bf16(&tm_u, act, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_o, act, Q, T, 64, po.BN) ||
       tc_encode_2d_bf16(&tm_g, act, F, T, 64, pd.BN) || tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN))
     return VLA_ERR_CUDA;
-  const int dh = c.head_dim, nkv = c.n_kv_heads, P8 = d.P8;
-  AttnArgs aa{};
-  aa.B = B; aa.P = P; aa.H = c.horizon; aa.n_q = c.n_q_heads; aa.n_kv = nkv; aa.d_h = dh;
-  aa.group = c.n_q_heads / nkv;
-  aa.n_qt = cdiv(aa.group * c.horizon, 128);
-  aa.cs = attn_cluster(P);
-  aa.kc = attn_kc(P, aa.cs);
-  aa.kc_s = round_up(c.horizon, 16);
-  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
-  aa.o = act; aa.o32 = h->f32buf; aa.xo = h->xo; aa.status = h->d_status;
-  CUtensorMap tmQ, tmK, tmVt, tmKs, tmVs;
-  if (tc_encode_2d_bf16(&tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
-      tc_encode_3d_bf16(&tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, aa.kc) ||
-      tc_encode_3d_bf16(&tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh) ||
-      tc_encode_3d_bf16(&tmKs, h->ks, dh, c.horizon, (uint64_t)B * nkv, (uint64_t)dh * 2,
-                        (uint64_t)c.horizon * dh * 2, 64, aa.kc_s) ||
-      tc_encode_3d_bf16(&tmVs, h->vs, c.horizon, dh, (uint64_t)B * nkv, (uint64_t)h->Hp * 2,
-                        (uint64_t)dh * h->Hp * 2, 64, dh))
-    return VLA_ERR_CUDA;
+  AttnPlan ap;
+  VLA_ST(plan_attention(h, B, P, kc, vc, nullptr, h->f32buf, &ap));
   const DevCtl ctl{h->d_status, h->d_abort};
   for (int k = 0; k < h->S; ++k) {
     const float* x_in = k == 0 ? noise : actions;
@@ -491,8 +515,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       LinArgs a = lin_args(h, pq, h->qkvdim, T, l);
       a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
       VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
-      aa.layer = l;
-      VLA_CK(launch_attn_tc(&tmQ, &tmK, &tmVt, &tmKs, &tmVs, aa, st));
+      VLA_ST(enqueue_attention(ap, l, nullptr, st));
       VLA_CK(launch_quant_rows(T, Q, h->f32buf, act, h->alpha, st));
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.beta_slot = 3;
@@ -567,6 +590,7 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   VLA_CK(expert_kernels_init());
   VLA_CK(linear_kernels_init());
   VLA_CK(attn_kernels_init());
+  VLA_CK(attn_stream_init());
   VLA_CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
   return VLA_OK;
 }

@@ -357,6 +357,23 @@ __device__ __forceinline__ void tmem_wait16(uint32_t* r) {
                :
                : "memory");
 }
+// tcgen05.st of 16 columns (32 lanes x 32 bit); complete with tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Bounded wait that ignores the error latch: used only to let this CTA's own
+// asynchronous copies or MMAs finish before it frees their destination.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > VLA_WAIT_LIMIT_NS) return;
+}
 // 2^x with the hardware approximation (relative error ~2^-22), for softmax.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -545,6 +562,14 @@ cudaError_t attn_kernels_init();
 // (box 64 x d_h); all bf16 with the 128-byte swizzle.
 cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
                            const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st);
+// Streaming joint attention (k_attn_stream.cu): one CTA per 128-row query
+// tile streams every key in 64-key chunks (no cross-CTA merge).  Uses the
+// AttnArgs fields B, P, H, n_q, n_kv, d_h, group, layer, n_qt, scale_log2, o,
+// o32, status.  tmK and tmKs have 64-row boxes; tmQ, tmVt, tmVs as above.
+size_t attn_stream_smem_bytes(int d_h);
+cudaError_t attn_stream_init();
+cudaError_t launch_attn_stream(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
+                               const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st);
 int tc_encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                      uint32_t box_rows);
 // uint8 map (no swizzle) over packed ternary codes [rows][inner bytes].

@@ -72,6 +72,41 @@ def test_small_bf16_cuda_core_gemm_path():
     _check(gpu_run(CONFIGS["small_bf16"], flags=V.FLAG_SIMT_GEMM), obs=[0])
 
 
+@pytest.mark.parametrize("form", ["split", "stream"])
+def test_small_bf16_attention_forms(form):
+    """Both attention kernels (keys split over a cluster / streamed through one
+    CTA) on a ragged case: odd prefix (partial last key chunk, padded V^T
+    rows), a horizon of 80 (two action-key chunks, a partial last query
+    tile), two observations."""
+    import prefix_cached_flow_gb300 as V
+    flag = V.FLAG_ATTN_SPLIT if form == "split" else V.FLAG_ATTN_STREAM
+    cfg = CONFIGS["small_bf16"].replace(H=80)
+    _check(gpu_run(cfg, B=2, P=77, flags=flag), obs=[0, 1])
+
+
+def test_small_bf16_single_prefix_token_stream_attention():
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["small_bf16"], B=1, P=1, flags=V.FLAG_ATTN_STREAM), obs=[0])
+
+
+def test_full_bf16_b1_stream_attention():
+    """d_h = 256 (the largest TMEM/shared-memory footprint), four query tiles
+    of which the last holds 16 rows."""
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["full_bf16_b1"], flags=V.FLAG_ATTN_STREAM), obs=[0])
+
+
+def test_full_bf16_b64_split_attention():
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["full_bf16_b64"], flags=V.FLAG_ATTN_SPLIT), obs=[37], free_running=True)
+
+
+def test_w2a8_b1_stream_attention():
+    """fp32 attention output (the W2A8 quantiser's input) from the streaming form."""
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["w2a8_b1"], flags=V.FLAG_ATTN_STREAM), obs=[0])
+
+
 def test_tiny_f32_ragged():
     cfg = CONFIGS["tiny_f32"]
     _check(gpu_run(cfg, B=2, P=13), obs=[0, 1])
