@@ -60,7 +60,7 @@ typedef enum { VLA_DTYPE_F32 = 0, VLA_DTYPE_BF16 = 1 } vla_dtype;
 #define VLA_FLAG_SIMT_GEMM 1u  /* run bf16 GEMMs on the CUDA-core kernel instead of tcgen05 */
 #define VLA_FLAG_NO_GRAPH 2u   /* enqueue the solver kernels directly instead of one graph launch */
 #define VLA_FLAG_ATTN_SPLIT 4u  /* attention: always the clustered form (a query tile's keys split over SMs) */
-#define VLA_FLAG_ATTN_STREAM 8u /* attention: always the streaming form (one CTA per query tile, all keys) */
+#define VLA_FLAG_ATTN_STREAM 8u /* attention: the streaming form (one CTA per query tile, all keys) where d_h is 64, 128 or 256 */
 
 typedef struct {
   int n_layers;    /* L */

@@ -351,10 +351,11 @@ bool fused_supported(const vla_expert_config& c, bool f32, bool w2a8, bool use_t
 }
 
 // Attention for one solve: the kernel form, its arguments and tensor maps.
-// The streaming kernel (one CTA per query tile, all keys) is used when the
-// query tiles alone occupy a fifth of the SMs; otherwise the clustered kernel
-// spreads each tile's keys over a cluster.  VLA_FLAG_ATTN_SPLIT /
-// VLA_FLAG_ATTN_STREAM force one form.
+// The streaming kernel (one CTA per query tile, all keys; head sizes 64, 128
+// and 256) is used when the query tiles alone occupy a fifth of the SMs;
+// otherwise the clustered kernel spreads each tile's keys over a cluster.
+// VLA_FLAG_ATTN_SPLIT / VLA_FLAG_ATTN_STREAM force one form (the streaming
+// one only where it applies).
 struct AttnPlan {
   bool stream;
   AttnArgs aa;
@@ -376,8 +377,9 @@ vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, con
   aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
   aa.o = (bf16*)o; aa.o32 = o32; aa.xo = h->xo; aa.status = h->d_status;
   const unsigned fl = c.flags;
-  ap->stream = (fl & VLA_FLAG_ATTN_STREAM) ||
-               (!(fl & VLA_FLAG_ATTN_SPLIT) && B * nkv * aa.n_qt * 5 >= h->num_sms);
+  const bool stream_ok = dh == 64 || dh == 128 || dh == 256;
+  ap->stream = stream_ok && ((fl & VLA_FLAG_ATTN_STREAM) ||
+                             (!(fl & VLA_FLAG_ATTN_SPLIT) && B * nkv * aa.n_qt * 5 >= h->num_sms));
   const uint32_t krows = ap->stream ? 64u : (uint32_t)aa.kc, ksrows = ap->stream ? 64u : (uint32_t)aa.kc_s;
   if (tc_encode_2d_bf16(&ap->tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
       tc_encode_3d_bf16(&ap->tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64,
