@@ -34,9 +34,6 @@ constexpr uint32_t kA = 128 * 128;  // bytes of one 128 x 64 bf16 weight stage
 constexpr int kMaxC = 16;           // largest cluster
 constexpr int kPre = 2;             // residual quads prefetched per thread
 
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 struct LinSmem {
   uint32_t a, b, hs, pk, region, bars, slot, rstat, gam, bet, wss, total;

@@ -1,0 +1,309 @@
+// Fused linear layer of the action expert for many tokens (batched
+// requests), on tcgen05.  Same operation and epilogues as k_linear_tc.cu
+// ("vla.cpp: A Unified Inference Runtime for Vision-Language-Action Models",
+// §III-A Eq. (1): the velocity network of every Euler step; §III-B Eq. (2):
+// queries and action keys/values for the joint attention):
+//   y[t][n] = sum_k W[n][k] X[t][k]
+// followed by EPI_QKV (scatter to q, k_s, v_s^T), EPI_RESID (h += y and the
+// per-(128-row block, token) sums of squares of the new h) or EPI_GELU
+// (g = bf16(GeLU(y))).
+//
+// At batch 1 the layer is a weight stream and k_linear splits K over a
+// cluster; with thousands of tokens it is a dense GEMM, and this kernel is a
+// persistent, warp-specialised one:
+//   warp 0      TMA producer: 128 x 64 weight and BN x 64 token tiles into a
+//               four-stage ring (weights first, before the grid dependency
+//               wait, for the CTA's first tile)
+//   warp 1      MMA issuer: 128 x BN accumulator in one of two TMEM buffers
+//   warps 2-9   epilogue: warp w reads TMEM lane quarter w % 4 (one output
+//               row n per thread) and half (w - 2) / 4 of the token columns
+// Each CTA takes tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the epilogue
+// of one tile runs while the MMAs of the next accumulate into the other TMEM
+// buffer.  Tiles are ordered weight-tile fastest, so CTAs running at the same
+// time share token tiles in L2.
+#include "vla_common.cuh"
+
+namespace {
+
+constexpr uint32_t kWA = 128 * 128;  // one 128 x 64 bf16 weight stage
+constexpr int kWS = 4;               // ring stages
+constexpr int kEpiWarps = 8;
+constexpr int kWideThreads = 64 + 32 * kEpiWarps;
+
+struct WideSmem {
+  uint32_t a, b, wss, bars, slot, total;
+};
+
+__host__ __device__ inline WideSmem wide_layout(int BN) {
+  WideSmem s;
+  s.a = 0;
+  s.b = (uint32_t)kWS * kWA;
+  s.wss = s.b + (uint32_t)kWS * (uint32_t)BN * 128u;  // [2 tile parities][2 halves][4 quarters][BN/2] fp32
+  s.bars = s.wss + 16u * (uint32_t)(BN / 2) * 4u;
+  s.slot = s.bars + (2 * kWS + 5) * 8;
+  s.total = s.slot + 16;
+  return s;
+}
+
+// After the call, lane l holds the sum over the warp's 32 lanes of v[l]
+// (a transposing butterfly: 16 + 8 + 4 + 2 + 1 shuffles for 32 columns).
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) {
+    const bool up = (lane & k) != 0;
+#pragma unroll
+    for (int j = 0; j < k; ++j) {
+      const float send = up ? v[j] : v[j + k];
+      const float keep = up ? v[j + k] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+    }
+  }
+  return v[0];
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    k_linear_wide(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const LinArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int BN = g.BN;
+  const WideSmem Ls = wide_layout(BN);
+  uint8_t* As = smem + Ls.a;
+  uint8_t* Bs = smem + Ls.b;
+  float* wss = (float*)(smem + Ls.wss);
+  uint64_t* full = (uint64_t*)(smem + Ls.bars);
+  uint64_t* empty = full + kWS;
+  uint64_t* accf = empty + kWS;  // [2] accumulator ready (MMA commit)
+  uint64_t* acce = accf + 2;     // [2] accumulator drained (epilogue threads)
+  uint64_t* fin = acce + 2;      // every MMA of this CTA complete
+  uint32_t* tmem_slot = (uint32_t*)(smem + Ls.slot);
+  __shared__ int s_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_n = g.N / 128, tiles_t = (g.T + BN - 1) / BN, tiles = tiles_n * tiles_t;
+  const int nkb = g.KS / 64;
+  const uint32_t b_tile = (uint32_t)BN * 128u;
+
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    for (int s = 0; s < kWS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiWarps * 32);
+    }
+    mbar_init(fin, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint32_t tx = kWA + b_tile;
+      const int first = blockIdx.x;
+      int pre = 0;
+      if (first < tiles) {
+        // Weights of the first tile: independent of the previous kernel.
+        const int m0 = (first % tiles_n) * 128;
+        pre = nkb < kWS ? nkb : kWS;
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], tx);
+          tma_load_2d(As + (size_t)i * kWA, &tmA, &full[i], i * 64, g.a_row0 + m0);
+        }
+      }
+      griddep_wait();
+      int it = 0;
+      bool okp = true;
+      for (int tile = first; okp && tile < tiles; tile += gridDim.x) {
+        const int m0 = (tile % tiles_n) * 128, t0 = (tile / tiles_n) * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kWS;
+          if (it >= pre) {
+            if (!mbar_wait(&empty[s], ((it / kWS) & 1) ^ 1, g.status)) {
+              s_fail = 1;
+              okp = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], tx);
+            tma_load_2d(As + (size_t)s * kWA, &tmA, &full[s], kb * 64, g.a_row0 + m0);
+          }
+          tma_load_2d(Bs + (size_t)s * b_tile, &tmB, &full[s], kb * 64, t0);
+        }
+      }
+      // Own copies land before the CTA can exit (normally all consumed).
+      const int first_live = it > kWS ? it - kWS : 0;
+      for (int i = first_live; i < it; ++i) mbar_drain(&full[i % kWS], (uint32_t)(i / kWS) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      int it = 0, lt = 0;
+      bool okm = true;
+      for (int tile = blockIdx.x; okm && tile < tiles; tile += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        if (!mbar_wait(&acce[buf], ((lt >> 1) & 1) ^ 1, g.status)) {
+          okm = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(buf * 256);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kWS;
+          if (!mbar_wait(&full[s], (it / kWS) & 1, g.status)) {
+            okm = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(As + (size_t)s * kWA);
+          const uint32_t b_addr = smem_u32(Bs + (size_t)s * b_tile);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(dt, sdesc_k128(a_addr + k * 32), sdesc_k128(b_addr + k * 32), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        if (okm) umma_commit(&accf[buf]);
+      }
+      if (!okm) s_fail = 1;
+      umma_commit(fin);
+      mbar_drain(fin, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2-9) ----------------
+    griddep_wait();  // reads and writes activations of earlier kernels
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int hbn = BN / 2;
+    int slot = g.beta_slot;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&accf[buf], (lt >> 1) & 1, g.status));
+      tc_fence_after();
+      const int m0 = (tile % tiles_n) * 128, t0 = (tile / tiles_n) * BN;
+      const int n = m0 + row;
+      const int tcols = (g.T - t0) < BN ? (g.T - t0) : BN;
+      if (EPI == EPI_QKV) slot = n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2);
+      float* wq = wss + ((size_t)(buf * 2 + half) * 4 + quarter) * hbn;  // this warp's column sums
+      for (int c0 = half * hbn; c0 < (half + 1) * hbn; c0 += 32) {
+        uint32_t r[32];
+        if (okw) {
+          tmem_ld16_nowait(tq + (uint32_t)(buf * 256 + c0), r);
+          tmem_ld16_nowait(tq + (uint32_t)(buf * 256 + c0 + 16), r + 16);
+          tmem_wait16(r);
+          tmem_wait16(r + 16);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = 0u;
+        }
+        const int nv = okw ? (tcols - c0 < 32 ? tcols - c0 : 32) : 0;  // valid columns in this chunk
+        if (EPI == EPI_RESID) {
+          float hv[32];
+          float* hp = g.h + (size_t)(t0 + c0) * g.D + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) hv[j] = j < nv ? hp[(size_t)j * g.D] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            hv[j] += __uint_as_float(r[j]);
+            if (j < nv) hp[(size_t)j * g.D] = hv[j];
+            hv[j] = j < nv ? hv[j] * hv[j] : 0.f;
+          }
+          const float cs = warp_transpose_sum32(hv, lane);
+          wq[c0 - half * hbn + lane] = cs;
+        } else if (EPI == EPI_GELU) {
+          bf16* gp = g.g + (size_t)(t0 + c0) * g.ldg + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) gp[(size_t)j * g.ldg] = __float2bfloat16_rn(gelu_exact(__uint_as_float(r[j])));
+        } else {  // EPI_QKV
+          int b = (t0 + c0) / g.H, i = (t0 + c0) - b * g.H;
+          const int rr = slot == 0 ? n : (slot == 1 ? n - g.qdim : n - g.qdim - g.kvdim);
+          const int hd = rr / g.d_h, d = rr - hd * g.d_h;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nv) {
+              const bf16 bv = __float2bfloat16_rn(__uint_as_float(r[j]));
+              if (slot == 0)
+                g.q[(((size_t)b * g.n_q + hd) * g.H + i) * g.d_h + d] = bv;
+              else if (slot == 1)
+                g.ks[(((size_t)b * g.n_kv + hd) * g.H + i) * g.d_h + d] = bv;
+              else
+                g.vst[(((size_t)b * g.n_kv + hd) * g.d_h + d) * g.Hp + i] = bv;
+            }
+            if (++i == g.H) {
+              i = 0;
+              ++b;
+            }
+          }
+        }
+      }
+      // TMEM buffer drained: the MMA warp may overwrite it.
+      tc_fence_before();
+      mbar_arrive(&acce[buf]);
+      if (EPI == EPI_RESID) {
+        // Sum the four quarters' column sums (fixed order) for this half.
+        named_bar_sync(1 + half, 128);
+        const int col = quarter * 32 + lane;  // column within the half
+        if (okw && col < hbn && half * hbn + col < tcols) {
+          const float* ws = wss + (size_t)(buf * 2 + half) * 4 * hbn;
+          g.ss_out[(size_t)(tile % tiles_n) * g.T + t0 + half * hbn + col] =
+              (ws[col] + ws[hbn + col]) + (ws[2 * hbn + col] + ws[3 * hbn + col]);
+        }
+      }
+      if (!okw) s_fail = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+size_t linear_wide_smem_bytes(int BN) { return 1024 + wide_layout(BN).total; }
+
+cudaError_t linear_wide_init() {
+  cudaError_t e = set_max_dyn_smem(k_linear_wide<EPI_QKV>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear_wide<EPI_RESID>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear_wide<EPI_GELU>);
+  return e;
+}
+
+cudaError_t launch_linear_wide(const CUtensorMap* tmA, const CUtensorMap* tmB, const LinArgs& g, int grid,
+                               cudaStream_t st) {
+  if (g.BN < 64 || g.BN > 256 || g.BN % 64 || g.KS % 64 || g.KS < 64 || g.N % 128 || g.T < 1 || grid < 1 ||
+      g.amode != 0 || g.w2a8 != 0 || (g.epi != EPI_QKV && g.epi != EPI_RESID && g.epi != EPI_GELU))
+    return cudaErrorInvalidValue;
+  const size_t smem = linear_wide_smem_bytes(g.BN);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  void (*fn)(CUtensorMap, CUtensorMap, LinArgs) =
+      g.epi == EPI_QKV ? k_linear_wide<EPI_QKV> : (g.epi == EPI_RESID ? k_linear_wide<EPI_RESID> : k_linear_wide<EPI_GELU>);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kWideThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, *tmA, *tmB, g);
+}

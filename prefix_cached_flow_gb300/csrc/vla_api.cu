@@ -280,7 +280,42 @@ vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B,
 
 struct LinPlan {
   int C = 1, KS = 64, BN = 16, tiles_n = 1, tiles_t = 1, stages = 1, bmode = 0;
+  bool wide = false;  // persistent many-token kernel (k_linear_wide.cu)
+  int grid = 0;       // its CTA count
 };
+
+// Many-token plan: the persistent kernel with 128 x BN tiles, BN in
+// {64, 128, 192, 256} chosen to minimise waves x (BN + 32) (the tile's token
+// columns plus a fixed per-tile cost).  Used when even 128-token tiles give a
+// wave of work for every SM (or always, with VLA_FLAG_LINEAR_WIDE); never for
+// packed ternary weights.
+LinPlan plan_wide(int num_sms, int N, int K, int T) {
+  LinPlan p;
+  const int tn = N / 128;
+  long best = -1;
+  for (int bn = 256; bn >= 64; bn -= 64) {
+    const long cost = (long)cdiv(tn * cdiv(T, bn), num_sms) * (bn + 32);
+    if (best < 0 || cost < best) {
+      best = cost;
+      p.BN = bn;
+    }
+  }
+  p.wide = true;
+  p.C = 1;
+  p.KS = K;
+  p.tiles_n = tn;
+  p.tiles_t = cdiv(T, p.BN);
+  p.grid = p.tiles_n * p.tiles_t < num_sms ? p.tiles_n * p.tiles_t : num_sms;
+  p.bmode = 0;
+  p.stages = 4;
+  return p;
+}
+
+bool wide_applies(unsigned flags, int num_sms, int N, int K, int T) {
+  if ((flags & VLA_FLAG_LINEAR_SPLIT) || N % 128 || K % 64) return false;
+  if (flags & VLA_FLAG_LINEAR_WIDE) return true;
+  return (N / 128) * cdiv(T, 128) >= num_sms;
+}
 
 // Cluster split-K plan: the smallest power-of-two cluster (<= 16) that puts
 // about one CTA on every SM, with the modulated-norm prologue fused when the
@@ -312,7 +347,15 @@ LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool p
 }
 
 LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
+  if (!h->w2a8 && wide_applies(h->cfg.flags, h->num_sms, N, K, T)) return plan_wide(h->num_sms, N, K, T);
   return plan_linear_sms(h->num_sms, N, K, T, want_norm && !h->w2a8, h->w2a8);
+}
+
+// One linear layer on the kernel its plan names.
+cudaError_t run_lin(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& a,
+                    const LinPlan& p, cudaStream_t st) {
+  if (p.wide) return launch_linear_wide(tmA, tmB, a, p.grid, st);
+  return launch_linear(tmA, tmB, tmH, a, p.tiles_n, p.tiles_t, p.C, st);
 }
 
 LinArgs lin_args(const vla_expert* h, const LinPlan& p, int N, int T, int layer) {
@@ -423,9 +466,9 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   const LinPlan pu = plan_linear(h, F, D, T, true);
   const LinPlan pd = plan_linear(h, D, F, T, false);
   bf16* act = (bf16*)h->act;
-  CUtensorMap tm_u, tm_o, tm_g;  // activations as B operands
-  if (tc_encode_2d_bf16(&tm_u, act, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_o, act, h->qdim, T, 64, po.BN) ||
-      tc_encode_2d_bf16(&tm_g, h->gbuf, F, T, 64, pd.BN))
+  CUtensorMap tm_uq, tm_uu, tm_o, tm_g;  // activations as B operands (box: 64 x the plan's BN)
+  if (tc_encode_2d_bf16(&tm_uq, act, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_uu, act, D, T, 64, pu.BN) ||
+      tc_encode_2d_bf16(&tm_o, act, h->qdim, T, 64, po.BN) || tc_encode_2d_bf16(&tm_g, h->gbuf, F, T, 64, pd.BN))
     return VLA_ERR_CUDA;
   AttnPlan ap;
   VLA_ST(plan_attention(h, B, P, kc, vc, act, nullptr, &ap));
@@ -457,13 +500,13 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       } else {
         VLA_CK(launch_modnorm(d, h->h, h->ss2, n_ss, mod, mod + D, act, st));
       }
-      VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
+      VLA_CK(run_lin(&h->tm_wqkv, &tm_uq, &tmH, a, pq, st));
       // attention
       VLA_ST(enqueue_attention(ap, l, tls(1), st));
       // O projection + residual
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
-      VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
+      VLA_CK(run_lin(&h->tm_wo, &tm_o, &tmH, a, po, st));
       // MLP up + GeLU
       a = lin_args(h, pu, F, T, l);
       a.epi = EPI_GELU; a.g = (bf16*)h->gbuf; a.ldg = F; a.tl = tls(3);
@@ -472,11 +515,11 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       } else {
         VLA_CK(launch_modnorm(d, h->h, h->ss1, po.tiles_n, mod + 2 * D, mod + 3 * D, act, st));
       }
-      VLA_CK(launch_linear(&h->tm_wup, &tm_u, &tmH, a, pu.tiles_n, pu.tiles_t, pu.C, st));
+      VLA_CK(run_lin(&h->tm_wup, &tm_uu, &tmH, a, pu, st));
       // MLP down + residual
       a = lin_args(h, pd, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.tl = tls(4);
-      VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
+      VLA_CK(run_lin(&h->tm_wdown, &tm_g, &tmH, a, pd, st));
       n_ss = pd.tiles_n;
     }
     VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));
@@ -593,6 +636,7 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   VLA_CK(linear_kernels_init());
   VLA_CK(attn_kernels_init());
   VLA_CK(attn_stream_init());
+  VLA_CK(linear_wide_init());
   VLA_CK(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
   return VLA_OK;
 }

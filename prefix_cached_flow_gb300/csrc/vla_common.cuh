@@ -259,6 +259,10 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void st_shared_v4_u32(uint32_t saddr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -537,6 +541,14 @@ cudaError_t linear_kernels_init();
 // tmH: fp32 map over h [T][D] with box 64 x BN (no swizzle), used by bmode 1.
 cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& g,
                           int tiles_n, int tiles_t, int C, cudaStream_t st);
+
+// Persistent many-token linear kernel (k_linear_wide.cu): same LinArgs and
+// epilogues (EPI_QKV, EPI_RESID, EPI_GELU; bf16 weights, TMA'd tokens with a
+// 64 x BN box, KS = K), BN in {64, 128, 192, 256}, N a multiple of 128.
+size_t linear_wide_smem_bytes(int BN);
+cudaError_t linear_wide_init();
+cudaError_t launch_linear_wide(const CUtensorMap* tmA, const CUtensorMap* tmB, const LinArgs& g, int grid,
+                               cudaStream_t st);
 
 // tcgen05 joint attention (k_attn_tc.cu): a cluster of `cs` CTAs per
 // 128-row query tile of one (observation, K/V head); ranks 0..cs-2 take kc

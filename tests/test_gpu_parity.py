@@ -107,6 +107,26 @@ def test_w2a8_b1_stream_attention():
     _check(gpu_run(CONFIGS["w2a8_b1"], flags=V.FLAG_ATTN_STREAM), obs=[0])
 
 
+@pytest.mark.parametrize("B,P", [(1, 256), (3, 77)])
+def test_small_bf16_wide_linear(B, P):
+    """The persistent many-token linear kernel forced at small sizes: partial
+    token tiles, an odd batch (QKV scatter across observations)."""
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["small_bf16"], B=B, P=P, flags=V.FLAG_LINEAR_WIDE), obs=list(range(B)))
+
+
+def test_full_bf16_b1_wide_linear():
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["full_bf16_b1"], flags=V.FLAG_LINEAR_WIDE), obs=[0])
+
+
+def test_full_bf16_b64_split_linear():
+    """The cluster split-K linear kernel at 3200 tokens (the default there is
+    the persistent kernel)."""
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["full_bf16_b64"], flags=V.FLAG_LINEAR_SPLIT), obs=[11], free_running=True)
+
+
 def test_tiny_f32_ragged():
     cfg = CONFIGS["tiny_f32"]
     _check(gpu_run(cfg, B=2, P=13), obs=[0, 1])
