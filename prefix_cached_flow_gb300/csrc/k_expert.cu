@@ -19,6 +19,7 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMultiTokens = 256;  // from this many tokens the embed / head CTAs take several tokens
 
 // ---------------------------------------------------------------------------
 // Time conditioning table (built once per handle; tau_k = k / S)
@@ -348,6 +349,56 @@ __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* s
   if (threadIdx.x == 0) ss_out[t] = ss;
 }
 
+// Many-token form of k_embed_ss: a CTA takes kMT consecutive tokens, so each
+// W_in row is read once per kMT tokens (the per-token form reads all of W_in
+// for every token).  Same arithmetic per element.
+constexpr int kMT = 16;
+__global__ void k_embed_ss_multi(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  extern __shared__ float sm[];
+  float* xs = sm;                // [kMT][d_a]
+  float* red = sm + kMT * d.d_a; // [kMT][warps]
+  const int T = d.B * d.H, t0 = blockIdx.x * kMT;
+  const int nt = T - t0 < kMT ? T - t0 : kMT;
+  const int nw = blockDim.x >> 5, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && ctl.abort && *ctl.abort) latch_error(ctl.status, VLA_DEV_ABORTED);
+  for (int e = threadIdx.x; e < kMT * d.d_a; e += blockDim.x)
+    xs[e] = e < nt * d.d_a ? x_in[(size_t)t0 * d.d_a + e] : 0.f;
+  __syncthreads();
+  float ss[kMT];
+#pragma unroll
+  for (int t = 0; t < kMT; ++t) ss[t] = 0.f;
+  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+    const float* w = b.win + (size_t)i * d.d_a;
+    float acc[kMT];
+#pragma unroll
+    for (int t = 0; t < kMT; ++t) acc[t] = 0.f;
+    for (int j = 0; j < d.d_a; ++j) {
+      const float wv = w[j];
+#pragma unroll
+      for (int t = 0; t < kMT; ++t) acc[t] += xs[t * d.d_a + j] * wv;
+    }
+#pragma unroll
+    for (int t = 0; t < kMT; ++t)
+      if (t < nt) {
+        b.h[(size_t)(t0 + t) * d.D + i] = acc[t];
+        ss[t] += acc[t] * acc[t];
+      }
+  }
+#pragma unroll
+  for (int t = 0; t < kMT; ++t) {
+    const float v = warp_sum(ss[t]);
+    if (lane == 0) red[t * nw + wid] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    float v = 0.f;
+    for (int w = 0; w < nw; ++w) v += red[threadIdx.x * nw + w];
+    ss_out[t0 + threadIdx.x] = v;
+  }
+}
+
 // u = h / rms(h) * (1 + gamma) + beta as bf16 [T][D], rms from n_ss slots.
 __global__ void k_modnorm(int T, int D, float eps, const float* h, const float* ss, int n_ss, const float* gamma,
                           const float* beta, bf16* u) {
@@ -397,6 +448,59 @@ __global__ void k_head_fused(ExpertDims d, StepBufs b, int step, float dt, const
       const size_t o = (size_t)t * d.d_a + a;
       x_out[o] = fmaf(dt, acc, x_in[o]);
       if (tap) tap[(size_t)step * T * d.d_a + o] = acc;
+    }
+  }
+}
+
+// Many-token form of k_head_fused: a CTA takes kHT tokens (one warp each for
+// the norm), so each W_out row is read once per kHT tokens.
+constexpr int kHT = 8;
+__global__ void k_head_multi(ExpertDims d, StepBufs b, int step, float dt, const float* x_in, float* x_out,
+                             float* tap) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  extern __shared__ float sm[];  // [kHT][D] modulated rows
+  const int T = d.B * d.H, t0 = blockIdx.x * kHT;
+  const int nt = T - t0 < kHT ? T - t0 : kHT;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float* gf = b.modf + (size_t)step * 2 * d.D;
+  const float* bf = gf + d.D;
+  for (int t = wid; t < kHT; t += nw) {
+    float* row = sm + (size_t)t * d.D;
+    if (t < nt) {
+      const float* hr = b.h + (size_t)(t0 + t) * d.D;
+      float ss = 0.f;
+      for (int i = lane; i < d.D; i += 32) {
+        const float hv = hr[i];
+        row[i] = hv;
+        ss += hv * hv;
+      }
+      ss = warp_sum(ss);
+      const float r = rsqrtf(ss / (float)d.D + d.eps);
+      for (int i = lane; i < d.D; i += 32) row[i] = row[i] * r * (1.f + gf[i]) + bf[i];
+    } else {
+      for (int i = lane; i < d.D; i += 32) row[i] = 0.f;
+    }
+  }
+  __syncthreads();
+  for (int a = wid; a < d.d_a; a += nw) {
+    const float* w = b.wout + (size_t)a * d.D;
+    float acc[kHT];
+#pragma unroll
+    for (int t = 0; t < kHT; ++t) acc[t] = 0.f;
+    for (int i = lane; i < d.D; i += 32) {
+      const float wv = w[i];
+#pragma unroll
+      for (int t = 0; t < kHT; ++t) acc[t] += sm[(size_t)t * d.D + i] * wv;
+    }
+#pragma unroll
+    for (int t = 0; t < kHT; ++t) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0 && t < nt) {
+        const size_t o = (size_t)(t0 + t) * d.d_a + a;
+        x_out[o] = fmaf(dt, v, x_in[o]);
+        if (tap) tap[(size_t)step * T * d.d_a + o] = v;
+      }
     }
   }
 }
@@ -471,6 +575,12 @@ cudaError_t expert_kernels_init() {
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_attn_combine<float>);
   if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_head_multi);
+  if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_head_fused);
+  if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_embed_ss_multi);
+  if (e != cudaSuccess) return e;
   return set_max_dyn_smem(k_attn_combine<bf16>);
 }
 
@@ -502,8 +612,11 @@ cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float*
   ExpertDims dd = d;
   StepBufs bb = b;
   void* args[] = {&dd, &bb, (void*)&x_in, &ss_out, &ctl};
-  return launch_pdl((const void*)k_embed_ss, dim3(d.B * d.H), dim3(kThreads), (size_t)(d.d_a + 32) * sizeof(float),
-                    st, args);
+  const int T = d.B * d.H;
+  if (T >= kMultiTokens && d.d_a <= 256)
+    return launch_pdl((const void*)k_embed_ss_multi, dim3((T + kMT - 1) / kMT), dim3(kThreads),
+                      (size_t)(kMT * d.d_a + kMT * (kThreads / 32)) * sizeof(float), st, args);
+  return launch_pdl((const void*)k_embed_ss, dim3(T), dim3(kThreads), (size_t)(d.d_a + 32) * sizeof(float), st, args);
 }
 
 cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss, int n_ss, const float* gamma,
@@ -538,8 +651,11 @@ cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, 
   ExpertDims dd = d;
   StepBufs bb = b;
   void* args[] = {&dd, &bb, &step, &dt, (void*)&x_in, &x_out, &tap};
-  return launch_pdl((const void*)k_head_fused, dim3(d.B * d.H), dim3(kThreads), (size_t)(d.D + 32) * sizeof(float),
-                    st, args);
+  const int T = d.B * d.H;
+  if (T >= kMultiTokens && (size_t)kHT * d.D * sizeof(float) <= 200 * 1024)
+    return launch_pdl((const void*)k_head_multi, dim3((T + kHT - 1) / kHT), dim3(kThreads),
+                      (size_t)kHT * d.D * sizeof(float), st, args);
+  return launch_pdl((const void*)k_head_fused, dim3(T), dim3(kThreads), (size_t)(d.D + 32) * sizeof(float), st, args);
 }
 
 cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st) {

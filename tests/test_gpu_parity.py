@@ -115,6 +115,14 @@ def test_small_bf16_wide_linear(B, P):
     _check(gpu_run(CONFIGS["small_bf16"], B=B, P=P, flags=V.FLAG_LINEAR_WIDE), obs=list(range(B)))
 
 
+def test_small_bf16_many_tokens_ragged():
+    """350 action tokens (7 observations x H = 50): the many-token embed and
+    head kernels with a partial last block, the persistent linear kernel and
+    the streaming attention, all by their own size rules."""
+    cfg = CONFIGS["small_bf16"].replace(H=50)
+    _check(gpu_run(cfg, B=7, P=77), obs=[0, 6])
+
+
 def test_full_bf16_b1_wide_linear():
     import prefix_cached_flow_gb300 as V
     _check(gpu_run(CONFIGS["full_bf16_b1"], flags=V.FLAG_LINEAR_WIDE), obs=[0])
