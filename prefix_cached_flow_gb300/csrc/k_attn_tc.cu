@@ -54,14 +54,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
-template <bool O32>
+template <bool O32, int CS>
 __global__ void __launch_bounds__(128, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmKs,
               const __grid_constant__ CUtensorMap tmVs, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int dh = a.d_h, CS = a.cs;
+  const int dh = a.d_h;  // cluster size CS is a template parameter (code size: only CS ranks' exchanges)
   const int nsub = dh / 64;
   const bool suffix = (int)blockIdx.x == CS - 1;
   const int kc = suffix ? a.kc_s : a.kc;             // keys this rank's tiles hold
@@ -158,37 +158,55 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
   float m = -INFINITY, l = 0.f;
   if (ok && nk > 0) {
-    // The whole row of S (kc <= 128 columns) in registers: every TMEM load is
-    // issued back to back and waited on once.
-    uint32_t sr[128];
+    // Two passes over TMEM in 32-column pieces.  Every CTA runs this code
+    // once, so it is kept compact (rolled loops whose bodies repeat, instead
+    // of holding the row in registers with fully unrolled code).  Columns in
+    // [nk, 32-roundup of kc) are masked by a select; they lie inside the
+    // TMEM allocation (at least 64 columns, d_h >= 64).
+    float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+    for (int c0 = 0; c0 < kc; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld16_nowait(taddr + (uint32_t)c0, r);
+      tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
+      tmem_wait16(r);
+      tmem_wait16(r + 16);
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q * 16 < kc) tmem_ld16_nowait(taddr + (uint32_t)(q * 16), sr + q * 16);
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q * 16 < kc) tmem_wait16(sr + q * 16);
-#pragma unroll
-    for (int j = 0; j < 128; ++j)
-      if (j < nk) m = fmaxf(m, __uint_as_float(sr[j]) * a.scale_log2);
+      for (int u = 0; u < 32; ++u) mxv[u & 3] = fmaxf(mxv[u & 3], c0 + u < nk ? __uint_as_float(r[u]) : -INFINITY);
+    }
+    m = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])) * a.scale_log2;  // the scale is positive
+    VLA_TL(a.tl, 0, 11);
+    const float nm = -m;
+    float lv[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t pa = smem_u32(Ps);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kc; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld16_nowait(taddr + (uint32_t)c0, r);
+      tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
+      tmem_wait16(r);
+      tmem_wait16(r + 16);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {  // 8-key chunks
-      if (q * 8 < kc) {
+      for (int q = 0; q < 4; ++q) {  // 8-key chunks
         float p[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int j = q * 8 + u;
-          p[u] = j < nk ? fast_exp2(__uint_as_float(sr[j]) * a.scale_log2 - m) : 0.f;
-          l += p[u];
+          const int j = c0 + q * 8 + u;
+          p[u] = fast_exp2(fmaf(__uint_as_float(r[q * 8 + u]), a.scale_log2, nm));
+          p[u] = j < nk ? p[u] : 0.f;
+          lv[u & 3] += p[u];
         }
         uint4 pk;
         pk.x = pack_bf16x2(p[0], p[1]);
         pk.y = pack_bf16x2(p[2], p[3]);
         pk.z = pack_bf16x2(p[4], p[5]);
         pk.w = pack_bf16x2(p[6], p[7]);
-        st_shared_v4_u32(pa + (uint32_t)(q >> 3) * 16384u + sw128_offset((uint32_t)row, (uint32_t)(q & 7)), pk);
+        const int ch = c0 / 8 + q;  // 8-key chunk index within the rank's keys
+        if (ch * 8 < kc)
+          st_shared_v4_u32(pa + (uint32_t)(ch >> 3) * 16384u + sw128_offset((uint32_t)row, (uint32_t)(ch & 7)), pk);
       }
     }
+    l = (lv[0] + lv[1]) + (lv[2] + lv[3]);
   }
   VLA_TL(a.tl, 0, 8);
   sm_m[row] = m;
@@ -222,21 +240,19 @@ __global__ void __launch_bounds__(128, 1)
 
   // Merge factors for this row: M = max_c m_c, den = sum_c exp2(m_c - M) l_c.
   const uint32_t mloc = smem_u32(&sm_m[row]), lloc = smem_u32(&sm_l[row]);
-  float mc[16], lc[16];
+  float mc[CS], lc[CS];
 #pragma unroll
-  for (int c = 0; c < 16; ++c)
-    if (c < CS) {
-      mc[c] = ld_dsmem_f32(mapa_shared(mloc, (uint32_t)c));
-      lc[c] = ld_dsmem_f32(mapa_shared(lloc, (uint32_t)c));
-    }
+  for (int c = 0; c < CS; ++c) {
+    mc[c] = ld_dsmem_f32(mapa_shared(mloc, (uint32_t)c));
+    lc[c] = ld_dsmem_f32(mapa_shared(lloc, (uint32_t)c));
+  }
   float M = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 16; ++c)
-    if (c < CS) M = fmaxf(M, mc[c]);
+  for (int c = 0; c < CS; ++c) M = fmaxf(M, mc[c]);
   float den = 0.f;
 #pragma unroll
-  for (int c = 0; c < 16; ++c)
-    if (c < CS && lc[c] > 0.f) den += fast_exp2(mc[c] - M) * lc[c];
+  for (int c = 0; c < CS; ++c)
+    if (lc[c] > 0.f) den += fast_exp2(mc[c] - M) * lc[c];
   const float f = (nk > 0 && l > 0.f) ? fast_exp2(m - M) / den : 0.f;
   VLA_TL(a.tl, 0, 10);
 
@@ -280,12 +296,12 @@ __global__ void __launch_bounds__(128, 1)
     const int j = gk * a.group + jj;
     bf16* out = a.o + ((size_t)b * a.H + i) * (size_t)(a.n_q * dh) + (size_t)j * dh + rank * cols;
     for (int c8 = 0; c8 < q8; c8 += 2) {
-      uint4 v[2][16];
+      uint4 v[2][CS];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const bool held = (c8 + h) < q8 && c < CS && (c == CS - 1 || c * a.kc < a.P);
+        for (int c = 0; c < CS; ++c) {
+          const bool held = (c8 + h) < q8 && (c == CS - 1 || c * a.kc < a.P);
           v[h][c] = held ? __ldcg((const uint4*)(a.xo + (cl * CS + c) * 128 * (size_t)dh) +
                                   (size_t)(rank * q8 + c8 + h) * 128 + row)
                          : make_uint4(0u, 0u, 0u, 0u);
@@ -295,7 +311,7 @@ __global__ void __launch_bounds__(128, 1)
         if (c8 + h >= q8) break;
         float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < CS; ++c) {
           const uint32_t w[4] = {v[h][c].x, v[h][c].y, v[h][c].z, v[h][c].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -333,17 +349,24 @@ __global__ void __launch_bounds__(128, 1)
 
 size_t attn_tc_smem_bytes(int d_h, int kc) { return 1024 + attn_layout(d_h, kc).total; }
 
+template <bool O32, int CS>
+cudaError_t attn_init_one() {
+  cudaError_t e = set_max_dyn_smem(k_attn_tc<O32, CS>);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc<O32, CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
 cudaError_t attn_kernels_init() {
-  cudaError_t e = set_max_dyn_smem(k_attn_tc<false>);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_tc<true>);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = attn_init_one<false, 8>();
+  if (e == cudaSuccess) e = attn_init_one<false, 16>();
+  if (e == cudaSuccess) e = attn_init_one<true, 8>();
+  if (e == cudaSuccess) e = attn_init_one<true, 16>();
   return e;
 }
 
 cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
                            const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st) {
-  if (a.d_h % 64 || a.d_h > 256 || a.d_h < 64 || a.cs < 2 || a.cs > 16 || (a.cs & (a.cs - 1)) || a.kc < 16 ||
+  if (a.d_h % 64 || a.d_h > 256 || a.d_h < 64 || (a.cs != 8 && a.cs != 16) || a.kc < 16 ||
       a.kc > 128 || a.kc % 16 || a.kc_s < 16 || a.kc_s > 128 || a.kc_s % 16 || (a.d_h / a.cs) % 8)
     return cudaErrorInvalidValue;
   const int kmax = a.kc > a.kc_s ? a.kc : a.kc_s;
@@ -363,6 +386,10 @@ cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_tc<true>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
-  return cudaLaunchKernelEx(&cfg, k_attn_tc<false>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  if (a.cs == 8) {
+    if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_tc<true, 8>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+    return cudaLaunchKernelEx(&cfg, k_attn_tc<false, 8>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  }
+  if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_tc<true, 16>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  return cudaLaunchKernelEx(&cfg, k_attn_tc<false, 16>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
 }

@@ -47,13 +47,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Optional event trace (built only with -DVLA_TIMELINE): thread `who` of each
-// CTA stores %globaltimer for event `ev` (< 16) into tl[cta * 16 + ev].
+// CTA stores a timestamp for event `ev` (< 16) into tl[cta * 16 + ev]:
+// %globaltimer (comparable across SMs and kernels, coarse), or with
+// -DVLA_TIMELINE_CYCLES the SM's cycle counter (fine, comparable only within
+// one CTA).
+#ifdef VLA_TIMELINE_CYCLES
+#define VLA_TL_NOW() ((unsigned long long)clock64())
+#else
+#define VLA_TL_NOW() globaltimer_ns()
+#endif
 #ifdef VLA_TIMELINE
 #define VLA_TL(tl, who, ev)                                                                          \
   do {                                                                                               \
     if ((tl) != nullptr && threadIdx.x == (who))                                                     \
       (tl)[((size_t)blockIdx.x + gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z)) * 16 + (ev)] = \
-          globaltimer_ns();                                                                          \
+          VLA_TL_NOW();                                                                              \
   } while (0)
 #else
 #define VLA_TL(tl, who, ev) \
