@@ -160,16 +160,19 @@ __global__ void __launch_bounds__(128, 1)
       }
       const uint8_t* pk = Pk + (size_t)s * kPk;
       const uint32_t at = smem_u32(Abase + (size_t)s * kA);
-#pragma unroll 4
-      for (int e = dt; e < 1024; e += 64) {
-        const int r = e >> 3, ch = e & 7;
-        const uint32_t two = *(const uint16_t*)(pk + r * 16 + ch * 2);  // codes of k = 8ch .. 8ch+7
-        uint4 o;
-        o.x = ternary_pair_bf16(two & 0xFu);
-        o.y = ternary_pair_bf16((two >> 4) & 0xFu);
-        o.z = ternary_pair_bf16((two >> 8) & 0xFu);
-        o.w = ternary_pair_bf16((two >> 12) & 0xFu);
-        st_shared_v4_u32(at + sw128_offset((uint32_t)r, (uint32_t)ch), o);
+      // Rows dt and dt + 64: one 16-byte load of 64 codes each, eight
+      // 16-byte chunks out (consecutive lanes cover all eight swizzle phases).
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = dt + h * 64;
+        const uint4 cw = *(const uint4*)(pk + r * 16);
+        const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {  // codes of k = 8ch .. 8ch+7
+          const uint32_t two = (wd[ch >> 1] >> ((ch & 1) * 16)) & 0xFFFFu;
+          const uint2 lo = ternary_quad_bf16(two & 0xFFu), hi = ternary_quad_bf16(two >> 8);
+          st_shared_v4_u32(at + sw128_offset((uint32_t)r, (uint32_t)ch), make_uint4(lo.x, lo.y, hi.x, hi.y));
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();

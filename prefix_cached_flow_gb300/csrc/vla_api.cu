@@ -556,21 +556,32 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
     VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
     for (int l = 0; l < L; ++l) {
       const float* mod = h->modtab + ((size_t)k * L + l) * 4 * D;
+#ifdef VLA_TIMELINE
+      auto tls = [&](int kidx) -> unsigned long long* {
+        return (h->tl && k == 1 && l >= 1 && l <= 4) ? h->tl + ((size_t)((l - 1) * 5 + kidx)) * 4096 * 16 : nullptr;
+      };
+#else
+      auto tls = [&](int) -> unsigned long long* { return nullptr; };
+#endif
       VLA_CK(launch_quant_norm(d, h->h, mod, mod + D, act, h->alpha, st));
       LinArgs a = lin_args(h, pq, h->qkvdim, T, l);
+      a.tl = tls(0);
       a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
       VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
-      VLA_ST(enqueue_attention(ap, l, nullptr, st));
+      VLA_ST(enqueue_attention(ap, l, tls(1), st));
       VLA_CK(launch_quant_rows(T, Q, h->f32buf, act, h->alpha, st));
       a = lin_args(h, po, D, T, l);
+      a.tl = tls(2);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.beta_slot = 3;
       VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
       VLA_CK(launch_quant_norm(d, h->h, mod + 2 * D, mod + 3 * D, act, h->alpha, st));
       a = lin_args(h, pu, F, T, l);
+      a.tl = tls(3);
       a.epi = EPI_GELU; a.g32 = h->f32buf; a.ldg = F; a.beta_slot = 4;
       VLA_CK(launch_linear(&h->tm_wup, &tm_u, &tmH, a, pu.tiles_n, pu.tiles_t, pu.C, st));
       VLA_CK(launch_quant_rows(T, F, h->f32buf, act, h->alpha, st));
       a = lin_args(h, pd, D, T, l);
+      a.tl = tls(4);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.beta_slot = 5;
       VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
     }

@@ -131,13 +131,18 @@ __device__ __forceinline__ float w2a8_scale(float acc, float alpha, float beta) 
   return __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(acc, alpha), beta)));
 }
 
-// Two ternary 2-bit codes (c0 in bits 0-1, c1 in bits 2-3; code = q + 1) as
-// a bf16x2 word with q0 in the low half: -1 -> 0xBF80, 0 -> 0, +1 -> 0x3F80.
-__device__ __forceinline__ uint32_t ternary_pair_bf16(uint32_t nib) {
-  const uint32_t c0 = nib & 3u, c1 = nib >> 2;
-  const uint32_t v0 = (c0 == 1u) ? 0u : (0x3F80u | (c0 == 0u ? 0x8000u : 0u));
-  const uint32_t v1 = (c1 == 1u) ? 0u : (0x3F80u | (c1 == 0u ? 0x8000u : 0u));
-  return v0 | (v1 << 16);
+// Four ternary codes (one byte, code c_i = q_i + 1 in bits 2i..2i+1) as two
+// bf16x2 words, element 0 in the low half of the first: a byte-permute table
+// lookup.  Selector nibble i is c_i; the tables hold, for codes 0..3, the
+// high bytes (BF 00 3F 00) and the low bytes (80 00 80 00) of -1, 0, +1, 0.
+__device__ __forceinline__ uint2 ternary_quad_bf16(uint32_t byte) {
+  const uint32_t sel = (byte & 0x3u) | ((byte & 0xCu) << 2) | ((byte & 0x30u) << 4) | ((byte & 0xC0u) << 6);
+  uint32_t hi, lo, w0, w1;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(0x003F00BFu), "r"(0x00800080u), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(0x003F00BFu), "r"(0x00800080u), "r"(sel | 0x4444u));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w0) : "r"(lo), "r"(hi), "r"(0x5140u));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(w1) : "r"(lo), "r"(hi), "r"(0x7362u));
+  return make_uint2(w0, w1);
 }
 
 __device__ __forceinline__ float gelu_exact(float x) {
