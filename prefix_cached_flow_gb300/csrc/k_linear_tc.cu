@@ -60,13 +60,14 @@ __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   return s;
 }
 
-template <int EPI, int AMODE, int BMODE, bool SPLIT>
+template <int EPI, int AMODE, int BMODE, int CS>
 __global__ void __launch_bounds__(128, 1)
     k_linear(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmH, const LinArgs g) {
-  // EPI, AMODE (1: packed ternary weights, W2A8 scaling), BMODE and SPLIT
-  // (cluster size > 1) are compile-time so that every instantiation carries
-  // only its own path.
+  // EPI, AMODE (1: packed ternary weights, W2A8 scaling), BMODE and the
+  // cluster size CS (1: no split) are compile-time so that every
+  // instantiation carries only its own path: these CTAs run their code once,
+  // and instruction fetch is a large part of their time.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const LinSmem Ls = lin_layout(g);
@@ -92,7 +93,8 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * 128;
   const int t0 = blockIdx.y * BN;
-  const int C = gridDim.z;
+  constexpr bool SPLIT = CS > 1;
+  constexpr int C = CS;
   const int rank = blockIdx.z;
   const int k0 = rank * g.KS;
   uint32_t ncols = 32;
@@ -499,15 +501,15 @@ __global__ void __launch_bounds__(128, 1)
     if (iters < 2) lv1 = false;
     const float* p0 = tpart + (size_t)cl0 * 128 + rank * RPR + qd0 * 4;
     const float* p1 = tpart + (size_t)cl1 * 128 + rank * RPR + qd1 * 4;
-    float4 v0[kMaxC], v1[kMaxC];
+    float4 v0[C], v1[C];
 #pragma unroll
-    for (int c = 0; c < kMaxC; ++c) {
-      v0[c] = (c < C && lv0) ? __ldcg((const float4*)(p0 + (size_t)c * BN * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      v1[c] = (c < C && lv1) ? __ldcg((const float4*)(p1 + (size_t)c * BN * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < C; ++c) {
+      v0[c] = lv0 ? __ldcg((const float4*)(p0 + (size_t)c * BN * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v1[c] = lv1 ? __ldcg((const float4*)(p1 + (size_t)c * BN * 128)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
 #pragma unroll
-    for (int c = 0; c < kMaxC; ++c) {
+    for (int c = 0; c < C; ++c) {
       a0.x += v0[c].x; a0.y += v0[c].y; a0.z += v0[c].z; a0.w += v0[c].w;
       a1.x += v1[c].x; a1.y += v1[c].y; a1.z += v1[c].z; a1.w += v1[c].w;
     }
@@ -518,15 +520,15 @@ __global__ void __launch_bounds__(128, 1)
     bool live;
     int col, quad;
     geom(it, live, col, quad);
-    float4 v[kMaxC];
+    float4 v[C];
 #pragma unroll
-    for (int c = 0; c < kMaxC; ++c)
-      v[c] = (c < C && live) ? __ldcg((const float4*)(tpart + (size_t)c * BN * 128 + (size_t)col * 128 + rank * RPR +
+    for (int c = 0; c < C; ++c)
+      v[c] = live ? __ldcg((const float4*)(tpart + (size_t)c * BN * 128 + (size_t)col * 128 + rank * RPR +
                                                       quad * 4))
                              : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < kMaxC; ++c) {
+    for (int c = 0; c < C; ++c) {
       acc.x += v[c].x; acc.y += v[c].y; acc.z += v[c].z; acc.w += v[c].w;
     }
     epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false);
@@ -541,12 +543,12 @@ __global__ void __launch_bounds__(128, 1)
     if (rank == 0 && ok) {
       const float* tss = g.xss + (size_t)tile * C * BN;
       for (int col = threadIdx.x; col < tcols; col += 128) {
-        float v[kMaxC];
+        float v[C];
 #pragma unroll
-        for (int c = 0; c < kMaxC; ++c) v[c] = c < C ? __ldcg(tss + (size_t)c * BN + col) : 0.f;
+        for (int c = 0; c < C; ++c) v[c] = __ldcg(tss + (size_t)c * BN + col);
         float s2 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kMaxC; ++c) s2 += v[c];
+        for (int c = 0; c < C; ++c) s2 += v[c];
         g.ss_out[(size_t)blockIdx.x * g.T + t0 + col] = s2;
       }
     }
@@ -574,10 +576,16 @@ size_t linear_smem_bytes(const LinArgs& g) { return 1024 + lin_layout(g).total; 
 
 template <int EPI, int AMODE, int BMODE>
 cudaError_t init_one() {
-  cudaError_t e = set_max_dyn_smem(k_linear<EPI, AMODE, BMODE, false>);
-  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear<EPI, AMODE, BMODE, true>);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_linear<EPI, AMODE, BMODE, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = set_max_dyn_smem(k_linear<EPI, AMODE, BMODE, 1>);
+#define VLA_LIN_INIT(CSZ)                                                                                   \
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear<EPI, AMODE, BMODE, CSZ>);                          \
+  if (e == cudaSuccess)                                                                                   \
+    e = cudaFuncSetAttribute(k_linear<EPI, AMODE, BMODE, CSZ>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  VLA_LIN_INIT(2)
+  VLA_LIN_INIT(4)
+  VLA_LIN_INIT(8)
+  VLA_LIN_INIT(16)
+#undef VLA_LIN_INIT
   return e;
 }
 
@@ -606,8 +614,10 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
   const size_t smem = linear_smem_bytes(g);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   void (*fn)(CUtensorMap, CUtensorMap, CUtensorMap, LinArgs) = nullptr;
-#define VLA_LIN_CASE(E, A, B) \
-  if (g.epi == E && g.amode == A && g.bmode == B) fn = C > 1 ? k_linear<E, A, B, true> : k_linear<E, A, B, false>;
+#define VLA_LIN_CASE(E, A, B)                                                                             \
+  if (g.epi == E && g.amode == A && g.bmode == B)                                                        \
+    fn = C == 16 ? k_linear<E, A, B, 16>                                                                 \
+                 : (C == 8 ? k_linear<E, A, B, 8> : (C == 4 ? k_linear<E, A, B, 4> : (C == 2 ? k_linear<E, A, B, 2> : k_linear<E, A, B, 1>)));
   VLA_LIN_CASE(EPI_QKV, 0, 0)
   VLA_LIN_CASE(EPI_QKV, 0, 1)
   VLA_LIN_CASE(EPI_RESID, 0, 0)
