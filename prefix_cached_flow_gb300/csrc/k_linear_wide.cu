@@ -31,15 +31,17 @@ constexpr int kEpiWarps = 8;
 constexpr int kWideThreads = 64 + 32 * kEpiWarps;
 
 struct WideSmem {
-  uint32_t a, b, wss, bars, slot, total;
+  uint32_t a, b, wss, stg, bars, slot, total;
 };
+constexpr int kStg = 32 * 34;  // bf16 staging elements per epilogue warp (32 x 32 chunk, rows padded to 34)
 
 __host__ __device__ inline WideSmem wide_layout(int BN) {
   WideSmem s;
   s.a = 0;
   s.b = (uint32_t)kWS * kWA;
   s.wss = s.b + (uint32_t)kWS * (uint32_t)BN * 128u;  // [2 tile parities][2 halves][4 quarters][BN/2] fp32
-  s.bars = s.wss + 16u * (uint32_t)(BN / 2) * 4u;
+  s.stg = s.wss + 16u * (uint32_t)(BN / 2) * 4u;      // [8 warps][kStg] bf16
+  s.bars = s.stg + (uint32_t)kEpiWarps * kStg * 2u;
   s.slot = s.bars + (2 * kWS + 5) * 8;
   s.total = s.slot + 16;
   return s;
@@ -61,6 +63,20 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) 
   return v[0];
 }
 
+// GeLU x * Phi(x) with erf by Abramowitz & Stegun, Handbook of Mathematical
+// Functions, formula 7.1.26 (|error of erf| <= 1.5e-7, far below the bf16
+// rounding of the output): erf(z) ~ 1 - t (a1 + a2 t + ... + a5 t^4) e^(-z^2),
+// t = 1 / (1 + p z), z >= 0, odd extension for negative arguments.
+__device__ __forceinline__ float gelu_as7126(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  const float tail = poly * fast_exp2(-z * z * 1.4426950408889634f);  // 1 - erf(z)
+  const float erfv = copysignf(1.f - tail, x);
+  return 0.5f * x * (1.f + erfv);
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kWideThreads, 1)
     k_linear_wide(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const LinArgs g) {
@@ -71,6 +87,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   uint8_t* As = smem + Ls.a;
   uint8_t* Bs = smem + Ls.b;
   float* wss = (float*)(smem + Ls.wss);
+  bf16* stg_all = (bf16*)(smem + Ls.stg);
   uint64_t* full = (uint64_t*)(smem + Ls.bars);
   uint64_t* empty = full + kWS;
   uint64_t* accf = empty + kWS;  // [2] accumulator ready (MMA commit)
@@ -226,29 +243,56 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           }
           const float cs = warp_transpose_sum32(hv, lane);
           wq[c0 - half * hbn + lane] = cs;
-        } else if (EPI == EPI_GELU) {
-          bf16* gp = g.g + (size_t)(t0 + c0) * g.ldg + n;
+        } else {
+          // GeLU and QKV: stage the warp's 32 x 32 bf16 chunk in shared
+          // memory, then write whole rows.  The warp's 32 output rows are
+          // consecutive features inside one head of one of q, k, v.
+          bf16* stg = stg_all + (size_t)(warp - 2) * kStg;
+          const int nb = m0 + quarter * 32;  // the warp's first output row
+          const bool vt = EPI == EPI_QKV && slot == 2;
+          __syncwarp();
+          if (!vt) {
+            // token-major outputs (g, q, k): [col][row] so a token's 32 features are 64 contiguous bytes
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nv) gp[(size_t)j * g.ldg] = __float2bfloat16_rn(gelu_exact(__uint_as_float(r[j])));
-        } else {  // EPI_QKV
-          int b = (t0 + c0) / g.H, i = (t0 + c0) - b * g.H;
-          const int rr = slot == 0 ? n : (slot == 1 ? n - g.qdim : n - g.qdim - g.kvdim);
-          const int hd = rr / g.d_h, d = rr - hd * g.d_h;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j < nv) {
-              const bf16 bv = __float2bfloat16_rn(__uint_as_float(r[j]));
-              if (slot == 0)
-                g.q[(((size_t)b * g.n_q + hd) * g.H + i) * g.d_h + d] = bv;
-              else if (slot == 1)
-                g.ks[(((size_t)b * g.n_kv + hd) * g.H + i) * g.d_h + d] = bv;
-              else
-                g.vst[(((size_t)b * g.n_kv + hd) * g.d_h + d) * g.Hp + i] = bv;
+            for (int j = 0; j < 32; ++j) {
+              const float y = __uint_as_float(r[j]);
+              stg[j * 32 + lane] = __float2bfloat16_rn(EPI == EPI_GELU ? gelu_as7126(y) : y);
             }
-            if (++i == g.H) {
-              i = 0;
-              ++b;
+            __syncwarp();
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {  // 8 tokens per pass, 4 lanes x 16 bytes per token
+              const int j = pass * 8 + (lane >> 2), part = lane & 3;
+              if (j < nv) {
+                const uint4 v = *(const uint4*)(stg + j * 32 + part * 8);
+                const int t = t0 + c0 + j;
+                bf16* dst;
+                if (EPI == EPI_GELU) {
+                  dst = g.g + (size_t)t * g.ldg + nb;
+                } else {
+                  const int b = t / g.H, i = t - b * g.H;
+                  const int rr = slot == 0 ? nb : nb - g.qdim;
+                  const int hd = rr / g.d_h, d0 = rr - hd * g.d_h;
+                  dst = slot == 0 ? g.q + (((size_t)b * g.n_q + hd) * g.H + i) * g.d_h + d0
+                                  : g.ks + (((size_t)b * g.n_kv + hd) * g.H + i) * g.d_h + d0;
+                }
+                *(uint4*)(dst + part * 8) = v;
+              }
+            }
+          } else {
+            // v_s^T [B][n_kv][d_h][Hp] is token-contiguous per feature: stage
+            // [row][col] (rows padded to 34 elements: conflict-free writes),
+            // then one feature row of 32 tokens per warp store.
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg[lane * 34 + j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+            __syncwarp();
+            const int rr0 = nb - g.qdim - g.kvdim;
+            const int hd = rr0 / g.d_h, d0 = rr0 - hd * g.d_h;
+            const int t = t0 + c0 + lane;
+            const int b = t / g.H, i = t - b * g.H;
+            bf16* col = g.vst + (((size_t)b * g.n_kv + hd) * g.d_h + d0) * g.Hp + i;
+            if (lane < nv) {
+#pragma unroll 4
+              for (int rw = 0; rw < 32; ++rw) col[(size_t)rw * g.Hp] = stg[rw * 34 + lane];
             }
           }
         }
