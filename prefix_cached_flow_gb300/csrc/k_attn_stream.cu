@@ -56,7 +56,7 @@ __host__ __device__ inline StreamSmem stream_layout(int d_h) {
 }
 
 enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 7, B_SF = 9, B_PF = 11, B_PV = 13, B_FIN = 15, B_XL = 16,
-       B_ST = 17, N_BARS = 18 };
+       B_ST = 17, B_QT = 18, N_BARS = 19 };
 constexpr int NSM = 256;  // softmax threads
 
 __device__ __forceinline__ void tma_load_3d_s(void* dst, const void* map, uint64_t* bar, int x, int y, int z) {
@@ -101,8 +101,12 @@ __global__ void __launch_bounds__(352, 1)
   const int b = bg / a.n_kv, gk = bg - b * a.n_kv;
   const int n_pre = (a.P + KB - 1) / KB, n_suf = (a.H + KB - 1) / KB;
   const int nch = n_pre + n_suf;
-  const uint32_t ncols = dh + 2 * KB <= 256 ? 256u : 512u;  // O (d_h columns) + two S buffers
+  // TMEM: O (d_h columns), two S buffers (KB columns each), Q (d_h / 2
+  // columns of bf16 pairs: the S MMA reads its A operand from here, not
+  // from shared memory, which leaves shared-memory bandwidth to K).
+  const uint32_t ncols = dh + 2 * KB + dh / 2 <= 256 ? 256u : 512u;
   const uint32_t s_col = (uint32_t)dh;
+  const uint32_t q_col = (uint32_t)(dh + 2 * KB);
 
   if (threadIdx.x == 0) {
     s_fail = 0;
@@ -119,6 +123,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&bars[B_FIN], 1);
     mbar_init(&bars[B_XL], NSM);
     mbar_init(&bars[B_ST], NSM);
+    mbar_init(&bars[B_QT], NSM);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, KB);
       const uint32_t idesc_o = idesc_bf16_f32(128, dh);
-      bool ok = mbar_wait(&bars[B_Q], 0, a.status);
+      bool ok = mbar_wait(&bars[B_QT], 0, a.status);
       auto pv = [&](int i) -> bool {
         const int st = i & 1;
         if (!mbar_wait(&bars[B_PF + st], (uint32_t)(i >> 1) & 1u, a.status)) return false;
@@ -210,11 +215,11 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_after();
         const uint32_t ka = smem_u32(Ks + (size_t)st * nsub * 8192);
         for (int s = 0; s < nsub; ++s) {
-          const uint32_t qa = smem_u32(Qs + (size_t)s * 16384), kb = ka + (uint32_t)s * 8192u;
+          const uint32_t kb = ka + (uint32_t)s * 8192u;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(tmem + s_col + (uint32_t)(st * KB), sdesc_k128(qa + k * 32), sdesc_k128(kb + k * 32), idesc_s,
-                      (s > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)  // K step of 16 = 8 TMEM columns of Q
+            umma_bf16_ts(tmem + s_col + (uint32_t)(st * KB), tmem + q_col + (uint32_t)((s * 4 + k) * 8),
+                         sdesc_k128(kb + k * 32), idesc_s, (s > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_SF + st]);
         umma_commit(&bars[B_KE + st]);
@@ -239,8 +244,31 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     const int hc = dh / 2;                // O columns of this half
     float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nch; ++j) {
+    bool ok = __all_sync(~0u, mbar_wait(&bars[B_Q], 0, a.status));
+    // Q row into TMEM (the S MMA's A operand): groups of four 16-byte chunks
+    // (32 bf16 = 16 columns) read from the 128-byte-swizzled shared tile;
+    // the two warps of a lane quarter take half of the groups each.
+    if (ok) {
+      const int G = nsub * 2;
+      for (int gi = half * G / 2; gi < (half + 1) * G / 2; ++gi) {
+        const uint8_t* rowp = Qs + (size_t)(gi >> 1) * 16384 + (size_t)row * 128;
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t j = (uint32_t)((gi & 1) * 4 + q);
+          const uint4 u = *(const uint4*)(rowp + ((j ^ (uint32_t)(row & 7)) << 4));
+          w[q * 4 + 0] = u.x;
+          w[q * 4 + 1] = u.y;
+          w[q * 4 + 2] = u.z;
+          w[q * 4 + 3] = u.w;
+        }
+        tmem_st16(trow + q_col + (uint32_t)(gi * 16), w);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    mbar_arrive(&bars[B_QT]);
+    for (int j = 0; ok && j < nch; ++j) {
       const int st = j & 1;
       if (!__all_sync(~0u, mbar_wait(&bars[B_SF + st], (uint32_t)(j >> 1) & 1u, a.status))) {
         ok = false;
