@@ -50,7 +50,7 @@ __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   s.pk = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
   const uint32_t end = s.pk + (g.amode == 1 ? (uint32_t)g.stages * kPk : 0u);
   s.region = end;
-  s.bars = s.region;                                  // full, empty, done, hbar, aready, bfull
+  s.bars = s.region;                                  // full, empty, done, hbar, aready (+ spare)
   s.slot = s.bars + (4u * (uint32_t)g.stages + 2u) * 8u;
   s.rstat = s.slot + 16u;                             // [BN] (also the epilogue's per-token sums)
   s.gam = s.rstat + (uint32_t)g.BN * 4u;              // [KS]
@@ -82,8 +82,7 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t* empty = full + NS;
   uint64_t* done = empty + NS;
   uint64_t* hbar = done + 1;
-  uint64_t* aready = hbar + 1;  // [NS]: decoded ternary A tile ready (amode 1)
-  uint64_t* bfull = aready + NS; // [NS]: B tile landed (amode 1; amode 0 uses full[])
+  uint64_t* aready = hbar + 1;  // [NS]: decoded ternary A tile and its B tile ready (amode 1)
   uint32_t* tmem_slot = (uint32_t*)(smem + Ls.slot);
   float* rstat = (float*)(smem + Ls.rstat);
   float* gam = (float*)(smem + Ls.gam);
@@ -110,8 +109,7 @@ __global__ void __launch_bounds__(128, 1)
     mbar_init(done, 1);
     mbar_init(hbar, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&aready[s], 2);
-      mbar_init(&bfull[s], 1);
+      mbar_init(&aready[s], 3);  // two decoder warps + the producer's B-tile transaction
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -130,8 +128,9 @@ __global__ void __launch_bounds__(128, 1)
   // Weight prefetch: independent of every earlier kernel.
   const int pre = nkb < NS ? nkb : NS;
   // full[s] carries the A stage (and, for bf16 weights with TMA'd tokens, the
-  // B stage); packed ternary stages put their B tile on bfull[s] instead, so
-  // the codes can be decoded before the previous kernel has finished.
+  // B stage); packed ternary stages put their B tile on aready[s] (with the
+  // decoders' arrivals) instead, so the codes can be decoded before the
+  // previous kernel has finished.
   const uint32_t stage_tx = AMODE == 1 ? kPk : kA + (BMODE == 0 ? b_tile : 0u);
   // A stage i: bf16 tile by TMA, or its 2-bit codes (16 bytes per row per 64 K)
   auto load_a = [&](int i, int s, uint64_t pol) {
@@ -192,8 +191,8 @@ __global__ void __launch_bounds__(128, 1)
       for (int i = 0; i < nkb; ++i) tma_load_2d(Hs + (size_t)i * BN * 64, &tmH, hbar, k0 + i * 64, t0);
     } else if (AMODE == 1) {
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&bfull[i], b_tile);
-        tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &bfull[i], k0 + i * 64, t0);
+        mbar_arrive_expect_tx(&aready[i], b_tile);
+        tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &aready[i], k0 + i * 64, t0);
       }
     } else {
       for (int i = 0; i < pre; ++i) tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &full[i], k0 + i * 64, t0);
@@ -260,8 +259,8 @@ __global__ void __launch_bounds__(128, 1)
       mbar_arrive_expect_tx(&full[s], stage_tx);
       load_a(i, s, pol);
       if (AMODE == 1) {
-        mbar_arrive_expect_tx(&bfull[s], b_tile);
-        tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &bfull[s], k0 + i * 64, t0);
+        mbar_arrive_expect_tx(&aready[s], b_tile);
+        tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &aready[s], k0 + i * 64, t0);
       } else if (BMODE == 0) {
         tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &full[s], k0 + i * 64, t0);
       }
@@ -272,20 +271,24 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t idesc = idesc_bf16_f32(128, BN);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % NS;
-      if (s_fail || !mbar_wait(&full[s], (i / NS) & 1, g.status) ||
-          (AMODE == 1 && (!mbar_wait(&aready[s], (i / NS) & 1, g.status) ||
-                            !mbar_wait(&bfull[s], (i / NS) & 1, g.status)))) {
+      // One wait per stage: the TMA transaction of the stage (bf16 weights),
+      // or the decoded tile plus its B tile (packed ternary weights).
+      if (s_fail || !mbar_wait(AMODE == 1 ? &aready[s] : &full[s], (i / NS) & 1, g.status)) {
         s_fail = 1;
         break;
       }
       if (i == 0) VLA_TL(g.tl, 32, 3);
+      if (i == 1) VLA_TL(g.tl, 32, 12);
+      if (i == 2) VLA_TL(g.tl, 32, 13);
+      if (i == 3) VLA_TL(g.tl, 32, 14);
+      if (i == nkb - 1) VLA_TL(g.tl, 32, 15);
       tc_fence_after();
       const uint32_t a_addr = smem_u32(Abase + (size_t)s * kA);
       const uint32_t b_addr = smem_u32(Bbase + (size_t)(BMODE == 0 ? s : i) * b_tile);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_bf16(tmem, sdesc_k128(a_addr + k * 32), sdesc_k128(b_addr + k * 32), idesc, (i > 0 || k > 0) ? 1u : 0u);
-      umma_commit(&empty[s]);
+      if (i + NS < nkb) umma_commit(&empty[s]);  // only a stage that will be refilled needs releasing
     }
     umma_commit(done);
     VLA_TL(g.tl, 32, 4);
@@ -560,7 +563,7 @@ __global__ void __launch_bounds__(128, 1)
     const int first = issued > NS ? issued - NS : 0;
     for (int i = first; i < issued; ++i) {
       mbar_wait(&full[i % NS], (i / NS) & 1, g.status);
-      if (AMODE == 1) mbar_wait(&bfull[i % NS], (i / NS) & 1, g.status);
+      if (AMODE == 1) mbar_wait(&aready[i % NS], (i / NS) & 1, g.status);
     }
     if (BMODE == 1) mbar_wait(hbar, 0, g.status);
   }
