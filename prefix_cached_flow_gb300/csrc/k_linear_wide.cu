@@ -5,8 +5,9 @@
 // queries and action keys/values for the joint attention):
 //   y[t][n] = sum_k W[n][k] X[t][k]
 // followed by EPI_QKV (scatter to q, k_s, v_s^T), EPI_RESID (h += y and the
-// per-(128-row block, token) sums of squares of the new h) or EPI_GELU
-// (g = bf16(GeLU(y))).
+// per-(128-row block, token) sums of squares of the new h), EPI_GELU
+// (g = bf16(GeLU(y))) or EPI_KV (the prefix cache, §III-B Eq. (2): K_C and
+// the transposed V_C of every layer from one GEMM over all layers' W_K, W_V).
 //
 // At batch 1 the layer is a weight stream and k_linear splits K over a
 // cluster; with thousands of tokens it is a dense GEMM, and this kernel is a
@@ -211,11 +212,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
       const int buf = lt & 1;
-      const bool okw = __all_sync(0xffffffffu, mbar_wait(&accf[buf], (lt >> 1) & 1, g.status));
-      tc_fence_after();
       const int m0 = (tile % tiles_n) * 128, t0 = (tile / tiles_n) * BN;
       const int n = m0 + row;
       const int tcols = (g.T - t0) < BN ? (g.T - t0) : BN;
+      // Residual rows of this tile's columns (only this tile touches them):
+      // the first chunk is fetched while the MMAs run, each next chunk
+      // while the current one is processed.
+      float hcur[32];
+      auto load_h = [&](int cc, float (&hb)[32]) {
+        const int nvv = tcols - cc;
+        const float* hq = g.h + (size_t)(t0 + cc) * g.D + n;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) hb[j] = j < nvv ? hq[(size_t)j * g.D] : 0.f;
+      };
+      if (EPI == EPI_RESID) load_h(half * hbn, hcur);
+      const bool okw = __all_sync(0xffffffffu, mbar_wait(&accf[buf], (lt >> 1) & 1, g.status));
+      tc_fence_after();
       if (EPI == EPI_QKV) slot = n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2);
       float* wq = wss + ((size_t)(buf * 2 + half) * 4 + quarter) * hbn;  // this warp's column sums
       for (int c0 = half * hbn; c0 < (half + 1) * hbn; c0 += 32) {
@@ -231,25 +243,40 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         }
         const int nv = okw ? (tcols - c0 < 32 ? tcols - c0 : 32) : 0;  // valid columns in this chunk
         if (EPI == EPI_RESID) {
+          const bool more = c0 + 32 < (half + 1) * hbn;
+          float hnxt[32];
+          if (more) load_h(c0 + 32, hnxt);
           float hv[32];
           float* hp = g.h + (size_t)(t0 + c0) * g.D + n;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) hv[j] = j < nv ? hp[(size_t)j * g.D] : 0.f;
-#pragma unroll
           for (int j = 0; j < 32; ++j) {
-            hv[j] += __uint_as_float(r[j]);
+            hv[j] = hcur[j] + __uint_as_float(r[j]);
             if (j < nv) hp[(size_t)j * g.D] = hv[j];
             hv[j] = j < nv ? hv[j] * hv[j] : 0.f;
           }
           const float cs = warp_transpose_sum32(hv, lane);
           wq[c0 - half * hbn + lane] = cs;
+          if (more) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) hcur[j] = hnxt[j];
+          }
         } else {
           // GeLU and QKV: stage the warp's 32 x 32 bf16 chunk in shared
           // memory, then write whole rows.  The warp's 32 output rows are
           // consecutive features inside one head of one of q, k, v.
           bf16* stg = stg_all + (size_t)(warp - 2) * kStg;
           const int nb = m0 + quarter * 32;  // the warp's first output row
-          const bool vt = EPI == EPI_QKV && slot == 2;
+          // EPI_KV: rows [L][K|V][n_kv][d_h]; the warp's 32 rows share (l, K|V, head)
+          int kl = 0, kwhich = 0, khd = 0, ke0 = 0;
+          if (EPI == EPI_KV) {
+            kl = nb / (2 * g.kvdim);
+            const int rem = nb - kl * 2 * g.kvdim;
+            kwhich = rem / g.kvdim;
+            const int r2 = rem - kwhich * g.kvdim;
+            khd = r2 / g.d_h;
+            ke0 = r2 - khd * g.d_h;
+          }
+          const bool vt = (EPI == EPI_QKV && slot == 2) || (EPI == EPI_KV && kwhich == 1);
           __syncwarp();
           if (!vt) {
             // token-major outputs (g, q, k): [col][row] so a token's 32 features are 64 contiguous bytes
@@ -268,6 +295,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 bf16* dst;
                 if (EPI == EPI_GELU) {
                   dst = g.g + (size_t)t * g.ldg + nb;
+                } else if (EPI == EPI_KV) {
+                  const int b = t / g.kv_P, pp = t - b * g.kv_P;
+                  dst = g.kc_out + ((((size_t)kl * g.kv_B + b) * g.n_kv + khd) * g.kv_P + pp) * g.d_h + ke0;
                 } else {
                   const int b = t / g.H, i = t - b * g.H;
                   const int rr = slot == 0 ? nb : nb - g.qdim;
@@ -285,14 +315,23 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) stg[lane * 34 + j] = __float2bfloat16_rn(__uint_as_float(r[j]));
             __syncwarp();
-            const int rr0 = nb - g.qdim - g.kvdim;
-            const int hd = rr0 / g.d_h, d0 = rr0 - hd * g.d_h;
             const int t = t0 + c0 + lane;
-            const int b = t / g.H, i = t - b * g.H;
-            bf16* col = g.vst + (((size_t)b * g.n_kv + hd) * g.d_h + d0) * g.Hp + i;
+            bf16* col;
+            size_t pitch;
+            if (EPI == EPI_KV) {
+              const int b = t / g.kv_P, pp = t - b * g.kv_P;
+              col = g.vc_out + ((((size_t)kl * g.kv_B + b) * g.n_kv + khd) * g.d_h + ke0) * g.kv_P8 + pp;
+              pitch = (size_t)g.kv_P8;
+            } else {
+              const int rr0 = nb - g.qdim - g.kvdim;
+              const int hd = rr0 / g.d_h, d0 = rr0 - hd * g.d_h;
+              const int b = t / g.H, i = t - b * g.H;
+              col = g.vst + (((size_t)b * g.n_kv + hd) * g.d_h + d0) * g.Hp + i;
+              pitch = (size_t)g.Hp;
+            }
             if (lane < nv) {
 #pragma unroll 4
-              for (int rw = 0; rw < 32; ++rw) col[(size_t)rw * g.Hp] = stg[rw * 34 + lane];
+              for (int rw = 0; rw < 32; ++rw) col[(size_t)rw * pitch] = stg[rw * 34 + lane];
             }
           }
         }
@@ -325,6 +364,7 @@ size_t linear_wide_smem_bytes(int BN) { return 1024 + wide_layout(BN).total; }
 
 cudaError_t linear_wide_init() {
   cudaError_t e = set_max_dyn_smem(k_linear_wide<EPI_QKV>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear_wide<EPI_KV>);
   if (e == cudaSuccess) e = set_max_dyn_smem(k_linear_wide<EPI_RESID>);
   if (e == cudaSuccess) e = set_max_dyn_smem(k_linear_wide<EPI_GELU>);
   return e;
@@ -333,12 +373,15 @@ cudaError_t linear_wide_init() {
 cudaError_t launch_linear_wide(const CUtensorMap* tmA, const CUtensorMap* tmB, const LinArgs& g, int grid,
                                cudaStream_t st) {
   if (g.BN < 64 || g.BN > 256 || g.BN % 64 || g.KS % 64 || g.KS < 64 || g.N % 128 || g.T < 1 || grid < 1 ||
-      g.amode != 0 || g.w2a8 != 0 || (g.epi != EPI_QKV && g.epi != EPI_RESID && g.epi != EPI_GELU))
+      g.amode != 0 || g.w2a8 != 0 ||
+      (g.epi != EPI_QKV && g.epi != EPI_RESID && g.epi != EPI_GELU && g.epi != EPI_KV))
     return cudaErrorInvalidValue;
   const size_t smem = linear_wide_smem_bytes(g.BN);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   void (*fn)(CUtensorMap, CUtensorMap, LinArgs) =
-      g.epi == EPI_QKV ? k_linear_wide<EPI_QKV> : (g.epi == EPI_RESID ? k_linear_wide<EPI_RESID> : k_linear_wide<EPI_GELU>);
+      g.epi == EPI_QKV ? k_linear_wide<EPI_QKV>
+                       : (g.epi == EPI_RESID ? k_linear_wide<EPI_RESID>
+                                             : (g.epi == EPI_GELU ? k_linear_wide<EPI_GELU> : k_linear_wide<EPI_KV>));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kWideThreads, 1, 1);

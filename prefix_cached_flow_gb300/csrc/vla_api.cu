@@ -961,6 +961,19 @@ vla_status vla_prefix_kv_build(vla_expert* h, const void* Z, int B, int P, void*
     VLA_CK(launch_gemm_simt(!h->f32, Z, K, !h->f32, h->wkv_pre, K, BP, N, K, 1, nullptr, 0, 0, &kv, st));
     return VLA_OK;
   }
+  if (wide_applies(c.flags, h->num_sms, N, K, BP)) {
+    // Many prefix tokens: the persistent kernel with the K / V^T scatter epilogue.
+    const LinPlan p = plan_wide(h->num_sms, N, K, BP);
+    CUtensorMap tmZw;
+    if (tc_encode_2d_bf16(&tmZw, Z, K, BP, 64, p.BN)) return VLA_ERR_CUDA;
+    LinArgs a{};
+    a.N = N; a.T = BP; a.a_row0 = 0; a.KS = K; a.BN = p.BN; a.stages = p.stages; a.epi = EPI_KV;
+    a.status = h->d_status;
+    a.n_kv = c.n_kv_heads; a.d_h = c.head_dim; a.kvdim = h->kvdim;
+    a.kc_out = (bf16*)Kc; a.vc_out = (bf16*)Vc; a.kv_B = B; a.kv_P = P; a.kv_P8 = round_up(P, 8);
+    VLA_CK(launch_linear_wide(&h->tm_wkv, &tmZw, a, p.grid, st));
+    return VLA_OK;
+  }
   const int BN = BP >= 256 ? 256 : round_up(BP < 16 ? 16 : BP, 16);
   CUtensorMap tmZ;
   if (tc_encode_2d_bf16(&tmZ, Z, K, BP, 64, BN)) return VLA_ERR_CUDA;

@@ -514,7 +514,7 @@ cudaError_t expert_kernels_init();
 cudaError_t launch_to_f32(const void* src, int src_bf16, float* dst, size_t n, cudaStream_t st);
 
 // Fused cluster split-K linear layer (k_linear_tc.cu).
-enum { EPI_QKV = 0, EPI_RESID = 1, EPI_GELU = 2, EPI_W2A8_OUT = 3 };
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_GELU = 2, EPI_W2A8_OUT = 3, EPI_KV = 4 };
 struct LinArgs {
   int N;        // output features (weight rows), multiple of 4
   int T;        // tokens
@@ -554,6 +554,10 @@ struct LinArgs {
   bf16* ks;            // [B][n_kv][H][d_h]
   bf16* vst;           // [B][n_kv][d_h][Hp]
   int H, n_q, n_kv, d_h, qdim, kvdim, Hp;
+  // EPI_KV (prefix K/V cache build, Eq. 2): rows [L][K|V][n_kv][d_h], tokens [B][P]
+  bf16* kc_out;  // K_C [L][B][n_kv][P][d_h]
+  bf16* vc_out;  // V_C^T [L][B][n_kv][d_h][P8]
+  int kv_B, kv_P, kv_P8;
   // split-K exchange through L2: [tile][rank][BN][128] fp32 partials and
   // [tile][rank][BN] per-token sums of squares (tile = tile_t * tiles_n + tile_n)
   float* xpart;
@@ -568,8 +572,9 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
                           int tiles_n, int tiles_t, int C, cudaStream_t st);
 
 // Persistent many-token linear kernel (k_linear_wide.cu): same LinArgs and
-// epilogues (EPI_QKV, EPI_RESID, EPI_GELU; bf16 weights, TMA'd tokens with a
-// 64 x BN box, KS = K), BN in {64, 128, 192, 256}, N a multiple of 128.
+// epilogues (EPI_QKV, EPI_RESID, EPI_GELU, and EPI_KV for the prefix K/V
+// build; bf16 weights, TMA'd tokens with a 64 x BN box, KS = K), BN in
+// {64, 128, 192, 256}, N a multiple of 128.
 size_t linear_wide_smem_bytes(int BN);
 cudaError_t linear_wide_init();
 cudaError_t launch_linear_wide(const CUtensorMap* tmA, const CUtensorMap* tmB, const LinArgs& g, int grid,
