@@ -20,6 +20,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMultiTokens = 256;  // from this many tokens the embed / head CTAs take several tokens
+constexpr int kEmbedThreads = 128;
+// CTAs per token of the per-token input projection (each writes its own
+// sum-of-squares slot; the slot buffer holds D / 128 + 1 of them).
+int embed_split(const ExpertDims& d) {
+  int s = d.D / 128;
+  return s > 8 ? 8 : (s < 1 ? 1 : s);
+}
 
 // ---------------------------------------------------------------------------
 // Time conditioning table (built once per handle; tau_k = k / S)
@@ -327,6 +334,9 @@ __global__ void k_head(ExpertDims d, StepBufs b, int step, int splits, float dt,
 
 // h = x W_in^T and its row sum of squares (one slot) for the first layer's
 // in-GEMM modulated RMSNorm; also latches the abort flag once per step.
+// The D features of a token are split over gridDim.y CTAs (kEmbedSplit at few
+// tokens, for parallelism); CTA y writes its partial sum of squares to slot
+// y of ss_out [slots][T], which the next norm sums in fixed order.
 __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -334,11 +344,13 @@ __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* s
   float* xs = sm;
   float* red = sm + d.d_a;
   const int t = blockIdx.x;
-  if (t == 0 && threadIdx.x == 0 && ctl.abort && *ctl.abort) latch_error(ctl.status, VLA_DEV_ABORTED);
+  const int per = (d.D + gridDim.y - 1) / gridDim.y;
+  const int i0 = blockIdx.y * per, i1 = i0 + per < d.D ? i0 + per : d.D;
+  if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0 && ctl.abort && *ctl.abort) latch_error(ctl.status, VLA_DEV_ABORTED);
   for (int j = threadIdx.x; j < d.d_a; j += blockDim.x) xs[j] = x_in[(size_t)t * d.d_a + j];
   __syncthreads();
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d.D; i += blockDim.x) {
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     const float* w = b.win + (size_t)i * d.d_a;
     float acc = 0.f;
     for (int j = 0; j < d.d_a; ++j) acc += xs[j] * w[j];
@@ -346,7 +358,7 @@ __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* s
     ss += acc * acc;
   }
   ss = block_sum(ss, red);
-  if (threadIdx.x == 0) ss_out[t] = ss;
+  if (threadIdx.x == 0) ss_out[(size_t)blockIdx.y * (d.B * d.H) + t] = ss;
 }
 
 // Many-token form of k_embed_ss: a CTA takes kMT consecutive tokens, so each
@@ -607,6 +619,8 @@ static cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+int embed_ss_slots(const ExpertDims& d) { return d.B * d.H >= kMultiTokens && d.d_a <= 256 ? 1 : embed_split(d); }
+
 cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float* x_in, float* ss_out, DevCtl ctl,
                             cudaStream_t st) {
   ExpertDims dd = d;
@@ -616,7 +630,8 @@ cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float*
   if (T >= kMultiTokens && d.d_a <= 256)
     return launch_pdl((const void*)k_embed_ss_multi, dim3((T + kMT - 1) / kMT), dim3(kThreads),
                       (size_t)(kMT * d.d_a + kMT * (kThreads / 32)) * sizeof(float), st, args);
-  return launch_pdl((const void*)k_embed_ss, dim3(T), dim3(kThreads), (size_t)(d.d_a + 32) * sizeof(float), st, args);
+  return launch_pdl((const void*)k_embed_ss, dim3(T, embed_split(d)), dim3(kEmbedThreads), (size_t)(d.d_a + 32) * sizeof(float),
+                    st, args);
 }
 
 cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss, int n_ss, const float* gamma,

@@ -480,7 +480,7 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
     const float* x_in = k == 0 ? noise : actions;
     const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
     VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
-    int n_ss = 1;  // slots of ss2 currently valid
+    int n_ss = embed_ss_slots(d);  // slots of ss2 currently valid
     for (int l = 0; l < L; ++l) {
       const float* mod = modt + ((size_t)k * L + l) * 4 * D;  // gamma_a, beta_a, gamma_m, beta_m
 #ifdef VLA_TIMELINE

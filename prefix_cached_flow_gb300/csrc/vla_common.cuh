@@ -671,6 +671,8 @@ cudaError_t launch_head(const ExpertDims& d, const StepBufs& b, int step, int sp
 // the in-GEMM prologue); the velocity head reading h directly.
 cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float* x_in, float* ss_out, DevCtl ctl,
                             cudaStream_t st);
+// Sum-of-squares slots k_embed_ss / k_embed_ss_multi write for this shape.
+int embed_ss_slots(const ExpertDims& d);
 cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss, int n_ss, const float* gamma,
                            const float* beta, bf16* u, cudaStream_t st);
 cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, float dt, const float* x_in,
