@@ -318,8 +318,12 @@ __global__ void k_head(ExpertDims d, StepBufs b, int step, int splits, float dt,
   const float* bf = gf + d.D;
   for (int i = threadIdx.x; i < d.D; i += blockDim.x) row[i] = row[i] * r * (1.f + gf[i]) + bf[i];
   __syncthreads();
+  // The d_a outputs are split over gridDim.y CTAs (each recomputes the
+  // row's norm): at few tokens this spreads the W_out reads over more SMs.
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int a = wid; a < d.d_a; a += nw) {
+  const int per = (d.d_a + gridDim.y - 1) / gridDim.y;
+  const int a0 = blockIdx.y * per, a1 = a0 + per < d.d_a ? a0 + per : d.d_a;
+  for (int a = a0 + wid; a < a1; a += nw) {
     const float* w = b.wout + (size_t)a * d.D;
     float acc = 0.f;
     for (int i = lane; i < d.D; i += 32) acc += row[i] * w[i];
@@ -450,8 +454,12 @@ __global__ void k_head_fused(ExpertDims d, StepBufs b, int step, float dt, const
   const float* bf = gf + d.D;
   for (int i = threadIdx.x; i < d.D; i += blockDim.x) row[i] = row[i] * r * (1.f + gf[i]) + bf[i];
   __syncthreads();
+  // The d_a outputs are split over gridDim.y CTAs (each recomputes the
+  // row's norm): at few tokens this spreads the W_out reads over more SMs.
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int a = wid; a < d.d_a; a += nw) {
+  const int per = (d.d_a + gridDim.y - 1) / gridDim.y;
+  const int a0 = blockIdx.y * per, a1 = a0 + per < d.d_a ? a0 + per : d.d_a;
+  for (int a = a0 + wid; a < a1; a += nw) {
     const float* w = b.wout + (size_t)a * d.D;
     float acc = 0.f;
     for (int i = lane; i < d.D; i += 32) acc += row[i] * w[i];
@@ -670,7 +678,9 @@ cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, 
   if (T >= kMultiTokens && (size_t)kHT * d.D * sizeof(float) <= 200 * 1024)
     return launch_pdl((const void*)k_head_multi, dim3((T + kHT - 1) / kHT), dim3(kThreads),
                       (size_t)kHT * d.D * sizeof(float), st, args);
-  return launch_pdl((const void*)k_head_fused, dim3(T), dim3(kThreads), (size_t)(d.D + 32) * sizeof(float), st, args);
+  const int split = d.d_a >= 32 ? 4 : 1;
+  return launch_pdl((const void*)k_head_fused, dim3(T, split), dim3(kThreads), (size_t)(d.D + 32) * sizeof(float), st,
+                    args);
 }
 
 cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st) {
