@@ -423,7 +423,7 @@ vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, con
   const bool stream_ok = dh == 64 || dh == 128 || dh == 256;
   ap->stream = stream_ok && ((fl & VLA_FLAG_ATTN_STREAM) ||
                              (!(fl & VLA_FLAG_ATTN_SPLIT) && B * nkv * aa.n_qt * 5 >= h->num_sms));
-  const uint32_t krows = ap->stream ? 64u : (uint32_t)aa.kc, ksrows = ap->stream ? 64u : (uint32_t)aa.kc_s;
+  const uint32_t krows = ap->stream ? 128u : (uint32_t)aa.kc, ksrows = ap->stream ? 128u : (uint32_t)aa.kc_s;
   if (tc_encode_2d_bf16(&ap->tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
       tc_encode_3d_bf16(&ap->tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64,
                         krows) ||
