@@ -11,8 +11,10 @@
 // One thread feeds the tensor cores one MMA instruction at a time, and an
 // instruction costs about the same to issue for any N up to 128, so a chunk
 // is 128 keys: S_j = Q K_j^T is d_h / 16 MMAs of N = 128.  Q lives in TMEM
-// (the S MMA's A operand), which leaves shared memory for two K chunks, one
-// V^T chunk and one P tile; TMEM holds O, Q and one S buffer.
+// (the S MMA's A operand); TMEM holds O, Q and one S buffer.  Shared memory
+// holds a ring of three chunk slots and one P tile: a slot receives K_j, and
+// once S_j is done, V_j^T in its place, so V_j streams in while the softmax
+// of chunk j runs, and K_{j+3} follows once P_j V_j is done.
 //
 // Warp roles (352 threads):
 //   warps 0-7  softmax and epilogue: warps w and w + 4 share the 32 query
@@ -20,10 +22,10 @@
 //              S_j and find the same maximum, then warp w exponentiates keys
 //              0..63 of the chunk (and owns the first half of O's columns),
 //              warp w + 4 keys 64..127 (the second half)
-//   warp 8     TMA producer of Q and of K_j (two-chunk ring)
+//   warp 8     TMA producer of Q and of K_j
 //   warp 9     MMA issuer: S_j into the TMEM S buffer, O += P_j V_j into the
 //              TMEM O accumulator
-//   warp 10    TMA producer of V_j^T (one chunk)
+//   warp 10    TMA producer of V_j^T
 // Per chunk j a softmax thread copies its half of its row of S_j into
 // registers while finding the row maximum over the whole chunk, then
 // releases the S buffer (the next chunk's S MMAs start while it works),
@@ -31,8 +33,8 @@
 // in bf16 to shared memory and adds it to the row sum l.  m is raised lazily:
 // only when a chunk maximum exceeds it by more than 2^8 in the exponent are O
 // (in TMEM) and l rescaled, so P never exceeds 256 and the final o = O / l is
-// unchanged in exact arithmetic.  The output tile is staged in the freed K
-// buffers and written with row-contiguous stores.
+// unchanged in exact arithmetic.  The output tile is staged in the freed
+// slots and written one bulk copy per row.
 #include "vla_common.cuh"
 
 namespace {
@@ -40,41 +42,43 @@ namespace {
 constexpr int KB = 128;              // keys per chunk
 constexpr float RESCALE_LOG2 = 8.f;  // lazy-rescale threshold (factor 256)
 
+constexpr int NSLOT = 3;              // chunk slots in the ring
+
 struct StreamSmem {
-  uint32_t k, v, p, bars, slot, total;
+  uint32_t kv, slot_bytes, p, bars, tslot, total;
 };
 
 // Byte offsets from the 1024-aligned base, every operand tile 128-byte
-// swizzled.  k: 2 chunks x nsub x [128 keys][64] (chunk buffer 1 first holds
-// Q, nsub x [128 rows][64], until Q is in TMEM); v: 2 x [d_h][64 keys] (V^T of
-// the chunk's two 64-key halves); p: 2 x [128][64 keys].
+// swizzled.  kv: NSLOT slots of d_h x 256 bytes, each holding either K_j
+// (nsub x [128 keys][64]) or V_j^T (2 x [d_h][64 keys], the chunk's two
+// 64-key halves); slot 2 first holds Q (nsub x [128 rows][64]) until Q is in
+// TMEM.  p: 2 x [128][64 keys].
 __host__ __device__ inline StreamSmem stream_layout(int d_h) {
-  const int nsub = d_h / 64;
   StreamSmem s;
-  s.k = 0;
-  s.v = s.k + 2u * (uint32_t)nsub * 16384u;
-  s.p = s.v + 2u * (uint32_t)d_h * 128u;
+  s.kv = 0;
+  s.slot_bytes = (uint32_t)d_h * 256u;
+  s.p = s.kv + NSLOT * s.slot_bytes;
   s.bars = s.p + 2u * 16384u;
-  s.slot = s.bars + 16 * 8;
-  s.total = s.slot + 16;
+  s.tslot = s.bars + 24 * 8;
+  s.total = s.tslot + 16;
   return s;
 }
 
 enum {
-  B_Q = 0,     // Q landed in K chunk buffer 1
+  B_Q = 0,     // Q landed in slot 2
   B_QT = 1,    // Q copied into TMEM (count NSM)
-  B_KF = 2,    // [2] K chunk buffer full
-  B_KE = 4,    // [2] K chunk buffer free (its S MMAs done)
-  B_VF = 6,    // V^T buffer full
-  B_VE = 7,    // V^T buffer free (P V done)
-  B_SF = 8,    // S ready (MMA commit)
-  B_SC = 9,    // S read by every softmax thread (count NSM)
-  B_PF = 10,   // P tile written (count NSM)
-  B_PV = 11,   // P V done (MMA commit)
-  B_FIN = 12,  // every MMA of the CTA complete
-  B_XL = 13,   // row-sum halves exchanged (count NSM)
-  B_ST = 14,   // output tile staged (count NSM)
-  N_BARS = 15
+  B_FK = 2,    // [NSLOT] K_j landed in its slot
+  B_FV = 5,    // [NSLOT] V_j^T landed in its slot
+  B_ES = 8,    // [NSLOT] S_j done: the slot may take V_j^T
+  B_EP = 11,   // [NSLOT] P_j V_j done: the slot is free
+  B_SF = 14,   // S ready (MMA commit)
+  B_SC = 15,   // S read by every softmax thread (count NSM)
+  B_PF = 16,   // P tile written (count NSM)
+  B_PV = 17,   // P V done (MMA commit)
+  B_FIN = 18,  // every MMA of the CTA complete
+  B_XL = 19,   // row-sum halves exchanged (count NSM)
+  B_ST = 20,   // output tile staged (count NSM)
+  N_BARS = 21
 };
 constexpr int NSM = 256;  // softmax threads
 
@@ -167,12 +171,12 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int dh = a.d_h, nsub = dh / 64;
   const StreamSmem L = stream_layout(dh);
-  uint8_t* Ks = smem + L.k;
-  uint8_t* Qs = Ks + (size_t)nsub * 16384;  // K chunk buffer 1 holds Q first
-  uint8_t* Vs = smem + L.v;
+  uint8_t* KV = smem + L.kv;
+  const uint32_t SB = L.slot_bytes;
+  uint8_t* Qs = KV + 2 * (size_t)SB;  // slot 2 holds Q first
   uint8_t* Ps = smem + L.p;
   uint64_t* bars = (uint64_t*)(smem + L.bars);
-  uint32_t* tmem_slot = (uint32_t*)(smem + L.slot);
+  uint32_t* tmem_slot = (uint32_t*)(smem + L.tslot);
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,12 +193,12 @@ __global__ void __launch_bounds__(352, 1)
     s_fail = 0;
     mbar_init(&bars[B_Q], 1);
     mbar_init(&bars[B_QT], NSM);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_KF + i], 1);
-      mbar_init(&bars[B_KE + i], 1);
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&bars[B_FK + i], 1);
+      mbar_init(&bars[B_FV + i], 1);
+      mbar_init(&bars[B_ES + i], 1);
+      mbar_init(&bars[B_EP + i], 1);
     }
-    mbar_init(&bars[B_VF], 1);
-    mbar_init(&bars[B_VE], 1);
     mbar_init(&bars[B_SF], 1);
     mbar_init(&bars[B_SC], NSM);
     mbar_init(&bars[B_PF], NSM);
@@ -224,37 +228,40 @@ __global__ void __launch_bounds__(352, 1)
       auto issue = [&](int j) {
         const bool pre = j < n_pre;
         const int k0 = pre ? j * KB : (j - n_pre) * KB;
+        const int sl = j % NSLOT;
+        uint8_t* dst = KV + (size_t)sl * SB;
         if (kp) {
-          uint64_t* fb = &bars[B_KF + (j & 1)];
-          mbar_arrive_expect_tx(fb, (uint32_t)nsub * 16384u);
-          uint8_t* kd = Ks + (size_t)(j & 1) * nsub * 16384;
-          for (int s = 0; s < nsub; ++s)
-            tma_load_3d_s(kd + (size_t)s * 16384, pre ? &tmK : &tmKs, fb, s * 64, k0, pre ? zc : zs);
+          uint64_t* fb = &bars[B_FK + sl];
+          mbar_arrive_expect_tx(fb, SB);
+          for (int t = 0; t < nsub; ++t)
+            tma_load_3d_s(dst + (size_t)t * 16384, pre ? &tmK : &tmKs, fb, t * 64, k0, pre ? zc : zs);
         } else {
-          uint64_t* fb = &bars[B_VF];
-          mbar_arrive_expect_tx(fb, 2u * (uint32_t)dh * 128u);
+          uint64_t* fb = &bars[B_FV + sl];
+          mbar_arrive_expect_tx(fb, SB);
           for (int hh = 0; hh < 2; ++hh)
-            tma_load_3d_s(Vs + (size_t)hh * dh * 128, pre ? &tmVt : &tmVs, fb, k0 + hh * 64, 0, pre ? zc : zs);
+            tma_load_3d_s(dst + (size_t)hh * dh * 128, pre ? &tmVt : &tmVs, fb, k0 + hh * 64, 0, pre ? zc : zs);
         }
       };
       // The cached prefix does not depend on the previous kernel: its first
-      // chunk is in flight before the grid dependency wait.
+      // two K chunks are in flight before the grid dependency wait.
       int j = 0;
-      if (n_pre > 0) issue(j++);
+      if (kp)
+        for (; j < 2 && j < n_pre; ++j) issue(j);
       griddep_wait();
       if (kp) {
         mbar_arrive_expect_tx(&bars[B_Q], (uint32_t)nsub * 16384u);
         const int qrow = (b * a.n_q + gk * a.group) * a.H + qt * 128;
-        for (int s = 0; s < nsub; ++s) tma_load_2d(Qs + (size_t)s * 16384, &tmQ, &bars[B_Q], s * 64, qrow);
+        for (int t = 0; t < nsub; ++t) tma_load_2d(Qs + (size_t)t * 16384, &tmQ, &bars[B_Q], t * 64, qrow);
       }
       for (; j < nch; ++j) {
+        const int sl = j % NSLOT;
         bool w = true;
         if (kp) {
-          // Buffer j & 1 is free once S_{j-2} is done; buffer 1 first holds Q.
-          if (j == 1) w = mbar_wait(&bars[B_QT], 0, a.status);
-          else if (j >= 2) w = mbar_wait(&bars[B_KE + (j & 1)], (uint32_t)((j - 2) >> 1) & 1u, a.status);
-        } else if (j >= 1) {
-          w = mbar_wait(&bars[B_VE], (uint32_t)(j - 1) & 1u, a.status);  // P_{j-1} V_{j-1} done
+          // K_j: slot 2 first holds Q; later a slot is free once P_{j-3} V_{j-3} is done.
+          if (j == 2) w = mbar_wait(&bars[B_QT], 0, a.status);
+          else if (j >= NSLOT) w = mbar_wait(&bars[B_EP + sl], (uint32_t)(j / NSLOT - 1) & 1u, a.status);
+        } else {
+          w = mbar_wait(&bars[B_ES + sl], (uint32_t)(j / NSLOT) & 1u, a.status);  // V_j^T replaces K_j
         }
         if (!w) {
           s_fail = 1;
@@ -262,13 +269,11 @@ __global__ void __launch_bounds__(352, 1)
         }
         issue(j);
       }
-      // Own copies land before the CTA can exit (normally already consumed).
-      if (kp) {
-        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&bars[B_KF + (i & 1)], (uint32_t)(i >> 1) & 1u);
-        mbar_drain(&bars[B_Q], 0);
-      } else if (j > 0) {
-        mbar_drain(&bars[B_VF], (uint32_t)(j - 1) & 1u);
-      }
+      // Own copies land before the CTA can exit (normally already consumed):
+      // the last use of each slot.
+      for (int i = j - NSLOT < 0 ? 0 : j - NSLOT; i < j; ++i)
+        mbar_drain(&bars[(kp ? B_FK : B_FV) + i % NSLOT], (uint32_t)(i / NSLOT) & 1u);
+      if (kp) mbar_drain(&bars[B_Q], 0);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -279,10 +284,11 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t idesc_o = idesc_bf16_f32(128, dh);
       bool ok = mbar_wait(&bars[B_QT], 0, a.status);
       auto pv = [&](int i) -> bool {
+        const int sl = i % NSLOT;
         if (!mbar_wait(&bars[B_PF], (uint32_t)i & 1u, a.status)) return false;
-        if (!mbar_wait(&bars[B_VF], (uint32_t)i & 1u, a.status)) return false;
+        if (!mbar_wait(&bars[B_FV + sl], (uint32_t)(i / NSLOT) & 1u, a.status)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(Ps), va = smem_u32(Vs);
+        const uint32_t pa = smem_u32(Ps), va = smem_u32(KV + (size_t)sl * SB);
 #pragma unroll
         for (int kk = 0; kk < KB / 16; ++kk) {
           const uint32_t hp = (uint32_t)(kk >> 2), ko = (uint32_t)(kk & 3) * 32u;
@@ -290,18 +296,18 @@ __global__ void __launch_bounds__(352, 1)
                     (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_PV]);
-        umma_commit(&bars[B_VE]);
+        umma_commit(&bars[B_EP + sl]);
         return true;
       };
       for (int j = 0; ok && j < nch; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&bars[B_KF + st], (uint32_t)(j >> 1) & 1u, a.status) ||
+        const int sl = j % NSLOT;
+        if (!mbar_wait(&bars[B_FK + sl], (uint32_t)(j / NSLOT) & 1u, a.status) ||
             (j >= 1 && !mbar_wait(&bars[B_SC], (uint32_t)(j - 1) & 1u, a.status))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t ka = smem_u32(Ks + (size_t)st * nsub * 16384);
+        const uint32_t ka = smem_u32(KV + (size_t)sl * SB);
         for (int s = 0; s < nsub; ++s) {
           const uint32_t kb = ka + (uint32_t)s * 16384u;
 #pragma unroll
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(352, 1)
                          (s > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_SF]);
-        umma_commit(&bars[B_KE + st]);
+        umma_commit(&bars[B_ES + sl]);
         if (j >= 1 && !pv(j - 1)) ok = false;
       }
       if (ok) ok = pv(nch - 1);
@@ -446,7 +452,7 @@ __global__ void __launch_bounds__(352, 1)
     if (!ok) s_fail = 1;
     // Epilogue: o = O / l with l the sum of the pair's partial sums.  Each
     // thread stages its half of the row (scaled, in the output type) in the
-    // K and V buffers, which every MMA and copy has finished with: rows of
+    // chunk slots, which every MMA and copy has finished with: rows of
     // d_h elements, 16 bytes apart beyond their length so that the 32 rows of
     // a warp's store fall in different banks.  Each row is then one bulk copy
     // to its place in o, issued by the thread that owns the row.  All waits
@@ -455,8 +461,8 @@ __global__ void __launch_bounds__(352, 1)
         ok && __all_sync(~0u, mbar_wait(&bars[B_PV], (uint32_t)(nch - 1) & 1u, a.status));
     constexpr int ES = O32 ? 4 : 2;     // output element size
     const int RB = dh * ES;             // bytes per output row
-    const int RP = RB + 16;             // staged row pitch (128 rows fit in the K and V buffers)
-    const uint32_t stage = smem_u32(Ks);
+    const int RP = RB + 16;             // staged row pitch (128 rows fit in the slots)
+    const uint32_t stage = smem_u32(KV);
     float* xl = (float*)Ps;  // [2][128] partial row sums (the P tile is free now)
     xl[half * 128 + row] = l;
     mbar_arrive(&bars[B_XL]);
@@ -504,7 +510,7 @@ __global__ void __launch_bounds__(352, 1)
       uint8_t* orow = (O32 ? (uint8_t*)a.o32 : (uint8_t*)a.o) +
                       (((size_t)b * a.H + i) * (size_t)(a.n_q * dh) + (size_t)(gk * a.group + jj) * dh) * ES;
       bulk_store_s2g(orow, rbase, (uint32_t)RB);
-      bulk_commit_wait_all();
+      bulk_commit_wait_read();
     }
   }
 

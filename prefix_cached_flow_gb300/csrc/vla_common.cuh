@@ -171,10 +171,11 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
                : "memory");
 }
-// Commit the thread's bulk copies and wait until their writes are complete.
-__device__ __forceinline__ void bulk_commit_wait_all() {
+// Commit the thread's bulk copies and wait until they have read their shared
+// memory source (the writes to global memory complete with the grid).
+__device__ __forceinline__ void bulk_commit_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
