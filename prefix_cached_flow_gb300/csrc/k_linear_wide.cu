@@ -225,10 +225,39 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) hb[j] = j < nvv ? hq[(size_t)j * g.D] : 0.f;
       };
-      if (EPI == EPI_RESID) load_h(half * hbn, hcur);
+      if (EPI == EPI_RESID) {
+        // The whole tile's residual rows go to L2 while the MMAs run; the
+        // first chunk is loaded into registers.
+        const float* hq = g.h + (size_t)(t0 + half * hbn) * g.D + n;
+        const int nh = tcols - half * hbn;
+        for (int j = 0; j < hbn && j < nh; ++j) prefetch_l2(hq + (size_t)j * g.D);
+        load_h(half * hbn, hcur);
+      }
       const bool okw = __all_sync(0xffffffffu, mbar_wait(&accf[buf], (lt >> 1) & 1, g.status));
       tc_fence_after();
       if (EPI == EPI_QKV) slot = n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2);
+      // The warp's 32 output rows are consecutive features inside one head
+      // of one of q, k, v (EPI_QKV) or of one layer's K or V (EPI_KV).
+      const int nb = m0 + quarter * 32;  // the warp's first output row
+      int kl = 0, kwhich = 0, khd = 0, ke0 = 0;
+      if (EPI == EPI_KV) {
+        kl = nb / (2 * g.kvdim);
+        const int rem = nb - kl * 2 * g.kvdim;
+        kwhich = rem / g.kvdim;
+        const int r2 = rem - kwhich * g.kvdim;
+        khd = r2 / g.d_h;
+        ke0 = r2 - khd * g.d_h;
+      }
+      int qhd = 0, qd0 = 0;
+      if (EPI == EPI_QKV) {
+        const int rr = slot == 0 ? nb : (slot == 1 ? nb - g.qdim : nb - g.qdim - g.kvdim);
+        qhd = rr / g.d_h;
+        qd0 = rr - qhd * g.d_h;
+      }
+      // Token-major stores: lane l writes token (l >> 2) + 8 * pass of each
+      // 32-token chunk; tdiv = H (EPI_QKV) or P (EPI_KV) splits a token
+      // index into (observation, position) without a division per store.
+      const int tdiv = EPI == EPI_KV ? g.kv_P : g.H;
       float* wq = wss + ((size_t)(buf * 2 + half) * 4 + quarter) * hbn;  // this warp's column sums
       for (int c0 = half * hbn; c0 < (half + 1) * hbn; c0 += 32) {
         uint32_t r[32];
@@ -265,17 +294,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           // memory, then write whole rows.  The warp's 32 output rows are
           // consecutive features inside one head of one of q, k, v.
           bf16* stg = stg_all + (size_t)(warp - 2) * kStg;
-          const int nb = m0 + quarter * 32;  // the warp's first output row
-          // EPI_KV: rows [L][K|V][n_kv][d_h]; the warp's 32 rows share (l, K|V, head)
-          int kl = 0, kwhich = 0, khd = 0, ke0 = 0;
-          if (EPI == EPI_KV) {
-            kl = nb / (2 * g.kvdim);
-            const int rem = nb - kl * 2 * g.kvdim;
-            kwhich = rem / g.kvdim;
-            const int r2 = rem - kwhich * g.kvdim;
-            khd = r2 / g.d_h;
-            ke0 = r2 - khd * g.d_h;
-          }
           const bool vt = (EPI == EPI_QKV && slot == 2) || (EPI == EPI_KV && kwhich == 1);
           __syncwarp();
           if (!vt) {
@@ -286,26 +304,35 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               stg[j * 32 + lane] = __float2bfloat16_rn(EPI == EPI_GELU ? gelu_as7126(y) : y);
             }
             __syncwarp();
+            const int part = lane & 3;
+            int tb = 0, ti = 0;  // (observation, position) of token t0 + c0 + (lane >> 2)
+            if (EPI != EPI_GELU) {
+              const int t = t0 + c0 + (lane >> 2);
+              tb = t / tdiv;
+              ti = t - tb * tdiv;
+            }
 #pragma unroll
             for (int pass = 0; pass < 4; ++pass) {  // 8 tokens per pass, 4 lanes x 16 bytes per token
-              const int j = pass * 8 + (lane >> 2), part = lane & 3;
+              const int j = pass * 8 + (lane >> 2);
               if (j < nv) {
                 const uint4 v = *(const uint4*)(stg + j * 32 + part * 8);
-                const int t = t0 + c0 + j;
                 bf16* dst;
                 if (EPI == EPI_GELU) {
-                  dst = g.g + (size_t)t * g.ldg + nb;
+                  dst = g.g + (size_t)(t0 + c0 + j) * g.ldg + nb;
                 } else if (EPI == EPI_KV) {
-                  const int b = t / g.kv_P, pp = t - b * g.kv_P;
-                  dst = g.kc_out + ((((size_t)kl * g.kv_B + b) * g.n_kv + khd) * g.kv_P + pp) * g.d_h + ke0;
+                  dst = g.kc_out + ((((size_t)kl * g.kv_B + tb) * g.n_kv + khd) * g.kv_P + ti) * g.d_h + ke0;
                 } else {
-                  const int b = t / g.H, i = t - b * g.H;
-                  const int rr = slot == 0 ? nb : nb - g.qdim;
-                  const int hd = rr / g.d_h, d0 = rr - hd * g.d_h;
-                  dst = slot == 0 ? g.q + (((size_t)b * g.n_q + hd) * g.H + i) * g.d_h + d0
-                                  : g.ks + (((size_t)b * g.n_kv + hd) * g.H + i) * g.d_h + d0;
+                  dst = slot == 0 ? g.q + (((size_t)tb * g.n_q + qhd) * g.H + ti) * g.d_h + qd0
+                                  : g.ks + (((size_t)tb * g.n_kv + qhd) * g.H + ti) * g.d_h + qd0;
                 }
                 *(uint4*)(dst + part * 8) = v;
+              }
+              if (EPI != EPI_GELU) {
+                ti += 8;
+                while (ti >= tdiv) {
+                  ti -= tdiv;
+                  ++tb;
+                }
               }
             }
           } else {
@@ -323,10 +350,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               col = g.vc_out + ((((size_t)kl * g.kv_B + b) * g.n_kv + khd) * g.d_h + ke0) * g.kv_P8 + pp;
               pitch = (size_t)g.kv_P8;
             } else {
-              const int rr0 = nb - g.qdim - g.kvdim;
-              const int hd = rr0 / g.d_h, d0 = rr0 - hd * g.d_h;
               const int b = t / g.H, i = t - b * g.H;
-              col = g.vst + (((size_t)b * g.n_kv + hd) * g.d_h + d0) * g.Hp + i;
+              col = g.vst + (((size_t)b * g.n_kv + qhd) * g.d_h + qd0) * g.Hp + i;
               pitch = (size_t)g.Hp;
             }
             if (lane < nv) {
