@@ -564,6 +564,126 @@ __global__ void k_quant_rows(int K, const float* x, bf16* codes, float* alpha) {
   if (threadIdx.x == 0) alpha[t] = al;
 }
 
+// The same three row operations with the row held in registers: one CTA per
+// row of K floats (K % 4 == 0), thread i owns the float4 columns i,
+// i + blockDim.x, ... (RV of them), and every load of the row (and of gamma,
+// beta) is issued before any of them is used, so a row costs one memory
+// round trip.  RV = 1 (more threads per row) when there are few rows.
+template <int RV>
+__device__ __forceinline__ void load_row4(const float* p, int nc, float4 (&v)[RV]) {
+  const float4* p4 = (const float4*)p;
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    v[k] = c < nc ? p4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// u = v * r * (1 + gamma) + beta, elementwise (the expression of the
+// shared-memory kernels above).
+__device__ __forceinline__ float4 modulate4(float4 v, float r, float4 g, float4 b) {
+  return make_float4(v.x * r * (1.f + g.x) + b.x, v.y * r * (1.f + g.y) + b.y, v.z * r * (1.f + g.z) + b.z,
+                     v.w * r * (1.f + g.w) + b.w);
+}
+
+// Eq. (4) codes of four values (exact integers carried in bf16), packed.
+__device__ __forceinline__ uint2 codes4(float4 u, float al) {
+  auto q = [&](float x) { return fminf(fmaxf(rintf(__fdiv_rn(x, al)), -128.f), 127.f); };
+  return make_uint2(pack_bf16x2(q(u.x), q(u.y)), pack_bf16x2(q(u.z), q(u.w)));
+}
+
+__device__ __forceinline__ float absmax4(float4 u) { return fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))); }
+
+template <int RV>
+__global__ void k_modnorm_v(int T, int D, float eps, const float* h, const float* ss, int n_ss, const float* gamma,
+                            const float* beta, bf16* u) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int t = blockIdx.x, nc = D >> 2;
+  float4 v[RV], g[RV], b[RV];
+  load_row4(h + (size_t)t * D, nc, v);
+  load_row4(gamma, nc, g);
+  load_row4(beta, nc, b);
+  float s = 0.f;
+  for (int k = 0; k < n_ss; ++k) s += ss[(size_t)k * T + t];
+  const float r = rsqrtf(s / (float)D + eps);
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    if (c < nc) {
+      const float4 m = modulate4(v[k], r, g[k], b[k]);
+      *(uint2*)(u + (size_t)t * D + 4 * c) = make_uint2(pack_bf16x2(m.x, m.y), pack_bf16x2(m.z, m.w));
+    }
+  }
+}
+
+// Eq. (4) on the modulated RMSNorm of h (the row's own sum of squares).
+template <int RV>
+__global__ void k_quant_norm_v(int D, float eps, const float* h, const float* gamma, const float* beta, bf16* codes,
+                               float* alpha) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  __shared__ float red[32];
+  const int t = blockIdx.x, nc = D >> 2;
+  float4 v[RV], g[RV], b[RV];
+  load_row4(h + (size_t)t * D, nc, v);
+  load_row4(gamma, nc, g);
+  load_row4(beta, nc, b);
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < RV; ++k) s += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+  s = block_sum(s, red);
+  const float r = rsqrtf(s / (float)D + eps);
+  float am = 0.f;
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    v[k] = modulate4(v[k], r, g[k], b[k]);
+    if (threadIdx.x + k * blockDim.x < nc) am = fmaxf(am, absmax4(v[k]));
+  }
+  am = block_max(am, red);
+  const float al = __fdiv_rn(fmaxf(am, 1e-5f), 127.0f);
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    if (c < nc) *(uint2*)(codes + (size_t)t * D + 4 * c) = codes4(v[k], al);
+  }
+  if (threadIdx.x == 0) alpha[t] = al;
+}
+
+// Eq. (4) on fp32 rows x [T][K].
+template <int RV>
+__global__ void k_quant_rows_v(int K, const float* x, bf16* codes, float* alpha) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  __shared__ float red[32];
+  const int t = blockIdx.x, nc = K >> 2;
+  float4 v[RV];
+  load_row4(x + (size_t)t * K, nc, v);
+  float am = 0.f;
+#pragma unroll
+  for (int k = 0; k < RV; ++k) am = fmaxf(am, absmax4(v[k]));  // padding lanes hold zeros
+  am = block_max(am, red);
+  const float al = __fdiv_rn(fmaxf(am, 1e-5f), 127.0f);
+#pragma unroll
+  for (int k = 0; k < RV; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    if (c < nc) *(uint2*)(codes + (size_t)t * K + 4 * c) = codes4(v[k], al);
+  }
+  if (threadIdx.x == 0) alpha[t] = al;
+}
+
+// Threads for a register-held row of K floats with RV float4 per thread,
+// or 0 when the row does not fit.
+int row_threads(int K, int RV) {
+  if (K < 4 || K % 4 != 0) return 0;
+  const int nc = K / 4;
+  int th = (nc + RV - 1) / RV;
+  th = (th + 31) / 32 * 32;
+  return th <= 1024 ? th : 0;
+}
+// Few rows (a small batch): one float4 per thread where the row fits.
+int row_vec(int rows, int K) { return rows < 256 && row_threads(K, 1) ? 1 : 2; }
+
 __global__ void k_i8_to_bf16(const int8_t* a, bf16* out, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     out[i] = __float2bfloat16_rn((float)a[i]);
@@ -647,6 +767,8 @@ cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss,
   int T = d.B * d.H, D = d.D;
   float eps = d.eps;
   void* args[] = {&T, &D, &eps, (void*)&h, (void*)&ss, &n_ss, (void*)&gamma, (void*)&beta, &u};
+  const int rv = row_vec(T, D), th = row_threads(D, rv);
+  if (th) return launch_pdl(rv == 1 ? (const void*)k_modnorm_v<1> : (const void*)k_modnorm_v<2>, dim3(T), dim3(th), 0, st, args);
   return launch_pdl((const void*)k_modnorm, dim3(T), dim3(kThreads), 0, st, args);
 }
 
@@ -655,11 +777,19 @@ cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* 
   int D = d.D;
   float eps = d.eps;
   void* args[] = {&D, &eps, (void*)&h, (void*)&gamma, (void*)&beta, &codes, &alpha};
+  const int rv = row_vec(d.B * d.H, D), th = row_threads(D, rv);
+  if (th)
+    return launch_pdl(rv == 1 ? (const void*)k_quant_norm_v<1> : (const void*)k_quant_norm_v<2>, dim3(d.B * d.H),
+                      dim3(th), 0, st, args);
   return launch_pdl((const void*)k_quant_norm, dim3(d.B * d.H), dim3(512), (size_t)(D + 32) * sizeof(float), st, args);
 }
 
 cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st) {
   void* args[] = {&K, (void*)&x, &codes, &alpha};
+  const int rv = row_vec(T, K), th = row_threads(K, rv);
+  if (th)
+    return launch_pdl(rv == 1 ? (const void*)k_quant_rows_v<1> : (const void*)k_quant_rows_v<2>, dim3(T), dim3(th), 0,
+                      st, args);
   return launch_pdl((const void*)k_quant_rows, dim3(T), dim3(512), (size_t)(K + 32) * sizeof(float), st, args);
 }
 
