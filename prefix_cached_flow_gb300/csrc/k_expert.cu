@@ -604,8 +604,10 @@ __global__ void k_modnorm_v(int T, int D, float eps, const float* h, const float
   load_row4(h + (size_t)t * D, nc, v);
   load_row4(gamma, nc, g);
   load_row4(beta, nc, b);
+  __shared__ float red[32];
   float s = 0.f;
-  for (int k = 0; k < n_ss; ++k) s += ss[(size_t)k * T + t];
+  for (int k = threadIdx.x; k < n_ss; k += blockDim.x) s += ss[(size_t)k * T + t];
+  s = block_sum(s, red);
   const float r = rsqrtf(s / (float)D + eps);
 #pragma unroll
   for (int k = 0; k < RV; ++k) {

@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
-    if (EPI == EPI_RESID) {
+    if (EPI == EPI_RESID && g.ss_out) {
       __syncthreads();
       for (int col = threadIdx.x; col < tcols; col += 128)
         g.ss_out[(size_t)blockIdx.x * g.T + t0 + col] =
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(128, 1)
     epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false);
   }
   VLA_TL(g.tl, 0, 11);
-  if (EPI == EPI_RESID) {
+  if (EPI == EPI_RESID && g.ss_out) {
     // Rank 0 combines the ranks' per-token sums of squares (fixed order).
     __syncthreads();
     float* myss = g.xss + ((size_t)tile * C + rank) * BN;

@@ -572,7 +572,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       VLA_CK(launch_quant_rows(T, Q, h->f32buf, act, h->alpha, st));
       a = lin_args(h, po, D, T, l);
       a.tl = tls(2);
-      a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.beta_slot = 3;
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_slot = 3;  // the quantiser reads h itself
       VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
       VLA_CK(launch_quant_norm(d, h->h, mod + 2 * D, mod + 3 * D, act, h->alpha, st));
       a = lin_args(h, pu, F, T, l);
@@ -582,7 +582,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       VLA_CK(launch_quant_rows(T, F, h->f32buf, act, h->alpha, st));
       a = lin_args(h, pd, D, T, l);
       a.tl = tls(4);
-      a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.beta_slot = 5;
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_slot = 5;
       VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
     }
     VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));

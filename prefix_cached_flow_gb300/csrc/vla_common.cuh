@@ -561,7 +561,7 @@ struct LinArgs {
   int D;               // width of h (row pitch of h / h_in)
   // EPI_RESID
   float* h;            // [T][D]
-  float* ss_out;       // [tiles_n][T]: sums of squares of each 128-row block
+  float* ss_out;       // [tiles_n][T]: sums of squares of each 128-row block (nullptr: not needed)
   // EPI_GELU
   bf16* g;
   int ldg;
