@@ -171,8 +171,16 @@ __global__ void __launch_bounds__(128, 1)
       tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
       tmem_wait16(r);
       tmem_wait16(r + 16);
+      if (c0 + 32 <= nk) {  // a full piece (uniform over the CTA): three-input max, no masks
 #pragma unroll
-      for (int u = 0; u < 32; ++u) mxv[u & 3] = fmaxf(mxv[u & 3], c0 + u < nk ? __uint_as_float(r[u]) : -INFINITY);
+        for (int u = 0; u < 32; u += 2) {
+          float& mm = mxv[(u >> 1) & 3];
+          asm("max.f32 %0, %0, %1, %2;" : "+f"(mm) : "f"(__uint_as_float(r[u])), "f"(__uint_as_float(r[u + 1])));
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) mxv[u & 3] = fmaxf(mxv[u & 3], c0 + u < nk ? __uint_as_float(r[u]) : -INFINITY);
+      }
     }
     m = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])) * a.scale_log2;  // the scale is positive
     VLA_TL(a.tl, 0, 11);
@@ -193,7 +201,7 @@ __global__ void __launch_bounds__(128, 1)
         for (int u = 0; u < 8; ++u) {
           const int j = c0 + q * 8 + u;
           p[u] = fast_exp2(fmaf(__uint_as_float(r[q * 8 + u]), a.scale_log2, nm));
-          p[u] = j < nk ? p[u] : 0.f;
+          if (c0 + 32 > nk) p[u] = j < nk ? p[u] : 0.f;  // only the last, partial piece is masked
           lv[u & 3] += p[u];
         }
         uint4 pk;

@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(128, 1)
     VLA_TL(g.tl, 32, 9);
     const uint32_t bb = smem_u32(Bbase) + (uint32_t)(kc >> 3) * b_tile;
     const float* hcol = Hs + (size_t)(kc >> 3) * BN * 64 + (kc & 7) * 8;
-#pragma unroll 2
+#pragma unroll 4
     for (int t = tid / kcs; t < BN; t += tstep) {
       const int tt = t0 + t;
       uint4 pk = make_uint4(0u, 0u, 0u, 0u);
