@@ -64,18 +64,49 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) 
   return v[0];
 }
 
+// fp32 pairs: pack, unpack, multiply, fused multiply-add.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 // GeLU x * Phi(x) with erf by Abramowitz & Stegun, Handbook of Mathematical
 // Functions, formula 7.1.26 (|error of erf| <= 1.5e-7, far below the bf16
 // rounding of the output): erf(z) ~ 1 - t (a1 + a2 t + ... + a5 t^4) e^(-z^2),
 // t = 1 / (1 + p z), z >= 0, odd extension for negative arguments.
-__device__ __forceinline__ float gelu_as7126(float x) {
-  const float z = fabsf(x) * 0.70710678118654752f;
-  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
-  const float poly =
-      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
-  const float tail = poly * fast_exp2(-z * z * 1.4426950408889634f);  // 1 - erf(z)
-  const float erfv = copysignf(1.f - tail, x);
-  return 0.5f * x * (1.f + erfv);
+// Evaluated for two values at once: the FMA-pipe arithmetic on fp32 pairs
+// (the reciprocal and the exponential stay per element), and the final
+// product as h + h * erf with h = x / 2.
+__device__ __forceinline__ void gelu_as7126_x2(float x0, float x1, float& g0, float& g1) {
+  const uint64_t z = mul2(pk2(fabsf(x0), fabsf(x1)), pk2(0.70710678118654752f, 0.70710678118654752f));
+  float d0, d1;
+  up2(fma2(pk2(0.3275911f, 0.3275911f), z, pk2(1.f, 1.f)), d0, d1);
+  const uint64_t t = pk2(__fdividef(1.f, d0), __fdividef(1.f, d1));
+  uint64_t q = fma2(t, pk2(1.061405429f, 1.061405429f), pk2(-1.453152027f, -1.453152027f));
+  q = fma2(t, q, pk2(1.421413741f, 1.421413741f));
+  q = fma2(t, q, pk2(-0.284496736f, -0.284496736f));
+  q = fma2(t, q, pk2(0.254829592f, 0.254829592f));
+  q = mul2(t, q);
+  float e0, e1;
+  up2(mul2(mul2(z, z), pk2(-1.4426950408889634f, -1.4426950408889634f)), e0, e1);
+  float tl0, tl1;
+  up2(mul2(q, pk2(fast_exp2(e0), fast_exp2(e1))), tl0, tl1);  // 1 - erf(z)
+  const uint64_t erfv = pk2(copysignf(1.f - tl0, x0), copysignf(1.f - tl1, x1));
+  const uint64_t h = mul2(pk2(x0, x1), pk2(0.5f, 0.5f));
+  up2(fma2(h, erfv, h), g0, g1);
 }
 
 template <int EPI>
@@ -299,9 +330,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (!vt) {
             // token-major outputs (g, q, k): [col][row] so a token's 32 features are 64 contiguous bytes
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float y = __uint_as_float(r[j]);
-              stg[j * 32 + lane] = __float2bfloat16_rn(EPI == EPI_GELU ? gelu_as7126(y) : y);
+            for (int j = 0; j < 32; j += 2) {
+              float y0 = __uint_as_float(r[j]), y1 = __uint_as_float(r[j + 1]);
+              if (EPI == EPI_GELU) gelu_as7126_x2(y0, y1, y0, y1);
+              stg[j * 32 + lane] = __float2bfloat16_rn(y0);
+              stg[(j + 1) * 32 + lane] = __float2bfloat16_rn(y1);
             }
             __syncwarp();
             const int part = lane & 3;
