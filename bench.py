@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -115,11 +116,17 @@ class ClockSampler:
 
 
 def _lib_hash() -> str:
+    """Hash of the library's CUDA/C++ sources with comments and blank lines
+    removed: a change to a kernel changes it, a change to a comment does not."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "prefix_cached_flow_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.split("\n")]
+        h.update(f.encode() + b"\0" + "\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -622,9 +622,9 @@ cudaError_t attn_kernels_init();
 cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
                            const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st);
 // Streaming joint attention (k_attn_stream.cu): one CTA per 128-row query
-// tile streams every key in 64-key chunks (no cross-CTA merge).  Uses the
+// tile streams every key in 128-key chunks (no cross-CTA merge).  Uses the
 // AttnArgs fields B, P, H, n_q, n_kv, d_h, group, layer, n_qt, scale_log2, o,
-// o32, status.  tmK and tmKs have 64-row boxes; tmQ, tmVt, tmVs as above.
+// o32, status.  tmK and tmKs have 128-row boxes; tmQ, tmVt, tmVs as above.
 size_t attn_stream_smem_bytes(int d_h);
 cudaError_t attn_stream_init();
 cudaError_t launch_attn_stream(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
