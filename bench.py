@@ -63,6 +63,27 @@ def _dist():
     return ws, rank, local
 
 
+def replica_seed(seed: int, rank: int) -> int:
+    """Seed of a replica's observations: every rank solves its own inputs."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(dist, values, device):
+    """Element-wise max of a list of floats over all ranks (the slowest rank
+    sets the job's time); the values themselves without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world_size: int, units_per_rank: int, ms: float) -> float:
+    """Units every rank processed per second of the slowest rank's time."""
+    return world_size * units_per_rank / (ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -291,7 +312,7 @@ def run_ours(args):
     cfg = CONFIGS[args.workload]
     B = cfg.B
     w = make_weights(cfg)
-    Z, noise = make_observations(cfg.replace(seed=cfg.seed + 1000 * rank), B)
+    Z, noise = make_observations(cfg.replace(seed=replica_seed(cfg.seed, rank)), B)
     ex = V.Expert(cfg, V.upload_weights(w, cfg.dtype, cfg.w2a8), max_batch=B, max_prefix=cfg.P)
     dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
     Zt = torch.from_numpy(Z).to(dt).cuda()
@@ -333,10 +354,7 @@ def run_ours(args):
     prefix_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     denoise_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     step_ms = prefix_ms + denoise_ms
-    if dist:
-        t = torch.tensor([step_ms, prefix_ms, denoise_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, prefix_ms, denoise_ms = t.tolist()
+    step_ms, prefix_ms, denoise_ms = max_over_ranks(dist, [step_ms, prefix_ms, denoise_ms], "cuda")
 
     # End to end through the public host-buffer call: H2D of Z and noise, the
     # whole request, D2H of the chunk, every step.
@@ -353,10 +371,7 @@ def run_ours(args):
         ex.policy_step_host(Zh, nh, ah)
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    (e2e_ms,) = max_over_ranks(dist, [e2e_ms], "cuda")
 
     hbm, tflops, tflops_sus, src = _peaks()
     solver_bytes = cfg.S * algorithmic_bytes_per_step(cfg)
@@ -376,7 +391,7 @@ def run_ours(args):
     launches = args.steps * (1 + ex.launch_count(B, cfg.P))
     line = {
         "metric": METRIC,
-        "value": ws * B / (step_ms * 1e-3),
+        "value": whole_job_rate(ws, B, step_ms),
         "unit": "chunks/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -396,7 +411,7 @@ def run_ours(args):
         "denoise_ms": denoise_ms,
         "us_per_solver_step": denoise_ms * 1e3 / cfg.S,
         "roofline": roof,
-        "e2e": {"value": ws * B / (e2e_ms * 1e-3), "unit": "chunks/s",
+        "e2e": {"value": whole_job_rate(ws, B, e2e_ms), "unit": "chunks/s",
                 "h2d_bytes_per_step": int(Zh.numel() * Zh.element_size() + nh.numel() * 4),
                 "d2h_bytes_per_step": int(ah.numel() * 4)},
         "gpu_launches": launches,
