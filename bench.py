@@ -192,202 +192,19 @@ def algorithmic_flops_per_step(cfg) -> float:
     return lin + attn
 
 
-def cpu_oracle_chunk(cfg, w, Z, noise):
-    import oracle as O
-    Kc, Vc = O.prefix_kv(Z.astype(np.float64), w, cfg)
-    if cfg.w2a8:
-        return O.denoise_w2a8(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
-    return O.denoise(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
+def config_dict(cfg, ws=1):
+    """The `config` object of a bench line (the same keys on both arms)."""
+    return {"workload": cfg.name, "B": cfg.B, "P": cfg.P, "S": cfg.S, "L": cfg.L, "D": cfg.D, "F": cfg.F,
+            "heads": f"{cfg.n_q}q/{cfg.n_kv}kv x {cfg.d_h}", "H": cfg.H, "d_a": cfg.d_a,
+            "d_vlm": cfg.d_vlm, "global_batch": ws * cfg.B, "parallelism": f"replicas x{ws}",
+            "l2": "flushed (256 MiB write) between timed steps"}
 
 
-def cpu_baseline(cfg, w, Z, noise, budget_s=10.0):
-    """Oracle throughput on the host cores on a bounded sample: whole chunks
-    of observation 0, repeated until ~budget_s of CPU work."""
-    c1 = cfg.replace(B=1)
-    times = []
-    t_all = time.perf_counter()
-    while True:
-        t0 = time.perf_counter()
-        cpu_oracle_chunk(c1, w, Z[:1], noise[:1])
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_all > budget_s:
-            break
-    mean = sum(times) / len(times)
-    return {"value": 1.0 / mean, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{len(times)} whole chunk(s) (prefix K/V + {cfg.S} Euler steps) of observation 0 of "
-                      f"{cfg.name}, fp64 numpy/OpenBLAS, {mean * 1e3:.0f} ms per chunk"}
-
-
-def run_reference(args):
-    ws, rank, _ = _dist()
-    if rank != 0:
-        return 0
-    cfg = CONFIGS[args.workload]
-    w = make_weights(cfg)
-    if cfg.w2a8:
-        import oracle as O
-        w = O.with_unpacked(w)
-    Z, noise = make_observations(cfg, 1)
-    c1 = cfg.replace(B=1)
-    for _ in range(args.warmup):
-        cpu_oracle_chunk(c1, w, Z, noise)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        cpu_oracle_chunk(c1, w, Z, noise)
-    dt = (time.perf_counter() - t0) / args.steps
-    value = 1.0 / dt
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "B": 1, "P": cfg.P, "S": cfg.S, "note": "one observation per step"},
-        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{args.steps} whole chunks of observation 0 of {cfg.name} (prefix K/V + "
-                                   f"{cfg.S} Euler steps), fp64 numpy/OpenBLAS"},
-        "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-    return 0
-
-
-def eq3_sweep(cfg, dev_w, Zt, nt, steps=(1, 2, 4, 8, 16), reps=20):
-    """Solver-step sweep of the latency model L(T) = P + T E ("vla.cpp", §III-B
-    Eq. (3)): P = prefix K/V build, E = one Euler step, fitted by least squares
-    over T, and the speedup over recomputing the conditioning every step,
-    T (P + E) / (P + T E)."""
-    import torch
-
-    import prefix_cached_flow_gb300 as V
-    rows = []
-    for S in steps:
-        ex = V.Expert(cfg, dev_w, max_batch=cfg.B, max_prefix=cfg.P, n_steps=S)
-        Kc, Vc = ex.alloc_cache(cfg.B, cfg.P)
-        act = torch.empty_like(nt)
-        for _ in range(3):
-            ex.prefix_kv_build(Zt, Kc, Vc)
-            ex.denoise(Kc, Vc, nt, act)
-        torch.cuda.synchronize()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        tp = td = 0.0
-        for _ in range(reps):
-            e[0].record()
-            ex.prefix_kv_build(Zt, Kc, Vc)
-            e[1].record()
-            ex.denoise(Kc, Vc, nt, act)
-            e[2].record()
-            torch.cuda.synchronize()
-            tp += e[0].elapsed_time(e[1])
-            td += e[1].elapsed_time(e[2])
-        rows.append((S, tp / reps, td / reps))
-        ex.close()
-    Ts = np.array([r[0] for r in rows], dtype=np.float64)
-    L = np.array([r[1] + r[2] for r in rows])
-    A = np.stack([np.ones_like(Ts), Ts], axis=1)
-    (P_fit, E_fit), *_ = np.linalg.lstsq(A, L, rcond=None)
-    P_meas = float(np.mean([r[1] for r in rows]))
-    return {
-        "T": [int(t) for t in Ts], "prefix_ms": [round(r[1], 4) for r in rows],
-        "solve_ms": [round(r[2], 4) for r in rows], "fit_P_ms": float(P_fit), "fit_E_ms": float(E_fit),
-        "prefix_ms_measured": P_meas,
-        "speedup_vs_recompute": [float(t * (P_meas + E_fit) / (P_meas + t * E_fit)) for t in Ts],
-    }
-
-
-def run_ours(args):
-    import torch
-
-    import prefix_cached_flow_gb300 as V
-
-    ws, rank, local = _dist()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device")
-    torch.cuda.set_device(local)
-    dist = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if not os.path.exists(V.LIB_PATH):
-        import __graft_entry__
-        __graft_entry__.build()
-    cfg = CONFIGS[args.workload]
-    B = cfg.B
-    w = make_weights(cfg)
-    Z, noise = make_observations(cfg.replace(seed=replica_seed(cfg.seed, rank)), B)
-    ex = V.Expert(cfg, V.upload_weights(w, cfg.dtype, cfg.w2a8), max_batch=B, max_prefix=cfg.P)
-    dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
-    Zt = torch.from_numpy(Z).to(dt).cuda()
-    nt = torch.from_numpy(noise).cuda()
-    act = torch.empty_like(nt)
-    Kc, Vc = ex.alloc_cache(B, cfg.P)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def step():
-        ex.prefix_kv_build(Zt, Kc, Vc)
-        ex.denoise(Kc, Vc, nt, act)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    assert ex.poll_status() == 0
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sampler = ClockSampler(torch.cuda.current_device())
-    sampler.start()
-    time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.random_(0, 255)  # L2 flush between timed steps (outside the events)
-        e0, e1, e2 = ev[i]
-        e0.record(stream)
-        ex.prefix_kv_build(Zt, Kc, Vc)
-        e1.record(stream)
-        ex.denoise(Kc, Vc, nt, act)
-        e2.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clocks = sampler.stop()
-    status = ex.poll_status()
-    prefix_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    denoise_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    step_ms = prefix_ms + denoise_ms
-    step_ms, prefix_ms, denoise_ms = max_over_ranks(dist, [step_ms, prefix_ms, denoise_ms], "cuda")
-
-    # End to end through the public host-buffer call: H2D of Z and noise, the
-    # whole request, D2H of the chunk, every step.
-    Zh = torch.from_numpy(Z).to(dt).pin_memory()
-    nh = torch.from_numpy(noise).pin_memory()
-    ah = torch.empty_like(nh).pin_memory()
-    for _ in range(3):
-        ex.policy_step_host(Zh, nh, ah)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        ex.policy_step_host(Zh, nh, ah)
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    (e2e_ms,) = max_over_ranks(dist, [e2e_ms], "cuda")
-
-    hbm, tflops, tflops_sus, src = _peaks()
-    solver_bytes = cfg.S * algorithmic_bytes_per_step(cfg)
-    solver_flops = cfg.S * algorithmic_flops_per_step(cfg)
-    traffic = _traffic_from_profile(cfg.name)
-    # The solver launch runs for milliseconds back to back: the sustained
-    # tensor peak applies to it.  Bound = whichever roof takes longer.
-    if solver_flops / (tflops_sus * 1e12) > solver_bytes / (hbm * 1e9):
-        roof = {"bound": "tensor", "achieved": solver_flops / (denoise_ms * 1e-3) / 1e12, "peak": tflops_sus,
-                "unit": "TFLOP/s", "algorithmic_flops_per_launch": solver_flops,
-                "peak_note": "bf16 sustained"}
-    else:
-        roof = {"bound": "hbm", "achieved": solver_bytes / (denoise_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof.update({"traffic": traffic, "kernel": "solver launch (one CUDA graph of all S steps)",
-                 "algorithmic_bytes_per_launch": solver_bytes, "peak_source": src})
+def roofline(cfg, denoise_ms, traffic=None):
+    """Roofline of the solver launch: algorithmic bytes (or tensor FLOP) of
+    the S steps over its measured time, against the measured peak."""
+    roof = roofline(cfg, denoise_ms, _traffic_from_profile(cfg.name))
+    roof["kernel"] = "solver launch (all S steps)"
     launches = args.steps * (1 + ex.launch_count(B, cfg.P))
     line = {
         "metric": METRIC,
@@ -402,15 +219,13 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": cfg.name, "B": B, "P": cfg.P, "S": cfg.S, "L": cfg.L, "D": cfg.D, "F": cfg.F,
-                   "heads": f"{cfg.n_q}q/{cfg.n_kv}kv x {cfg.d_h}", "H": cfg.H, "d_a": cfg.d_a,
-                   "d_vlm": cfg.d_vlm, "global_batch": ws * B, "parallelism": f"replicas x{ws}",
-                   "l2": "flushed (256 MiB write) between timed steps"},
+        "config": config_dict(cfg, ws),
         "ms_per_chunk": step_ms / 1.0,
         "prefix_build_ms": prefix_ms,
         "denoise_ms": denoise_ms,
         "us_per_solver_step": denoise_ms * 1e3 / cfg.S,
         "roofline": roof,
+        "prefix_roofline": prefix_roofline(cfg, prefix_ms),
         "e2e": {"value": whole_job_rate(ws, B, e2e_ms), "unit": "chunks/s",
                 "h2d_bytes_per_step": int(Zh.numel() * Zh.element_size() + nh.numel() * 4),
                 "d2h_bytes_per_step": int(ah.numel() * 4)},
@@ -420,8 +235,13 @@ def run_ours(args):
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, w, Z, noise)
-    if args.sweep and rank == 0:
+    if not args.only and rank == 0 and ws == 1:
         line["eq3"] = eq3_sweep(cfg, V.upload_weights(w, cfg.dtype, cfg.w2a8), Zt, nt)
+        subs = {}
+        for name in ("full_bf16_b64", "w2a8_b1", "w2a8_b16"):
+            if name != cfg.name:
+                subs[name] = sub_workload(name, max(5, min(args.steps, 10)), flush, stream)
+        line["workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
     ex.close()
@@ -433,12 +253,13 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full_bf16_b1", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", action="store_true", help="add the Eq. (3) solver-step sweep (S = 1..16)")
+    ap.add_argument("--only", action="store_true",
+                    help="time the chosen workload alone (no Eq. (3) sweep, no other workloads)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -197,16 +197,62 @@ vla_status vla_policy_step_host(vla_expert* h, const void* Z_host, int B, int P,
  * since the last poll (VLA_ERR_TIMEOUT, VLA_ERR_ABORTED) or VLA_OK; clears it. */
 vla_status vla_expert_poll_status(vla_expert* h, void* stream);
 
-/* Sets (1) or clears (0) the handle's abort flag.  Kernels that see it set
- * skip their work and latch VLA_ERR_ABORTED.  Host-mapped, takes effect for
- * kernels that start after the write. */
+/* Sets (1) or clears (0) the handle's abort flag (host-mapped memory, no
+ * device call).  The first kernel of every solver step reads it; if it is
+ * set, VLA_ERR_ABORTED is latched and vla_expert_poll_status() reports it.
+ * The launch in flight runs to completion (bounded; no kernel is cut off with
+ * work outstanding), and the action chunk of an aborted call is unspecified.
+ * Clear the flag and poll the status before the next request. */
 vla_status vla_expert_set_abort(vla_expert* h, int abort);
 
-/* Eq. 4, first line, as a standalone op (the same kernel the W2A8 solver uses):
+/* Limit, in ns, of every bounded device-side wait of this handle's kernels
+ * (a wait that runs out latches VLA_ERR_TIMEOUT, frees what its CTA holds and
+ * returns).  0 restores the default of 2 s.  Synchronous (a small host to
+ * device copy); applies to kernels enqueued after the call. */
+vla_status vla_expert_set_wait_limit(vla_expert* h, unsigned long long limit_ns);
+
+/* Failure-path check: enqueues one single-thread kernel whose bounded wait can
+ * never be satisfied (an mbarrier expecting two arrivals gets one).  The wait
+ * runs out after the handle's wait limit, latches VLA_ERR_TIMEOUT and the
+ * kernel returns with nothing left in flight; vla_expert_poll_status() then
+ * returns VLA_ERR_TIMEOUT (and clears it) and the handle stays usable. */
+vla_status vla_expert_check_wait_timeout(vla_expert* h, void* stream);
+
+/* Diagnostic tap of the W2A8 solver (§III-E of the paper: intermediate
+ * tensors localize discrepancies).  While a tap is set, W2A8 denoise calls on
+ * this handle run without the CUDA graph and record, for solver step `step`,
+ * every layer's intermediate tensors into tap_dev; NULL clears the tap.
+ * tap_dev needs vla_expert_w2a8_tap_bytes(h, max_batch) bytes.  For batch B
+ * (T = B*H tokens, Q = n_q*d_h, QKV = Q + 2*n_kv*d_h, Hp = H rounded up to a
+ * multiple of 8), layer l's record starts at l * (bytes / L) and holds, in
+ * this order, each tensor starting on a 256-byte boundary:
+ *    0 h_in   f32  [T][D]    residual stream entering the layer
+ *    1 u_a    f32  [T][D]    modulated RMSNorm (attention), the quantiser input
+ *    2 c_a    bf16 [T][D]    its Eq. 4 codes (integers carried in bf16)
+ *    3 al_a   f32  [T]       their row scales alpha
+ *    4 acc_qkv i32 [T][QKV]  exact accumulators of [W_q;W_k;W_v]
+ *    5 q      bf16 [B][n_q][H][d_h]
+ *    6 k_s    bf16 [B][n_kv][H][d_h]
+ *    7 v_s^T  bf16 [B][n_kv][d_h][Hp]
+ *    8 o      f32  [T][Q]    attention output (quantiser input)
+ *    9 c_o    bf16 [T][Q]   10 al_o f32 [T]   11 acc_o i32 [T][D]
+ *   12 h_mid  f32  [T][D]    after the O-projection residual
+ *   13 u_m    f32  [T][D]   14 c_m bf16 [T][D]  15 al_m f32 [T]
+ *   16 acc_up i32  [T][F]   17 g   f32 [T][F]  (GeLU output, quantiser input)
+ *   18 c_d    bf16 [T][F]   19 al_d f32 [T]    20 acc_d i32 [T][D]
+ *   21 h_out  f32  [T][D]    after the down-projection residual
+ * Returns VLA_ERR_INVALID_ARG for a dense handle, a bad step, or a short or
+ * misaligned buffer. */
+vla_status vla_expert_w2a8_tap_bytes(const vla_expert* h, int B, size_t* bytes);
+vla_status vla_expert_set_w2a8_tap(vla_expert* h, int step, void* tap_dev, size_t bytes);
+
+/* Eq. 4, first line, as a standalone op.  Runs the row quantiser the W2A8
+ * solver runs on its fp32 rows (the same kernel template; the solver stores
+ * the codes as exact bf16 carriers, this entry point as int8):
  *   x_dev     [M][K] fp32 rows
  *   a_dev     [M][K] int8 out: clip(round_half_even(x / alpha_m), -128, 127)
  *   alpha_dev [M] fp32 out: max(|x_m|_inf, 1e-5) / 127 (IEEE division)
- * M >= 1, 1 <= K <= 65536. */
+ * M >= 1, 1 <= K <= 53248. */
 vla_status vla_w2a8_quantize_rows(const float* x_dev, int M, int K, int8_t* a_dev,
                                   float* alpha_dev, void* stream);
 
@@ -216,10 +262,12 @@ vla_status vla_w2a8_quantize_rows(const float* x_dev, int M, int K, int8_t* a_de
  *   beta       per-tensor fp32 scale
  *   y_dev      [M][N] bf16 (raw uint16 bits) out: bf16_rne((float(acc) * alpha_m) * beta)
  *   acc_dev    NULL or [M][N] int32 out: acc_mn = sum_j a_mj q_nj (exact)
- * K must be a multiple of 64 and N of 4.  Codes are assumed valid (3 is not
- * checked here).  Runs on the tensor cores: the int8 codes are carried exactly
- * in bf16 and every partial sum is an integer below 2^24, so the fp32
- * accumulators equal the int32 definition. */
+ * K must be a multiple of 64 with 64 <= K <= 65536 (so every |acc| stays
+ * below 2^24 and the fp32 accumulation is exact), and N a multiple of 4.
+ * Codes are assumed valid (3 is not checked here).  Runs on the tensor
+ * cores: the int8 codes are carried exactly in bf16 and every partial sum is
+ * an integer below 2^24, so the fp32 accumulators equal the int32
+ * definition.  Allocates its scratch from the stream's memory pool. */
 vla_status vla_w2a8_ternary_gemm(const int8_t* a_dev, const float* alpha_dev, const uint8_t* q_dev,
                                  float beta, int M, int N, int K, uint16_t* y_dev,
                                  int32_t* acc_dev, void* stream);
@@ -229,15 +277,19 @@ vla_status vla_w2a8_ternary_gemm(const int8_t* a_dev, const float* alpha_dev, co
  * while they run -- a robot control loop with a hard period, where a device
  * allocation may synchronise the device or take an unbounded time, or a host
  * program whose device memory is reserved up front by another runtime's
- * pool.  Same arguments, layouts and results (bit for bit) as
- * vla_w2a8_ternary_gemm, but its fp32 partial-sum scratch is a fixed array
- * of VLA_NOALLOC_MAX_ELEMS floats (4 MiB) inside the library, held by every
- * GPU that loads the library until the process exits; the call itself makes
- * no allocation.
+ * pool.  Same arguments, layouts, limits and results (bit for bit) as
+ * vla_w2a8_ternary_gemm, with one more requirement: a_dev must be 4-byte
+ * aligned (its kernel reads the codes as 32-bit words; a misaligned a_dev is
+ * refused with VLA_ERR_INVALID_ARG before anything is enqueued).  Its fp32
+ * partial-sum scratch is a fixed array of VLA_NOALLOC_MAX_ELEMS floats
+ * (4 MiB) inside the library, held by every GPU that loads the library until
+ * the process exits; the call itself makes no allocation.
  *   - M * N > VLA_NOALLOC_MAX_ELEMS -> VLA_ERR_UNSUPPORTED (nothing enqueued).
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is cached per device ordinal: after a
+ *     cudaDeviceReset of a device, do not call this entry point on it again
+ *     in the same process.
  *   - All calls share the array, which keeps the last call's contents; calls
  *     that overlap on the GPU race on it, so order them (one stream, or
  *     explicit dependencies).  Nothing needs clearing between calls: every
@@ -246,6 +298,12 @@ vla_status vla_w2a8_ternary_gemm(const int8_t* a_dev, const float* alpha_dev, co
 vla_status vla_w2a8_ternary_gemm_noalloc(const int8_t* a_dev, const float* alpha_dev, const uint8_t* q_dev,
                                          float beta, int M, int N, int K, uint16_t* y_dev,
                                          int32_t* acc_dev, void* stream);
+
+/* Diagnostic: the exact GeLU x Phi(x) of the few-token kernels (erff) and the
+ * form the many-token linear epilogue uses (erf by Abramowitz & Stegun 7.1.26,
+ * |error| <= 1.5e-7, with approximate reciprocal and exponential), both for
+ * n fp32 inputs x_dev into exact_dev and fast_dev. */
+vla_status vla_debug_gelu_forms(const float* x_dev, int n, float* exact_dev, float* fast_dev, void* stream);
 
 /* Number of kernels one denoise call launches for batch B and prefix P
  * (all of them inside the one graph launch).  Host-only arithmetic. */

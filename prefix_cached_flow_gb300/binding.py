@@ -28,7 +28,9 @@ FLAG_LINEAR_SPLIT, FLAG_LINEAR_WIDE = 16, 32
 EXPORTED = ("vla_expert_create", "vla_expert_create_w2a8", "vla_expert_destroy", "vla_prefix_cache_bytes",
             "vla_prefix_kv_build", "vla_action_denoise", "vla_action_denoise_w2a8", "vla_policy_step_host",
             "vla_expert_poll_status", "vla_expert_set_abort", "vla_w2a8_quantize_rows",
-            "vla_w2a8_ternary_gemm", "vla_expert_launch_count", "vla_status_string", "vla_version", "vla_last_error")
+            "vla_w2a8_ternary_gemm", "vla_expert_launch_count", "vla_status_string", "vla_version", "vla_last_error",
+            "vla_expert_set_wait_limit", "vla_expert_check_wait_timeout", "vla_expert_w2a8_tap_bytes",
+            "vla_expert_set_w2a8_tap", "vla_debug_gelu_forms")
 
 
 class VlaError(RuntimeError):
@@ -84,6 +86,11 @@ def lib() -> ctypes.CDLL:
         "vla_w2a8_quantize_rows": [vp, ci, ci, vp, vp, vp],
         "vla_w2a8_ternary_gemm": [vp, vp, vp, cf, ci, ci, ci, vp, vp, vp],
         "vla_expert_launch_count": [vp, ci, ci, ctypes.POINTER(ci)],
+        "vla_expert_set_wait_limit": [vp, ctypes.c_ulonglong],
+        "vla_expert_check_wait_timeout": [vp, vp],
+        "vla_expert_w2a8_tap_bytes": [vp, ci, ctypes.POINTER(ctypes.c_size_t)],
+        "vla_expert_set_w2a8_tap": [vp, ci, vp, ctypes.c_size_t],
+        "vla_debug_gelu_forms": [vp, ci, vp, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -210,6 +217,59 @@ class Expert:
     def set_abort(self, flag: bool):
         _check(lib().vla_expert_set_abort(self._h, 1 if flag else 0), "vla_expert_set_abort")
 
+    def set_wait_limit(self, ns: int):
+        _check(lib().vla_expert_set_wait_limit(self._h, int(ns)), "vla_expert_set_wait_limit")
+
+    def check_wait_timeout(self, stream=None):
+        _check(lib().vla_expert_check_wait_timeout(self._h, _stream(stream)), "vla_expert_check_wait_timeout")
+
+    # -- W2A8 diagnostic tap ----------------------------------------------
+    TAP_NAMES = ("h_in", "u_a", "c_a", "al_a", "acc_qkv", "q", "k_s", "v_sT", "o", "c_o", "al_o", "acc_o", "h_mid",
+                 "u_m", "c_m", "al_m", "acc_up", "g", "c_d", "al_d", "acc_d", "h_out")
+
+    def set_w2a8_tap(self, step: int | None, B: int | None = None):
+        """Start recording solver step `step` of later W2A8 calls (None stops).
+        Returns the raw uint8 device buffer; decode it with w2a8_tap_views()."""
+        if step is None:
+            _check(lib().vla_expert_set_w2a8_tap(self._h, 0, None, 0), "vla_expert_set_w2a8_tap")
+            self._tap = None
+            return None
+        n = ctypes.c_size_t()
+        _check(lib().vla_expert_w2a8_tap_bytes(self._h, self._c.max_batch, ctypes.byref(n)),
+               "vla_expert_w2a8_tap_bytes")
+        buf = torch.zeros(n.value, dtype=torch.uint8, device="cuda")
+        _check(lib().vla_expert_set_w2a8_tap(self._h, step, _ptr(buf), n.value), "vla_expert_set_w2a8_tap")
+        self._tap = buf
+        return buf
+
+    def w2a8_tap_views(self, B: int) -> list:
+        """Per layer, a dict of host numpy arrays in the layout vla.h documents."""
+        c = self.cfg
+        T, D, F = B * c.H, c.D, c.F
+        Q, KV = c.n_q * c.d_h, c.n_kv * c.d_h
+        Hp = (c.H + 7) // 8 * 8
+        f32, bf, i32 = torch.float32, torch.bfloat16, torch.int32
+        shapes = [(f32, (T, D)), (f32, (T, D)), (bf, (T, D)), (f32, (T,)), (i32, (T, Q + 2 * KV)),
+                  (bf, (B, c.n_q, c.H, c.d_h)), (bf, (B, c.n_kv, c.H, c.d_h)), (bf, (B, c.n_kv, c.d_h, Hp)),
+                  (f32, (T, Q)), (bf, (T, Q)), (f32, (T,)), (i32, (T, D)), (f32, (T, D)),
+                  (f32, (T, D)), (bf, (T, D)), (f32, (T,)), (i32, (T, F)), (f32, (T, F)), (bf, (T, F)),
+                  (f32, (T,)), (i32, (T, D)), (f32, (T, D))]
+        n = ctypes.c_size_t()
+        _check(lib().vla_expert_w2a8_tap_bytes(self._h, B, ctypes.byref(n)), "vla_expert_w2a8_tap_bytes")
+        per_layer = n.value // c.L
+        raw = self._tap.cpu()
+        out = []
+        for l in range(c.L):
+            off = l * per_layer
+            rec = {}
+            for name, (dt, shp) in zip(self.TAP_NAMES, shapes):
+                nb = int(np_prod(shp)) * torch.tensor([], dtype=dt).element_size()
+                t = raw[off:off + nb].view(dt).reshape(shp)
+                rec[name] = t.float().numpy() if dt == bf else t.numpy()
+                off += (nb + 255) // 256 * 256
+            out.append(rec)
+        return out
+
     def close(self):
         if getattr(self, "_h", None):
             lib().vla_expert_destroy(self._h)
@@ -220,6 +280,22 @@ class Expert:
             self.close()
         except Exception:
             pass
+
+
+def np_prod(shape):
+    n = 1
+    for d in shape:
+        n *= int(d)
+    return n
+
+
+def gelu_forms(x, stream=None):
+    """(erff GeLU, many-token epilogue GeLU) of an fp32 device tensor."""
+    n = x.numel()
+    exact = torch.empty_like(x)
+    fast = torch.empty_like(x)
+    _check(lib().vla_debug_gelu_forms(_ptr(x), n, _ptr(exact), _ptr(fast), _stream(stream)), "vla_debug_gelu_forms")
+    return exact, fast
 
 
 def quantize_rows(x, stream=None):

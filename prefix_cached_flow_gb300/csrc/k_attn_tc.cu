@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(128, 1)
 
   // Drain the TMA copies (complete unless a wait timed out) and free TMEM.
   if (threadIdx.x == 0 && nk > 0) {
-    mbar_wait(&bars[0], 0, a.status);
-    mbar_wait(&bars[1], 0, a.status);
+    mbar_drain(&bars[0], 0);
+    mbar_drain(&bars[1], 0);
   }
   tc_fence_before();
   __syncthreads();

@@ -529,7 +529,7 @@ __global__ void k_head_multi(ExpertDims d, StepBufs b, int step, float dt, const
 // row's rms, u = h / rms * (1 + gamma) + beta, alpha = max(|u|, 1e-5) / 127
 // and the codes (as exact bf16 carriers).
 __global__ void k_quant_norm(int D, float eps, const float* h, const float* gamma, const float* beta, bf16* codes,
-                             float* alpha) {
+                             float* alpha, float* u_out) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
@@ -544,14 +544,18 @@ __global__ void k_quant_norm(int D, float eps, const float* h, const float* gamm
   }
   ss = block_sum(ss, red);
   const float r = rsqrtf(ss / (float)D + eps);
-  for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = row[i] * r * (1.f + gamma[i]) + beta[i];
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    row[i] = row[i] * r * (1.f + gamma[i]) + beta[i];
+    if (u_out) u_out[(size_t)t * D + i] = row[i];
+  }
   __syncthreads();
   const float al = quantize_row_block(row, D, nullptr, codes + (size_t)t * D, red);
   if (threadIdx.x == 0) alpha[t] = al;
 }
 
-// Eq. (4) on fp32 rows x [T][K].
-__global__ void k_quant_rows(int K, const float* x, bf16* codes, float* alpha) {
+// Eq. (4) on fp32 rows x [T][K]; codes as bf16 carriers (I8 false) or int8.
+template <bool I8>
+__global__ void k_quant_rows(int K, const float* x, void* codes, float* alpha) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
@@ -560,7 +564,8 @@ __global__ void k_quant_rows(int K, const float* x, bf16* codes, float* alpha) {
   const int t = blockIdx.x;
   for (int i = threadIdx.x; i < K; i += blockDim.x) row[i] = x[(size_t)t * K + i];
   __syncthreads();
-  const float al = quantize_row_block(row, K, nullptr, codes + (size_t)t * K, red);
+  const float al = I8 ? quantize_row_block(row, K, (int8_t*)codes + (size_t)t * K, nullptr, red)
+                      : quantize_row_block(row, K, nullptr, (bf16*)codes + (size_t)t * K, red);
   if (threadIdx.x == 0) alpha[t] = al;
 }
 
@@ -590,6 +595,12 @@ __device__ __forceinline__ float4 modulate4(float4 v, float r, float4 g, float4 
 __device__ __forceinline__ uint2 codes4(float4 u, float al) {
   auto q = [&](float x) { return fminf(fmaxf(rintf(__fdiv_rn(x, al)), -128.f), 127.f); };
   return make_uint2(pack_bf16x2(q(u.x), q(u.y)), pack_bf16x2(q(u.z), q(u.w)));
+}
+
+// The same four codes as int8, packed little-endian into one word.
+__device__ __forceinline__ uint32_t codes4_i8(float4 u, float al) {
+  auto q = [&](float x) { return (uint32_t)((int)fminf(fmaxf(rintf(__fdiv_rn(x, al)), -128.f), 127.f) & 0xFF); };
+  return q(u.x) | (q(u.y) << 8) | (q(u.z) << 16) | (q(u.w) << 24);
 }
 
 __device__ __forceinline__ float absmax4(float4 u) { return fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))); }
@@ -622,7 +633,7 @@ __global__ void k_modnorm_v(int T, int D, float eps, const float* h, const float
 // Eq. (4) on the modulated RMSNorm of h (the row's own sum of squares).
 template <int RV>
 __global__ void k_quant_norm_v(int D, float eps, const float* h, const float* gamma, const float* beta, bf16* codes,
-                               float* alpha) {
+                               float* alpha, float* u_out) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   __shared__ float red[32];
@@ -640,7 +651,11 @@ __global__ void k_quant_norm_v(int D, float eps, const float* h, const float* ga
 #pragma unroll
   for (int k = 0; k < RV; ++k) {
     v[k] = modulate4(v[k], r, g[k], b[k]);
-    if (threadIdx.x + k * blockDim.x < nc) am = fmaxf(am, absmax4(v[k]));
+    const int c = threadIdx.x + k * blockDim.x;
+    if (c < nc) {
+      am = fmaxf(am, absmax4(v[k]));
+      if (u_out) *(float4*)(u_out + (size_t)t * D + 4 * c) = v[k];
+    }
   }
   am = block_max(am, red);
   const float al = __fdiv_rn(fmaxf(am, 1e-5f), 127.0f);
@@ -652,9 +667,9 @@ __global__ void k_quant_norm_v(int D, float eps, const float* h, const float* ga
   if (threadIdx.x == 0) alpha[t] = al;
 }
 
-// Eq. (4) on fp32 rows x [T][K].
-template <int RV>
-__global__ void k_quant_rows_v(int K, const float* x, bf16* codes, float* alpha) {
+// Eq. (4) on fp32 rows x [T][K]; codes as bf16 carriers (I8 false) or int8.
+template <int RV, bool I8>
+__global__ void k_quant_rows_v(int K, const float* x, void* codes, float* alpha) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   __shared__ float red[32];
@@ -669,9 +684,30 @@ __global__ void k_quant_rows_v(int K, const float* x, bf16* codes, float* alpha)
 #pragma unroll
   for (int k = 0; k < RV; ++k) {
     const int c = threadIdx.x + k * blockDim.x;
-    if (c < nc) *(uint2*)(codes + (size_t)t * K + 4 * c) = codes4(v[k], al);
+    if (c < nc) {
+      if (I8)
+        *(uint32_t*)((int8_t*)codes + (size_t)t * K + 4 * c) = codes4_i8(v[k], al);
+      else
+        *(uint2*)((bf16*)codes + (size_t)t * K + 4 * c) = codes4(v[k], al);
+    }
   }
   if (threadIdx.x == 0) alpha[t] = al;
+}
+
+// A bounded wait that cannot be satisfied: the mbarrier expects two arrivals
+// and gets one.  The wait runs out after the handle's limit, latches
+// VLA_DEV_TIMEOUT and the kernel returns (nothing is left in flight).
+__global__ void k_expire_wait(int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 2);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive(&bar);
+    mbar_wait(&bar, 0, status);
+  }
 }
 
 // Threads for a register-held row of K floats with RV float4 per thread,
@@ -713,7 +749,9 @@ cudaError_t expert_kernels_init() {
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_quant_norm);
   if (e != cudaSuccess) return e;
-  e = set_max_dyn_smem(k_quant_rows);
+  e = set_max_dyn_smem(k_quant_rows<false>);
+  if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_quant_rows<true>);
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_attn_combine<float>);
   if (e != cudaSuccess) return e;
@@ -775,10 +813,10 @@ cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss,
 }
 
 cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* gamma, const float* beta, bf16* codes,
-                              float* alpha, cudaStream_t st) {
+                              float* alpha, float* u_out, cudaStream_t st) {
   int D = d.D;
   float eps = d.eps;
-  void* args[] = {&D, &eps, (void*)&h, (void*)&gamma, (void*)&beta, &codes, &alpha};
+  void* args[] = {&D, &eps, (void*)&h, (void*)&gamma, (void*)&beta, &codes, &alpha, &u_out};
   const int rv = row_vec(d.B * d.H, D), th = row_threads(D, rv);
   if (th)
     return launch_pdl(rv == 1 ? (const void*)k_quant_norm_v<1> : (const void*)k_quant_norm_v<2>, dim3(d.B * d.H),
@@ -786,13 +824,30 @@ cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* 
   return launch_pdl((const void*)k_quant_norm, dim3(d.B * d.H), dim3(512), (size_t)(D + 32) * sizeof(float), st, args);
 }
 
-cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st) {
+static cudaError_t launch_quant_rows_any(int T, int K, const float* x, void* codes, bool i8, float* alpha,
+                                         cudaStream_t st) {
   void* args[] = {&K, (void*)&x, &codes, &alpha};
   const int rv = row_vec(T, K), th = row_threads(K, rv);
-  if (th)
-    return launch_pdl(rv == 1 ? (const void*)k_quant_rows_v<1> : (const void*)k_quant_rows_v<2>, dim3(T), dim3(th), 0,
-                      st, args);
-  return launch_pdl((const void*)k_quant_rows, dim3(T), dim3(512), (size_t)(K + 32) * sizeof(float), st, args);
+  if (th) {
+    const void* fn = rv == 1 ? (i8 ? (const void*)k_quant_rows_v<1, true> : (const void*)k_quant_rows_v<1, false>)
+                             : (i8 ? (const void*)k_quant_rows_v<2, true> : (const void*)k_quant_rows_v<2, false>);
+    return launch_pdl(fn, dim3(T), dim3(th), 0, st, args);
+  }
+  return launch_pdl(i8 ? (const void*)k_quant_rows<true> : (const void*)k_quant_rows<false>, dim3(T), dim3(512),
+                    (size_t)(K + 32) * sizeof(float), st, args);
+}
+
+cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st) {
+  return launch_quant_rows_any(T, K, x, codes, false, alpha, st);
+}
+
+cudaError_t launch_quant_rows_i8(int T, int K, const float* x, int8_t* codes, float* alpha, cudaStream_t st) {
+  return launch_quant_rows_any(T, K, x, codes, true, alpha, st);
+}
+
+cudaError_t launch_expire_wait(int* status, cudaStream_t st) {
+  k_expire_wait<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_i8_to_bf16(const int8_t* a, bf16* out, size_t n, cudaStream_t st) {

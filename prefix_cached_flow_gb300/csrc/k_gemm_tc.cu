@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(128, 1)
   // Drain: make sure no TMA write into this CTA's shared memory is in flight.
   if (warp == 0 && lane == 0) {
     const int first = issued > NS ? issued - NS : 0;
-    for (int i = first; i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1, g.status);
+    for (int i = first; i < issued; ++i) mbar_drain(&full[i % NS], (i / NS) & 1);
+    mbar_drain(done, 0);  // the MMA warp always commits `done`
   }
   tc_fence_before();
   __syncthreads();

@@ -1,12 +1,13 @@
-// Fused linear layer of the action expert on tcgen05, with on-chip split-K.
+// Fused linear layer of the action expert on tcgen05, with split-K inside a
+// thread-block cluster.
 //
 // y[t][n] = sum_k W[n][k] X[t][k] for one weight tile of 128 output rows and
 // one token tile of BN tokens.  The K range is split over the C CTAs of a
 // thread-block cluster (grid.z = C = cluster size); each CTA accumulates its
-// slice in TMEM, stages the fp32 tile in its shared memory, and after a
-// cluster barrier CTA `rank` sums rows [rank*128/C, (rank+1)*128/C) of all C
-// tiles through distributed shared memory (fixed order: deterministic) and
-// applies the epilogue:
+// slice in TMEM and writes the fp32 tile to a per-rank exchange buffer in
+// global memory (L2); after a cluster barrier CTA `rank` sums rows
+// [rank*128/C, (rank+1)*128/C) of all C tiles from that buffer (fixed order:
+// deterministic) and applies the epilogue:
 //   EPI_QKV   scatter to q [B][n_q][H][d_h], k_s [B][n_kv][H][d_h] and
 //             v_s^T [B][n_kv][d_h][Hp] (bf16) for the attention kernel;
 //   EPI_RESID h[t][n] += y, and per-(128-row block, token) sums of squares of
@@ -347,7 +348,10 @@ __global__ void __launch_bounds__(128, 1)
         const int t = t0 + c0 + j;
         const bool valid = ok && c0 + j < tcols && n < g.N;
         float y = v[j];
-        if (AMODE == 1 && valid) y = w2a8_scale(y, g.alpha[t], be);
+        if (AMODE == 1 && valid) {
+          if (EPI != EPI_W2A8_OUT && g.accout) g.accout[(size_t)t * g.N + n] = (int32_t)y;  // diagnostic tap
+          y = w2a8_scale(y, g.alpha[t], be);
+        }
         float sq = 0.f;
         if (valid) {
           if (EPI == EPI_RESID) {
@@ -435,6 +439,8 @@ __global__ void __launch_bounds__(128, 1)
       acc.y = w2a8_scale(acc.y, al, be);
       acc.z = w2a8_scale(acc.z, al, be);
       acc.w = w2a8_scale(acc.w, al, be);
+      if (EPI != EPI_W2A8_OUT && g.accout)  // diagnostic tap of the exact accumulators
+        *(int4*)(g.accout + (size_t)t * g.N + n) = make_int4((int)raw.x, (int)raw.y, (int)raw.z, (int)raw.w);
     }
     if (EPI == EPI_RESID) {
       float ss = 0.f;
@@ -562,10 +568,11 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0 && lane == 0) {
     const int first = issued > NS ? issued - NS : 0;
     for (int i = first; i < issued; ++i) {
-      mbar_wait(&full[i % NS], (i / NS) & 1, g.status);
-      if (AMODE == 1) mbar_wait(&aready[i % NS], (i / NS) & 1, g.status);
+      mbar_drain(&full[i % NS], (i / NS) & 1);
+      if (AMODE == 1) mbar_drain(&aready[i % NS], (i / NS) & 1);
     }
-    if (BMODE == 1) mbar_wait(hbar, 0, g.status);
+    if (BMODE == 1) mbar_drain(hbar, 0);
+    mbar_drain(done, 0);  // the MMA warp always commits `done`
   }
   tc_fence_before();
   __syncthreads();

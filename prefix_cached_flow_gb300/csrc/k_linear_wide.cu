@@ -109,6 +109,22 @@ __device__ __forceinline__ void gelu_as7126_x2(float x0, float x1, float& g0, fl
   up2(fma2(h, erfv, h), g0, g1);
 }
 
+// Both GeLU forms of the library side by side (for the unit check of the
+// many-token epilogue's erf approximation against the erff form).
+__global__ void k_gelu_forms(const float* x, int n, float* exact, float* fast) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x0 = x[i], x1 = i + 1 < n ? x[i + 1] : 0.f;
+  float g0, g1;
+  gelu_as7126_x2(x0, x1, g0, g1);
+  exact[i] = gelu_exact(x0);
+  fast[i] = g0;
+  if (i + 1 < n) {
+    exact[i + 1] = gelu_exact(x1);
+    fast[i + 1] = g1;
+  }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kWideThreads, 1)
     k_linear_wide(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const LinArgs g) {
@@ -419,6 +435,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 }  // namespace
 
 size_t linear_wide_smem_bytes(int BN) { return 1024 + wide_layout(BN).total; }
+
+cudaError_t launch_gelu_forms(const float* x, int n, float* exact, float* fast, cudaStream_t st) {
+  const int pairs = (n + 1) / 2;
+  k_gelu_forms<<<(pairs + 255) / 256, 256, 0, st>>>(x, n, exact, fast);
+  return cudaGetLastError();
+}
 
 cudaError_t linear_wide_init() {
   cudaError_t e = set_max_dyn_smem(k_linear_wide<EPI_QKV>);

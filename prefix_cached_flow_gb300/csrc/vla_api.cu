@@ -105,6 +105,10 @@ struct vla_expert {
   cudaStream_t cap_stream = nullptr;
   std::vector<GraphEntry> graphs;
   uint64_t tick = 0;
+  // diagnostic tap of one W2A8 solver step (vla_expert_set_w2a8_tap)
+  void* tap = nullptr;
+  size_t tap_cap = 0;
+  int tap_step = -1;
   // request buffers (vla_policy_step_host), allocated on first use
   void* req_z = nullptr;
   void* req_kc = nullptr;
@@ -380,6 +384,37 @@ int attn_kc(int P, int cs) {
   return kc < 16 ? 16 : kc;
 }
 
+// Diagnostic W2A8 tap: for every layer of the tapped step, 22 tensors in this
+// order, each starting on a 256-byte boundary (the layout vla.h documents).
+constexpr int kTapTensors = 22;
+void tap_sizes(const vla_expert* h, int B, size_t sz[kTapTensors]) {
+  const vla_expert_config& c = h->cfg;
+  const size_t T = (size_t)B * c.horizon, D = c.width, F = c.mlp_width, Q = h->qdim;
+  const size_t v[kTapTensors] = {
+      T * D * 4, T * D * 4, T * D * 2, T * 4, T * h->qkvdim * 4,                        // h_in u_a c_a al_a acc_qkv
+      (size_t)B * c.n_q_heads * c.horizon * c.head_dim * 2,                             // q
+      (size_t)B * c.n_kv_heads * c.horizon * c.head_dim * 2,                            // k_s
+      (size_t)B * c.n_kv_heads * c.head_dim * h->Hp * 2,                                // v_s^T
+      T * Q * 4, T * Q * 2, T * 4, T * D * 4, T * D * 4,                                // o32 c_o al_o acc_o h_mid
+      T * D * 4, T * D * 2, T * 4, T * F * 4, T * F * 4, T * F * 2, T * 4, T * D * 4,   // u_m c_m al_m acc_up g32 c_d al_d acc_d
+      T * D * 4};                                                                      // h_out
+  for (int i = 0; i < kTapTensors; ++i) sz[i] = v[i];
+}
+size_t tap_pad(size_t b) { return (b + 255) / 256 * 256; }
+size_t tap_layer_bytes(const vla_expert* h, int B) {
+  size_t sz[kTapTensors], tot = 0;
+  tap_sizes(h, B, sz);
+  for (size_t x : sz) tot += tap_pad(x);
+  return tot;
+}
+// Device address of tensor `i` of layer `l` in the tap.
+char* tap_at(const vla_expert* h, int B, int l, int i) {
+  size_t sz[kTapTensors], off = tap_layer_bytes(h, B) * (size_t)l;
+  tap_sizes(h, B, sz);
+  for (int j = 0; j < i; ++j) off += tap_pad(sz[j]);
+  return (char*)h->tap + off;
+}
+
 bool fused_supported(const vla_expert_config& c, bool f32, bool w2a8, bool use_tc) {
   if (f32 || !use_tc) return false;
   (void)w2a8;
@@ -550,9 +585,17 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
   AttnPlan ap;
   VLA_ST(plan_attention(h, B, P, kc, vc, nullptr, h->f32buf, &ap));
   const DevCtl ctl{h->d_status, h->d_abort};
+  size_t tsz[kTapTensors];
+  tap_sizes(h, B, tsz);
   for (int k = 0; k < h->S; ++k) {
     const float* x_in = k == 0 ? noise : actions;
     const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    const bool tapping = h->tap && k == h->tap_step;
+    // tap: copy workspace tensor `src` into tensor `i` of layer `l`
+    auto cp = [&](int l, int i, const void* src) -> cudaError_t {
+      return tapping ? cudaMemcpyAsync(tap_at(h, B, l, i), src, tsz[i], cudaMemcpyDeviceToDevice, st) : cudaSuccess;
+    };
+    auto tp = [&](int l, int i) -> void* { return tapping ? (void*)tap_at(h, B, l, i) : nullptr; };
     VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
     for (int l = 0; l < L; ++l) {
       const float* mod = h->modtab + ((size_t)k * L + l) * 4 * D;
@@ -563,27 +606,47 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
 #else
       auto tls = [&](int) -> unsigned long long* { return nullptr; };
 #endif
-      VLA_CK(launch_quant_norm(d, h->h, mod, mod + D, act, h->alpha, st));
+      VLA_CK(cp(l, 0, h->h));
+      VLA_CK(launch_quant_norm(d, h->h, mod, mod + D, act, h->alpha, (float*)tp(l, 1), st));
+      VLA_CK(cp(l, 2, act));
+      VLA_CK(cp(l, 3, h->alpha));
       LinArgs a = lin_args(h, pq, h->qkvdim, T, l);
       a.tl = tls(0);
       a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
+      a.accout = (int32_t*)tp(l, 4);
       VLA_CK(launch_linear(&h->tm_wqkv, &tm_u, &tmH, a, pq.tiles_n, pq.tiles_t, pq.C, st));
+      VLA_CK(cp(l, 5, h->q));
+      VLA_CK(cp(l, 6, h->ks));
+      VLA_CK(cp(l, 7, h->vs));
       VLA_ST(enqueue_attention(ap, l, tls(1), st));
+      VLA_CK(cp(l, 8, h->f32buf));
       VLA_CK(launch_quant_rows(T, Q, h->f32buf, act, h->alpha, st));
+      VLA_CK(cp(l, 9, act));
+      VLA_CK(cp(l, 10, h->alpha));
       a = lin_args(h, po, D, T, l);
       a.tl = tls(2);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_slot = 3;  // the quantiser reads h itself
+      a.accout = (int32_t*)tp(l, 11);
       VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
-      VLA_CK(launch_quant_norm(d, h->h, mod + 2 * D, mod + 3 * D, act, h->alpha, st));
+      VLA_CK(cp(l, 12, h->h));
+      VLA_CK(launch_quant_norm(d, h->h, mod + 2 * D, mod + 3 * D, act, h->alpha, (float*)tp(l, 13), st));
+      VLA_CK(cp(l, 14, act));
+      VLA_CK(cp(l, 15, h->alpha));
       a = lin_args(h, pu, F, T, l);
       a.tl = tls(3);
       a.epi = EPI_GELU; a.g32 = h->f32buf; a.ldg = F; a.beta_slot = 4;
+      a.accout = (int32_t*)tp(l, 16);
       VLA_CK(launch_linear(&h->tm_wup, &tm_u, &tmH, a, pu.tiles_n, pu.tiles_t, pu.C, st));
+      VLA_CK(cp(l, 17, h->f32buf));
       VLA_CK(launch_quant_rows(T, F, h->f32buf, act, h->alpha, st));
+      VLA_CK(cp(l, 18, act));
+      VLA_CK(cp(l, 19, h->alpha));
       a = lin_args(h, pd, D, T, l);
       a.tl = tls(4);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_slot = 5;
+      a.accout = (int32_t*)tp(l, 20);
       VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
+      VLA_CK(cp(l, 21, h->h));
     }
     VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));
   }
@@ -1000,7 +1063,7 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
                      : enqueue_denoise_fused(h, Kc, Vc, B, P, noise, actions, tap, s2);
     return enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, s2);
   };
-  if (h->cfg.flags & VLA_FLAG_NO_GRAPH) return enqueue(st);
+  if ((h->cfg.flags & VLA_FLAG_NO_GRAPH) || h->tap) return enqueue(st);
   GraphEntry* hit = nullptr;
   for (auto& g : h->graphs)
     if (g.B == B && g.P == P && g.kc == Kc && g.vc == Vc && g.noise == noise && g.actions == actions && g.tap == tap)
@@ -1108,13 +1171,55 @@ vla_status vla_policy_step_host(vla_expert* h, const void* Z_host, int B, int P,
 
 vla_status vla_w2a8_quantize_rows(const float* x, int M, int K, int8_t* a, float* alpha, void* stream) {
   if (!x || !a || !alpha || M < 1 || K < 1 || K > 53248) return VLA_ERR_INVALID_ARG;
-  VLA_CK(launch_quantize_rows(x, M, K, a, alpha, (cudaStream_t)stream));
+  VLA_CK(expert_kernels_init());
+  VLA_CK(launch_quant_rows_i8(M, K, x, a, alpha, (cudaStream_t)stream));
+  return VLA_OK;
+}
+
+vla_status vla_debug_gelu_forms(const float* x, int n, float* exact, float* fast, void* stream) {
+  if (!x || !exact || !fast || n < 1) return VLA_ERR_INVALID_ARG;
+  VLA_CK(launch_gelu_forms(x, n, exact, fast, (cudaStream_t)stream));
+  return VLA_OK;
+}
+
+vla_status vla_expert_set_wait_limit(vla_expert* h, unsigned long long limit_ns) {
+  if (!h || !h->d_status) return VLA_ERR_INVALID_ARG;
+  VLA_CK(cudaMemcpy(h->d_status + 2, &limit_ns, sizeof(limit_ns), cudaMemcpyHostToDevice));
+  return VLA_OK;
+}
+
+vla_status vla_expert_check_wait_timeout(vla_expert* h, void* stream) {
+  if (!h || !h->d_status) return VLA_ERR_INVALID_ARG;
+  VLA_CK(launch_expire_wait(h->d_status, (cudaStream_t)stream));
+  return VLA_OK;
+}
+
+vla_status vla_expert_w2a8_tap_bytes(const vla_expert* h, int B, size_t* bytes) {
+  if (!h || !bytes || !h->w2a8 || B < 1 || B > h->cfg.max_batch) return VLA_ERR_INVALID_ARG;
+  *bytes = tap_layer_bytes(h, B) * (size_t)h->cfg.n_layers;
+  return VLA_OK;
+}
+
+vla_status vla_expert_set_w2a8_tap(vla_expert* h, int step, void* tap_dev, size_t bytes) {
+  if (!h || !h->w2a8) return VLA_ERR_INVALID_ARG;
+  if (!tap_dev) {
+    h->tap = nullptr;
+    h->tap_cap = 0;
+    h->tap_step = -1;
+    return VLA_OK;
+  }
+  if (!h->fused || !aligned16(tap_dev) || step < 0 || step >= h->S ||
+      bytes < tap_layer_bytes(h, h->cfg.max_batch) * (size_t)h->cfg.n_layers)
+    return VLA_ERR_INVALID_ARG;
+  h->tap = tap_dev;
+  h->tap_cap = bytes;
+  h->tap_step = step;
   return VLA_OK;
 }
 
 vla_status vla_w2a8_ternary_gemm(const int8_t* a, const float* alpha, const uint8_t* q, float beta, int M, int N,
                                  int K, uint16_t* y, int32_t* acc, void* stream) {
-  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64 || N % 4) return VLA_ERR_INVALID_ARG;
+  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64 || K > 65536 || N % 4) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   int dev = 0, sms = 0;
   VLA_CK(cudaGetDevice(&dev));

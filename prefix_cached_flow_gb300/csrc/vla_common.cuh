@@ -195,21 +195,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The status block a handle passes to its kernels: word 0 is the latched
+// error, words 2-3 the bounded-wait limit in ns (0: the default limit).
+__device__ __forceinline__ uint64_t wait_limit_ns(const int* status) {
+  if (!status) return VLA_WAIT_LIMIT_NS;
+  const uint64_t lim = *(const volatile unsigned long long*)(status + 2);
+  return lim ? lim : VLA_WAIT_LIMIT_NS;
+}
 // Bounded wait for the phase with the given parity.  On timeout latches
 // VLA_DEV_TIMEOUT and returns false; also gives up early once another thread
-// has latched an error.
+// has latched a timeout (the pipeline it belongs to is broken).  A latched
+// abort does not end waits: every kernel of the launch runs to completion.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t lim = wait_limit_ns(status);
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > VLA_WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > lim) {
       latch_error(status, VLA_DEV_TIMEOUT);
       return false;
     }
-    if (status && *(volatile int*)status != 0) return false;
+    if (status && *(volatile int*)status == VLA_DEV_TIMEOUT) return false;
   }
 }
 
@@ -592,6 +601,8 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
 // build; bf16 weights, TMA'd tokens with a 64 x BN box, KS = K), BN in
 // {64, 128, 192, 256}, N a multiple of 128.
 size_t linear_wide_smem_bytes(int BN);
+// GeLU by erff and by the many-token epilogue's approximation, elementwise.
+cudaError_t launch_gelu_forms(const float* x, int n, float* exact, float* fast, cudaStream_t st);
 cudaError_t linear_wide_init();
 cudaError_t launch_linear_wide(const CUtensorMap* tmA, const CUtensorMap* tmB, const LinArgs& g, int grid,
                                cudaStream_t st);
@@ -696,8 +707,13 @@ cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, 
 // W2A8 row quantisers (Eq. 4): bf16 carriers of the int8 codes [T][K] and
 // alpha [T].  quant_norm quantises the modulated RMSNorm of h (computing the
 // row's rms itself); quant_rows quantises fp32 rows x [T][K].
+// u_out (nullable): the fp32 modulated rows that were quantised [T][D].
 cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* gamma, const float* beta, bf16* codes,
-                              float* alpha, cudaStream_t st);
+                              float* alpha, float* u_out, cudaStream_t st);
 cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st);
+// The same quantiser writing int8 codes (the standalone Eq. (4) entry point).
+cudaError_t launch_quant_rows_i8(int T, int K, const float* x, int8_t* codes, float* alpha, cudaStream_t st);
+// One kernel whose bounded wait cannot be satisfied (exercises the timeout latch).
+cudaError_t launch_expire_wait(int* status, cudaStream_t st);
 cudaError_t launch_i8_to_bf16(const int8_t* a, bf16* out, size_t n, cudaStream_t st);
 

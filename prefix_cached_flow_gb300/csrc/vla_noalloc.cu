@@ -25,7 +25,10 @@ static __device__ __align__(256) float g_noalloc_scratch[VLA_NOALLOC_MAX_ELEMS];
 
 // Device address of g_noalloc_scratch per device ordinal.  In host code the
 // array's name is only a host-side stand-in, never a device address, so the
-// address is looked up once per device with that device current.
+// address is looked up once per device with that device current.  The cached
+// address belongs to the device context that was current at the lookup: a
+// caller that resets the device (cudaDeviceReset) must not call this entry
+// point on that device again in the same process.
 constexpr int kMaxDevices = 64;
 float* g_scratch_dev[kMaxDevices] = {};
 std::mutex g_scratch_mu;
@@ -51,7 +54,11 @@ cudaError_t noalloc_scratch(float** out) {
 extern "C" vla_status vla_w2a8_ternary_gemm_noalloc(const int8_t* a, const float* alpha, const uint8_t* q,
                                                     float beta, int M, int N, int K, uint16_t* y, int32_t* acc,
                                                     void* stream) {
-  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64) return VLA_ERR_INVALID_ARG;
+  // Same contract as vla_w2a8_ternary_gemm, plus: the product kernel reads the
+  // codes as 32-bit words, so `a` must be 4-byte aligned.
+  if (!a || !alpha || !q || !y || M < 1 || N < 1 || K < 64 || K % 64 || K > 65536 || N % 4 ||
+      ((uintptr_t)a & 3u))
+    return VLA_ERR_INVALID_ARG;
   if ((size_t)M * (size_t)N > (size_t)VLA_NOALLOC_MAX_ELEMS) return VLA_ERR_UNSUPPORTED;
   float* part = nullptr;
   cudaError_t e = noalloc_scratch(&part);

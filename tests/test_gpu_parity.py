@@ -175,3 +175,32 @@ def test_w2a8_zero_ternary_wiring_exact():
                        w["wout"])
         assert O.parity_metrics(run["tap"][k], ref)["e_inf"] <= 1e-4
         x = (x + np.float32(tau[k + 1] - tau[k]) * run["tap"][k]).astype(np.float32)
+
+
+@pytest.mark.parametrize("S", [1, 2, 16])
+def test_full_bf16_b1_solver_lengths(S):
+    """Solver lengths of the Eq. (3) sweep other than the workload's S = 10."""
+    _check(gpu_run(CONFIGS["full_bf16_b1"].replace(S=S)), obs=[0])
+
+
+def test_w2a8_b16_free_running_chunk():
+    _check(gpu_run(CONFIGS["w2a8_b16"]), obs=[7], free_running=True)
+
+
+def test_policy_step_host_matches_oracle():
+    """The host-buffer request call (the call behind the end-to-end number):
+    H2D copies, prefix build, solve and D2H in one call."""
+    import torch
+    import oracle as O
+    cfg = CONFIGS["full_bf16_b1"]
+    run = gpu_run(cfg)
+    ex = run["expert"]
+    Zh = torch.from_numpy(run["Z"]).to(torch.bfloat16).pin_memory()
+    nh = torch.from_numpy(run["noise"]).pin_memory()
+    ah = torch.empty_like(nh).pin_memory()
+    ex.policy_step_host(Zh, nh, ah)
+    Kc, Vc = O.prefix_kv(run["Z"].astype(np.float64), run["w"], cfg)
+    xr, _ = O.denoise(run["noise"].astype(np.float64), Kc, Vc, run["w"], cfg)
+    assert O.parity_metrics(ah.numpy(), xr)["e_inf"] <= GATES["bf16"][1]
+    # the same request through the device-pointer calls gives the same chunk bit for bit
+    assert np.array_equal(ah.numpy(), run["act"])

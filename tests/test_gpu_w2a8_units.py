@@ -64,3 +64,19 @@ def test_ternary_gemm_extreme_accumulator():
                             torch.from_numpy(packed).cuda(), 1.0)
     acc = acc.cpu().numpy()
     assert np.all(acc[0] == 127 * K) and np.all(acc[1] == -127 * K)
+
+
+def test_gelu_forms_within_bound():
+    """The many-token epilogue's GeLU (erf by Abramowitz & Stegun 7.1.26,
+    |erf error| <= 1.5e-7, approximate reciprocal and exponential) against
+    the erff form and the fp64 definition: |error| <= 4e-7 (1 + |x|)."""
+    import torch
+    import prefix_cached_flow_gb300 as V
+    x = np.concatenate([np.linspace(-12, 12, 200001), np.random.default_rng(5).standard_normal(100000) * 3])
+    x = x.astype(np.float32)
+    exact, fast = V.gelu_forms(torch.from_numpy(x).cuda())
+    exact, fast = exact.cpu().numpy().astype(np.float64), fast.cpu().numpy().astype(np.float64)
+    ref = O.gelu(x.astype(np.float64))
+    bound = 4e-7 * (1 + np.abs(x))
+    assert np.all(np.abs(fast - ref) <= bound)
+    assert np.all(np.abs(exact - ref) <= 2e-7 * (1 + np.abs(x)))

@@ -367,6 +367,88 @@ def test_w2a8_zero_ternary_weights_leave_residual_stream():
     np.testing.assert_allclose(v, ref, rtol=0, atol=1e-13)
 
 
+def _torch_unpack_ternary(packed):
+    """2-bit fields (code q+1, little-endian in the byte) -> int64 q, in torch."""
+    p = torch.from_numpy(np.asarray(packed)).to(torch.int64)
+    f = torch.stack([(p >> (2 * i)) & 3 for i in range(4)], dim=-1)
+    return f.reshape(*p.shape[:-1], p.shape[-1] * 4) - 1
+
+
+def _torch_w2a8_map(u, packed, beta):
+    """Eq. (4) written with torch routines: per-row absmax scale (fp32 IEEE
+    division), round-half-to-even codes, an exact integer product (fp64 sums
+    of small integers), (acc * alpha) * beta in fp32, then bf16 round-to-
+    nearest-even by torch's conversion; returned as fp64."""
+    u32 = u.to(torch.float32)
+    alpha = torch.clamp(u32.abs().amax(dim=-1, keepdim=True), min=1e-5) / torch.tensor(127.0, dtype=torch.float32)
+    a = torch.clamp(torch.round(u32 / alpha), -128, 127)
+    q = _torch_unpack_ternary(packed).to(torch.float64)
+    acc = a.to(torch.float64) @ q.transpose(0, 1)
+    y = (acc.to(torch.float32) * alpha) * torch.tensor(float(beta), dtype=torch.float32)
+    return y.to(torch.bfloat16).to(torch.float64)
+
+
+def _torch_velocity_w2a8(x, tau, Kc, Vc, w, cfg):
+    """The W2A8 velocity network with torch library routines (fp64 outside
+    Eq. 4): every per-layer map replaced by its own quantised product, Q, K
+    and V quantising the same normalised rows, the O-projection quantising the
+    attention output and W_down the GeLU output."""
+    T = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    e = T(O.sinusoidal_time_embedding(tau, cfg.d_t))
+    sc = tF.silu(tF.linear(tF.silu(tF.linear(e, T(w["wt1"]))), T(w["wt2"])))
+    h = tF.linear(T(x), T(w["win"]))
+    B, H, _ = x.shape
+    lin = lambda u, name, l: _torch_w2a8_map(u.reshape(B * H, -1), w[name][l], w["beta_" + name][l]).view(B, H, -1)
+    for l in range(cfg.L):
+        ga, ba, gm, bm = tF.linear(sc, T(w["wmod"][l])).view(4, cfg.D)
+        u = tF.rms_norm(h, (cfg.D,), eps=cfg.eps) * (1 + ga) + ba
+        q = lin(u, "wq", l).view(B, H, cfg.n_q, cfg.d_h).transpose(1, 2)
+        k = lin(u, "wk", l).view(B, H, cfg.n_kv, cfg.d_h).transpose(1, 2)
+        v = lin(u, "wv", l).view(B, H, cfg.n_kv, cfg.d_h).transpose(1, 2)
+        k = torch.cat([T(Kc[l]), k], dim=2)
+        v = torch.cat([T(Vc[l]), v], dim=2)
+        o = tF.scaled_dot_product_attention(q, k, v, enable_gqa=True).transpose(1, 2).reshape(B, H, -1)
+        h = h + lin(o, "wo", l)
+        u = tF.rms_norm(h, (cfg.D,), eps=cfg.eps) * (1 + gm) + bm
+        h = h + lin(tF.gelu(lin(u, "wup", l)), "wdown", l)
+    gf, bf = tF.linear(sc, T(w["wmod_f"])).view(2, cfg.D)
+    return tF.linear(tF.rms_norm(h, (cfg.D,), eps=cfg.eps) * (1 + gf) + bf, T(w["wout"])).numpy()
+
+
+def test_w2a8_velocity_vs_library_routines():
+    """velocity_w2a8 with non-zero ternary maps and six distinct scales per
+    layer against an independent torch restatement: a swapped scale, the
+    GeLU input quantised instead of its output, or Q's codes reused for the
+    O-projection would each change the result."""
+    cfg = PIN.replace(w2a8=True, dtype="bf16", L=2)
+    w = make_weights(cfg)
+    for l in range(cfg.L):
+        betas = [float(w["beta_" + n][l]) for n in ("wq", "wk", "wv", "wo", "wup", "wdown")]
+        assert len(set(betas)) == 6
+    Z, noise = make_observations(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    for tau in (0.0, 1.0 / 3.0, 0.75):
+        v = O.velocity_w2a8(noise, tau, Kc, Vc, w, cfg)
+        ref = _torch_velocity_w2a8(noise.astype(np.float64), tau, Kc, Vc, w, cfg)
+        assert np.max(np.abs(v)) > 0.1
+        np.testing.assert_allclose(v, ref, rtol=0, atol=1e-9)
+
+
+def test_w2a8_velocity_detects_swapped_scales():
+    """The restatement above is sensitive to the scale wiring: exchanging the
+    W_k and W_v scales of one layer moves the velocity by far more than the
+    tolerance used there."""
+    cfg = PIN.replace(w2a8=True, dtype="bf16", L=2)
+    w = make_weights(cfg)
+    Z, noise = make_observations(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    v = O.velocity_w2a8(noise, 0.5, Kc, Vc, w, cfg)
+    w2 = dict(w)
+    w2["beta_wk"], w2["beta_wv"] = w["beta_wv"].copy(), w["beta_wk"].copy()
+    v2 = O.velocity_w2a8(noise, 0.5, Kc, Vc, w2, cfg)
+    assert np.max(np.abs(v - v2)) > 1e-6
+
+
 def test_w2a8_linear_is_eq4_of_rows():
     """One W2A8 map on a batch of rows == Eq. 4 applied row by row."""
     cfg = PIN.replace(w2a8=True, dtype="bf16")
