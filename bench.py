@@ -203,6 +203,251 @@ def config_dict(cfg, ws=1):
 def roofline(cfg, denoise_ms, traffic=None):
     """Roofline of the solver launch: algorithmic bytes (or tensor FLOP) of
     the S steps over its measured time, against the measured peak."""
+    hbm, tflops, tflops_sus, src = _peaks()
+    solver_bytes = cfg.S * algorithmic_bytes_per_step(cfg)
+    solver_flops = cfg.S * algorithmic_flops_per_step(cfg)
+    # The solver launch runs for milliseconds back to back: the sustained
+    # tensor peak applies to it.  Bound = whichever roof takes longer.
+    if solver_flops / (tflops_sus * 1e12) > solver_bytes / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": solver_flops / (denoise_ms * 1e-3) / 1e12, "peak": tflops_sus,
+                "unit": "TFLOP/s", "algorithmic_flops_per_launch": solver_flops,
+                "peak_note": "bf16 sustained"}
+    else:
+        roof = {"bound": "hbm", "achieved": solver_bytes / (denoise_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": traffic, "algorithmic_bytes_per_launch": solver_bytes, "peak_source": src})
+    return roof
+
+
+def prefix_roofline(cfg, prefix_ms):
+    """The prefix K/V build (one GEMM over every layer): tensor-bound."""
+    _, tflops, _, src = _peaks()
+    flops = 2.0 * cfg.B * cfg.P * cfg.d_vlm * cfg.L * 2 * cfg.kvdim
+    ach = flops / (prefix_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": tflops, "unit": "TFLOP/s", "frac": ach / tflops,
+            "algorithmic_flops_per_launch": flops, "peak_note": "bf16 burst", "peak_source": src}
+
+
+def time_request(ex, Zt, Kc, Vc, nt, act, steps, flush, stream):
+    """CUDA-event times (ms) of the prefix build and the solve, per step, with
+    an L2 flush between timed steps (outside the events)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.random_(0, 255)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        ex.prefix_kv_build(Zt, Kc, Vc)
+        e1.record(stream)
+        ex.denoise(Kc, Vc, nt, act)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    prefix_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    denoise_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    return prefix_ms, denoise_ms
+
+
+def sub_workload(name, steps, flush, stream):
+    """Device-timed numbers of one more workload (same method as the main line)."""
+    import torch
+
+    import prefix_cached_flow_gb300 as V
+    cfg = CONFIGS[name]
+    w = make_weights(cfg)
+    Z, noise = make_observations(cfg, cfg.B)
+    ex = V.Expert(cfg, V.upload_weights(w, cfg.dtype, cfg.w2a8), max_batch=cfg.B, max_prefix=cfg.P)
+    del w
+    dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    Zt = torch.from_numpy(Z).to(dt).cuda()
+    nt = torch.from_numpy(noise).cuda()
+    act = torch.empty_like(nt)
+    Kc, Vc = ex.alloc_cache(cfg.B, cfg.P)
+    for _ in range(3):
+        ex.prefix_kv_build(Zt, Kc, Vc)
+        ex.denoise(Kc, Vc, nt, act)
+    torch.cuda.synchronize()
+    prefix_ms, denoise_ms = time_request(ex, Zt, Kc, Vc, nt, act, steps, flush, stream)
+    status = ex.poll_status()
+    out = {"config": config_dict(cfg), "value": cfg.B / ((prefix_ms + denoise_ms) * 1e-3), "unit": "chunks/s",
+           "ms_per_request": prefix_ms + denoise_ms, "prefix_build_ms": prefix_ms, "denoise_ms": denoise_ms,
+           "us_per_solver_step": denoise_ms * 1e3 / cfg.S, "roofline": roofline(cfg, denoise_ms),
+           "prefix_roofline": prefix_roofline(cfg, prefix_ms),
+           "gpu_launches_per_request": 1 + ex.launch_count(cfg.B, cfg.P), "steps": steps,
+           "device_status": status}
+    ex.close()
+    return out
+
+
+def cpu_oracle_chunk(cfg, w, Z, noise):
+    import oracle as O
+    Kc, Vc = O.prefix_kv(Z.astype(np.float64), w, cfg)
+    if cfg.w2a8:
+        return O.denoise_w2a8(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
+    return O.denoise(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
+
+
+def cpu_baseline(cfg, w, Z, noise, budget_s=10.0):
+    """Oracle throughput on the host cores on a bounded sample: whole chunks
+    of observation 0, repeated until ~budget_s of CPU work."""
+    c1 = cfg.replace(B=1)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        cpu_oracle_chunk(c1, w, Z[:1], noise[:1])
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    mean = sum(times) / len(times)
+    return {"value": 1.0 / mean, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(times)} whole chunk(s) (prefix K/V + {cfg.S} Euler steps) of observation 0 of "
+                      f"{cfg.name}, fp64 numpy/OpenBLAS, {mean * 1e3:.0f} ms per chunk"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    cfg = CONFIGS[args.workload]
+    w = make_weights(cfg)
+    if cfg.w2a8:
+        import oracle as O
+        w = O.with_unpacked(w)
+    Z, noise = make_observations(cfg, 1)
+    c1 = cfg.replace(B=1)
+    for _ in range(args.warmup):
+        cpu_oracle_chunk(c1, w, Z, noise)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_chunk(c1, w, Z, noise)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 1.0 / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "chunks/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(config_dict(cfg.replace(B=1)), note="one observation per step"),
+        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.steps} whole chunks of observation 0 of {cfg.name} (prefix K/V + "
+                                   f"{cfg.S} Euler steps), fp64 numpy/OpenBLAS"},
+        "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def eq3_sweep(cfg, dev_w, Zt, nt, steps=(1, 2, 4, 8, 16), reps=20):
+    """Solver-step sweep of the latency model L(T) = P + T E ("vla.cpp", §III-B
+    Eq. (3)): P = prefix K/V build, E = one Euler step, fitted by least squares
+    over T, and the speedup over recomputing the conditioning every step,
+    T (P + E) / (P + T E)."""
+    import torch
+
+    import prefix_cached_flow_gb300 as V
+    rows = []
+    for S in steps:
+        ex = V.Expert(cfg, dev_w, max_batch=cfg.B, max_prefix=cfg.P, n_steps=S)
+        Kc, Vc = ex.alloc_cache(cfg.B, cfg.P)
+        act = torch.empty_like(nt)
+        for _ in range(3):
+            ex.prefix_kv_build(Zt, Kc, Vc)
+            ex.denoise(Kc, Vc, nt, act)
+        torch.cuda.synchronize()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        tp = td = 0.0
+        for _ in range(reps):
+            e[0].record()
+            ex.prefix_kv_build(Zt, Kc, Vc)
+            e[1].record()
+            ex.denoise(Kc, Vc, nt, act)
+            e[2].record()
+            torch.cuda.synchronize()
+            tp += e[0].elapsed_time(e[1])
+            td += e[1].elapsed_time(e[2])
+        rows.append((S, tp / reps, td / reps))
+        ex.close()
+    Ts = np.array([r[0] for r in rows], dtype=np.float64)
+    L = np.array([r[1] + r[2] for r in rows])
+    A = np.stack([np.ones_like(Ts), Ts], axis=1)
+    (P_fit, E_fit), *_ = np.linalg.lstsq(A, L, rcond=None)
+    P_meas = float(np.mean([r[1] for r in rows]))
+    return {
+        "T": [int(t) for t in Ts], "prefix_ms": [round(r[1], 4) for r in rows],
+        "solve_ms": [round(r[2], 4) for r in rows], "fit_P_ms": float(P_fit), "fit_E_ms": float(E_fit),
+        "prefix_ms_measured": P_meas,
+        "speedup_vs_recompute": [float(t * (P_meas + E_fit) / (P_meas + t * E_fit)) for t in Ts],
+    }
+
+
+def run_ours(args):
+    import torch
+
+    import prefix_cached_flow_gb300 as V
+
+    ws, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if not os.path.exists(V.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    cfg = CONFIGS[args.workload]
+    B = cfg.B
+    w = make_weights(cfg)
+    Z, noise = make_observations(cfg.replace(seed=replica_seed(cfg.seed, rank)), B)
+    ex = V.Expert(cfg, V.upload_weights(w, cfg.dtype, cfg.w2a8), max_batch=B, max_prefix=cfg.P)
+    dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    Zt = torch.from_numpy(Z).to(dt).cuda()
+    nt = torch.from_numpy(noise).cuda()
+    act = torch.empty_like(nt)
+    Kc, Vc = ex.alloc_cache(B, cfg.P)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ex.prefix_kv_build(Zt, Kc, Vc)
+        ex.denoise(Kc, Vc, nt, act)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert ex.poll_status() == 0
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    prefix_ms, denoise_ms = time_request(ex, Zt, Kc, Vc, nt, act, args.steps, flush, stream)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = ex.poll_status()
+    step_ms = prefix_ms + denoise_ms
+    step_ms, prefix_ms, denoise_ms = max_over_ranks(dist, [step_ms, prefix_ms, denoise_ms], "cuda")
+
+    # End to end through the public host-buffer call: H2D of Z and noise, the
+    # whole request, D2H of the chunk, every step.
+    Zh = torch.from_numpy(Z).to(dt).pin_memory()
+    nh = torch.from_numpy(noise).pin_memory()
+    ah = torch.empty_like(nh).pin_memory()
+    for _ in range(3):
+        ex.policy_step_host(Zh, nh, ah)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ex.policy_step_host(Zh, nh, ah)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    (e2e_ms,) = max_over_ranks(dist, [e2e_ms], "cuda")
+
     roof = roofline(cfg, denoise_ms, _traffic_from_profile(cfg.name))
     roof["kernel"] = "solver launch (all S steps)"
     launches = args.steps * (1 + ex.launch_count(B, cfg.P))

@@ -105,6 +105,18 @@ struct vla_expert {
   cudaStream_t cap_stream = nullptr;
   std::vector<GraphEntry> graphs;
   uint64_t tick = 0;
+  // persistent whole-solve kernel for few tokens (k_solver_persist.cu)
+  bool persist_ok = false;
+  int persist_T = 0;         // tokens its buffers hold
+  float* cqkv = nullptr;     // [S][L][qkvdim]  W_qkv beta_a per (step, layer)
+  float* cup = nullptr;      // [S][L][F]       W_up beta_m
+  float* p_accq = nullptr;
+  float* p_accu = nullptr;
+  float* p_rms = nullptr;
+  bf16* p_opart = nullptr;
+  float2* p_oml = nullptr;
+  unsigned* p_bar = nullptr;
+  size_t p_units = 0;
   // diagnostic tap of one W2A8 solver step (vla_expert_set_w2a8_tap)
   void* tap = nullptr;
   size_t tap_cap = 0;
@@ -653,6 +665,62 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
   return VLA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Persistent whole-solve path (few tokens, bf16)
+// ---------------------------------------------------------------------------
+constexpr int kPersistMaxT = 64;
+
+// Fills the per-call arguments; false when this (B, P) does not fit the
+// persistent kernel's limits (B tiles per phase, TMEM columns, tokens).
+bool persist_plan(const vla_expert* h, int B, int P, PersistArgs* pa) {
+  const vla_expert_config& c = h->cfg;
+  const int T = B * c.horizon, G = h->num_sms;
+  if (!h->persist_ok || T > h->persist_T || T > G) return false;
+  PersistArgs a{};
+  a.L = c.n_layers; a.D = c.width; a.F = c.mlp_width; a.S = h->S; a.T = T; a.BN = round_up(T, 16);
+  a.B = B; a.H = c.horizon; a.P = P; a.d_a = c.action_dim; a.d_h = c.head_dim; a.n_kv = c.n_kv_heads;
+  a.group = c.n_q_heads / c.n_kv_heads; a.qdim = h->qdim; a.kvdim = h->kvdim; a.qkvdim = h->qkvdim;
+  a.nqt = cdiv(a.group * c.horizon, 128);
+  a.nch = cdiv(P + c.horizon, 128);
+  a.att_units = B * c.n_kv_heads * a.nqt * a.nch;
+  if ((size_t)a.att_units > h->p_units) return false;
+  const int NK[4][2] = {{h->qkvdim, c.width}, {c.width, h->qdim}, {c.mlp_width, c.width}, {c.width, c.mlp_width}};
+  for (int ph = 0; ph < 4; ++ph) {
+    a.N[ph] = NK[ph][0];
+    a.nkb[ph] = NK[ph][1] / 64;
+    a.U[ph] = (NK[ph][0] / 128) * a.nkb[ph];
+    for (int cta = 0; cta < G; ++cta) {  // limits of every CTA's unit range
+      const int u0 = (int)((long)a.U[ph] * cta / G), u1 = (int)((long)a.U[ph] * (cta + 1) / G);
+      if (u1 <= u0) continue;
+      const int len = u1 - u0, ntiles = len < a.nkb[ph] ? len : a.nkb[ph];
+      const int nseg = (u1 - 1) / a.nkb[ph] - u0 / a.nkb[ph] + 1;
+      if (ntiles > 4 || nseg * a.BN > 256) return false;
+    }
+  }
+  a.eps = c.rms_eps;
+  a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+  a.win = h->win; a.wout = h->wout; a.modtab = h->modtab; a.modf = h->modf; a.cqkv = h->cqkv; a.cup = h->cup;
+  a.h = h->h; a.accq = h->p_accq; a.accu = h->p_accu; a.rms = h->p_rms; a.opart = h->p_opart; a.oml = h->p_oml;
+  a.bar = h->p_bar; a.stop = (int*)(h->p_bar + 1); a.status = h->d_status; a.abort = h->d_abort;
+  *pa = a;
+  return true;
+}
+
+vla_status enqueue_persist(vla_expert* h, const void* kc, const void* vc, const PersistArgs& base, const float* noise,
+                           float* actions, float* tap, cudaStream_t st) {
+  const vla_expert_config& c = h->cfg;
+  PersistArgs a = base;
+  a.noise = noise; a.actions = actions; a.vtap = tap;
+  const int dh = c.head_dim, nkv = c.n_kv_heads, L = c.n_layers, P = a.P, B = a.B, P8 = round_up(P, 8);
+  CUtensorMap tmW[4] = {h->tm_wqkv, h->tm_wo, h->tm_wup, h->tm_wdown};
+  CUtensorMap tmK, tmVt;
+  if (tc_encode_3d_bf16(&tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, 128) ||
+      tc_encode_3d_bf16(&tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh))
+    return VLA_ERR_CUDA;
+  VLA_CK(launch_persist(tmW, &tmK, &tmVt, a, h->num_sms, st));
+  return VLA_OK;
+}
+
 vla_status validate_config(const vla_expert_config* c, int n_steps, bool w2a8) {
   if (!c || n_steps < 1) return VLA_ERR_INVALID_ARG;
   if (c->n_layers < 1 || c->width < 1 || c->mlp_width < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
@@ -832,6 +900,44 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
       if (tc_encode_2d_bf16(&h->tm_wdown, h->wdown, c.mlp_width, (uint64_t)L * D, 64, 128)) return VLA_ERR_CUDA;
     }
   }
+  // persistent few-token solver: W beta vectors, accumulators, attention partials
+  const int dh = c.head_dim;
+  if (h->fused && !h->w2a8 && !h->f32 && !(c.flags & VLA_FLAG_NO_PERSIST) && (dh == 64 || dh == 128 || dh == 256) &&
+      D % 128 == 0 && c.mlp_width % 128 == 0 && h->qkvdim % 128 == 0 && h->qdim % 64 == 0 && c.action_dim <= 64 &&
+      persist_ring_stages(D) >= 4 && persist_smem_bytes(D) <= 227 * 1024) {
+    int occ = 0;
+    VLA_CK(persist_init());
+    VLA_CK(persist_blocks_per_sm(D, &occ));
+    const int Tp = occ >= 1 ? (Tm < kPersistMaxT ? Tm : kPersistMaxT) : 0;
+    const int F = c.mlp_width;
+    const int Bmax = Tp / c.horizon;
+    if (Bmax >= 1) {
+      h->persist_T = Tp;
+      const int group = c.n_q_heads / c.n_kv_heads;
+      h->p_units = (size_t)Bmax * c.n_kv_heads * cdiv(group * c.horizon, 128) * cdiv(c.max_prefix + c.horizon, 128);
+      if ((s = dalloc(&h->cqkv, (size_t)S * L * h->qkvdim * 4)) != VLA_OK) return s;
+      if ((s = dalloc(&h->cup, (size_t)S * L * F * 4)) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_accq, (size_t)Tp * h->qkvdim * 4)) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_accu, (size_t)Tp * F * 4)) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_rms, (size_t)2 * Tp * 4)) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_opart, h->p_units * 128 * dh * 2)) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_oml, h->p_units * 128 * sizeof(float2))) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_bar, 64)) != VLA_OK) return s;
+      VLA_CK(cudaMemset(h->p_bar, 0, 64));
+      // W beta for every (step, layer): the beta half of the factored modulated norm
+      for (int l = 0; l < L && err == cudaSuccess; ++l) {
+        err = launch_gemm_simt(0, h->modtab + ((size_t)l * 4 + 1) * D, L * 4 * D, 1,
+                               (const char*)h->wqkv + (size_t)l * h->qkvdim * D * 2, D, S, h->qkvdim, D, 1,
+                               h->cqkv + (size_t)l * h->qkvdim, 0, L * h->qkvdim, nullptr, st);
+        if (err == cudaSuccess)
+          err = launch_gemm_simt(0, h->modtab + ((size_t)l * 4 + 3) * D, L * 4 * D, 1,
+                                 (const char*)h->wup + (size_t)l * F * D * 2, D, S, F, D, 1, h->cup + (size_t)l * F, 0,
+                                 L * F, nullptr, st);
+      }
+      VLA_CK(err);
+      h->persist_ok = true;
+    }
+  }
   VLA_CK(cudaStreamSynchronize(st));
   return VLA_OK;
 }
@@ -881,7 +987,8 @@ void vla_expert_destroy(vla_expert* h) {
   void* ptrs[] = {h->wkv_pre, h->wqkv, h->wo,   h->wup,   h->wdown, h->beta,  h->win,     h->wout,
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
-                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf};
+                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf,
+                  h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -1057,6 +1164,12 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
     return VLA_ERR_INVALID_ARG;
   if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  // Few tokens (bf16): the whole solve is one persistent kernel launch.
+  PersistArgs pa;
+  if (!w2a8 && !h->tap && !(h->cfg.flags & (VLA_FLAG_SIMT_GEMM | VLA_FLAG_ATTN_SPLIT | VLA_FLAG_ATTN_STREAM |
+                                            VLA_FLAG_LINEAR_SPLIT | VLA_FLAG_LINEAR_WIDE)) &&
+      persist_plan(h, B, P, &pa))
+    return enqueue_persist(h, Kc, Vc, pa, noise, actions, tap, st);
   auto enqueue = [&](cudaStream_t s2) {
     if (h->fused)
       return h->w2a8 ? enqueue_denoise_w2a8_fused(h, Kc, Vc, B, P, noise, actions, tap, s2)
@@ -1109,6 +1222,13 @@ vla_status vla_action_denoise_w2a8(vla_expert* h, const void* Kc, const void* Vc
 
 vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kernels) {
   if (!h || !kernels || B < 1 || P < 1) return VLA_ERR_INVALID_ARG;
+  PersistArgs pa;
+  if (!(h->cfg.flags & (VLA_FLAG_SIMT_GEMM | VLA_FLAG_ATTN_SPLIT | VLA_FLAG_ATTN_STREAM | VLA_FLAG_LINEAR_SPLIT |
+                        VLA_FLAG_LINEAR_WIDE)) &&
+      persist_plan(h, B, P, &pa)) {
+    *kernels = 1;  // the persistent solve kernel
+    return VLA_OK;
+  }
   // per solver step: embed+norm, then per layer 4 GEMMs, reduce_qkv,
   // attention partials, attention combine, 2 residual/norm reductions (the
   // last layer's second one is the velocity head) and the GeLU reduction.

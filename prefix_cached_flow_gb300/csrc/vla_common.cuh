@@ -648,6 +648,43 @@ int tc_encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 int tc_encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
                       uint64_t stride2_bytes, uint32_t box0, uint32_t box1);
 
+// Persistent whole-solve kernel for few tokens (k_solver_persist.cu).
+struct PersistArgs {
+  int L, D, F, S, T, BN, B, H, P, d_a, d_h, n_kv, group, qdim, kvdim, qkvdim;
+  int nqt, nch, att_units;        // attention: query tiles per (b, g), key chunks, units
+  int U[4], nkb[4], N[4];         // linear phases (qkv, o, up, down): units, K blocks, rows
+  float eps, scale_log2;
+  const float* win;     // [D][d_a]
+  const float* wout;    // [d_a][D]
+  const float* modtab;  // [S][L][4][D]
+  const float* modf;    // [S][2][D]
+  const float* cqkv;    // [S][L][qkvdim]  W_qkv beta_a
+  const float* cup;     // [S][L][F]       W_up beta_m
+  const float* noise;   // [T][d_a]
+  float* actions;       // [T][d_a]
+  float* vtap;          // [S][T][d_a] or null
+  float* h;             // [T][D]
+  float* accq;          // [T][qkvdim]
+  float* accu;          // [T][F]
+  float* rms;           // [2][T]
+  bf16* opart;          // [att_units][128][d_h]
+  float2* oml;          // [att_units][128]
+  unsigned* bar;        // grid barrier counter; bar[1] is the stop word
+  int* stop;
+  int* status;
+  const volatile int* abort;
+};
+size_t persist_smem_bytes(int D);
+int persist_ring_stages(int D);
+cudaError_t persist_init();
+cudaError_t persist_blocks_per_sm(int D, int* n);
+// tmW[4]: bf16 weight maps (box 64 x 128) of [W_q;W_k;W_v], W_o, W_up, W_down;
+// tmK over K_C {d_h, P, L*B*n_kv} (box 64 x 128); tmVt over V_C^T {P, d_h,
+// L*B*n_kv} (box 64 x d_h).  Clears the barrier words, then one cooperative
+// launch of `grid` CTAs.
+cudaError_t launch_persist(const CUtensorMap* tmW, const CUtensorMap* tmK, const CUtensorMap* tmVt,
+                           const PersistArgs& a, int grid, cudaStream_t st);
+
 // Expert kernels (k_expert.cu).
 struct ExpertDims {
   int L, D, F, n_q, n_kv, d_h, d_a, H, B, P, S, d_t;

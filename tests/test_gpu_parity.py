@@ -32,12 +32,13 @@ def _kv_gate(cfg):
     return 1e-5 if cfg.dtype == "f32" else 2.0 ** -8 + 1e-3
 
 
-def _check(run, obs, free_running=True):
+def _check(run, obs, free_running=True, chunk_gate=None):
     cfg = run["cfg"]
     assert run["status"] == 0
     assert np.all(np.isfinite(run["act"])) and np.all(np.isfinite(run["tap"]))
     res = oracle_compare(run, obs=obs, free_running=free_running)
     g_v, g_x = _gates(cfg)
+    g_x = g_x if chunk_gate is None else chunk_gate
     print(cfg.name, "kv", res["kv"], "v_tf", res["v_tf"], "x", res["x"])
     assert max(res["kv"]) <= _kv_gate(cfg)
     assert max(res["v_tf"]) <= g_v
@@ -123,6 +124,18 @@ def test_small_bf16_many_tokens_ragged():
     _check(gpu_run(cfg, B=7, P=77), obs=[0, 6])
 
 
+def test_full_bf16_b1_per_kernel_graph():
+    """The per-kernel CUDA-graph solver at batch 1 (the default there is the
+    single persistent solve kernel)."""
+    import prefix_cached_flow_gb300 as V
+    _check(gpu_run(CONFIGS["full_bf16_b1"], flags=V.FLAG_NO_PERSIST), obs=[0])
+
+
+def test_full_bf16_b1_persistent_kernel_is_one_launch():
+    run = gpu_run(CONFIGS["full_bf16_b1"])
+    assert run["expert"].launch_count(1, CONFIGS["full_bf16_b1"].P) == 1
+
+
 def test_full_bf16_b1_wide_linear():
     import prefix_cached_flow_gb300 as V
     _check(gpu_run(CONFIGS["full_bf16_b1"], flags=V.FLAG_LINEAR_WIDE), obs=[0])
@@ -179,8 +192,14 @@ def test_w2a8_zero_ternary_wiring_exact():
 
 @pytest.mark.parametrize("S", [1, 2, 16])
 def test_full_bf16_b1_solver_lengths(S):
-    """Solver lengths of the Eq. (3) sweep other than the workload's S = 10."""
-    _check(gpu_run(CONFIGS["full_bf16_b1"].replace(S=S)), obs=[0])
+    """Solver lengths of the Eq. (3) sweep other than the workload's S = 10.
+    The chunk gate 1e-2 is stated for the workloads' own lengths (S >= 4),
+    where the chunk averages S velocity errors.  With S = 1 the chunk is
+    X^0 + v(X^0) (Eq. 1 with dt = 1), so its error IS one velocity error and
+    the per-step velocity gate (2e-2) is the applicable bound; S = 2 averages
+    two.  Longer solves keep the stated 1e-2."""
+    gate = {1: GATES["bf16"][0], 2: GATES["bf16"][0]}.get(S)
+    _check(gpu_run(CONFIGS["full_bf16_b1"].replace(S=S)), obs=[0], chunk_gate=gate)
 
 
 def test_w2a8_b16_free_running_chunk():
@@ -202,5 +221,7 @@ def test_policy_step_host_matches_oracle():
     Kc, Vc = O.prefix_kv(run["Z"].astype(np.float64), run["w"], cfg)
     xr, _ = O.denoise(run["noise"].astype(np.float64), Kc, Vc, run["w"], cfg)
     assert O.parity_metrics(ah.numpy(), xr)["e_inf"] <= GATES["bf16"][1]
-    # the same request through the device-pointer calls gives the same chunk bit for bit
-    assert np.array_equal(ah.numpy(), run["act"])
+    # the same request through the device-pointer calls: the same chunk up to
+    # the order of the fp32 split-K additions (the persistent solver adds its
+    # partial sums atomically)
+    assert np.max(np.abs(ah.numpy() - run["act"])) <= 2e-3
