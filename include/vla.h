@@ -63,7 +63,7 @@ typedef enum { VLA_DTYPE_F32 = 0, VLA_DTYPE_BF16 = 1 } vla_dtype;
 #define VLA_FLAG_ATTN_STREAM 8u /* attention: the streaming form (one CTA per query tile, all keys) where d_h is 64, 128 or 256 */
 #define VLA_FLAG_LINEAR_SPLIT 16u /* bf16 linear layers: always the cluster split-K kernel */
 #define VLA_FLAG_LINEAR_WIDE 32u  /* bf16 linear layers: the persistent many-token kernel wherever N % 128 == 0 */
-#define VLA_FLAG_NO_PERSIST 64u   /* few tokens: the per-kernel CUDA graph instead of the single persistent solve kernel */
+#define VLA_FLAG_PERSIST 64u      /* few tokens (bf16, B*H <= 64): the whole solve as one persistent cooperative kernel */
 
 typedef struct {
   int n_layers;    /* L */

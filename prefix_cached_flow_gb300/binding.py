@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "VLA_OK", 1: "VLA_ERR_INVALID_ARG", 2: "VLA_ERR_SHAPE", 3: "V
                 8: "VLA_ERR_NO_DEVICE"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 FLAG_SIMT_GEMM, FLAG_NO_GRAPH, FLAG_ATTN_SPLIT, FLAG_ATTN_STREAM = 1, 2, 4, 8
-FLAG_LINEAR_SPLIT, FLAG_LINEAR_WIDE, FLAG_NO_PERSIST = 16, 32, 64
+FLAG_LINEAR_SPLIT, FLAG_LINEAR_WIDE, FLAG_PERSIST = 16, 32, 64
 
 EXPORTED = ("vla_expert_create", "vla_expert_create_w2a8", "vla_expert_destroy", "vla_prefix_cache_bytes",
             "vla_prefix_kv_build", "vla_action_denoise", "vla_action_denoise_w2a8", "vla_policy_step_host",

@@ -675,32 +675,47 @@ constexpr int kPersistMaxT = 64;
 bool persist_plan(const vla_expert* h, int B, int P, PersistArgs* pa) {
   const vla_expert_config& c = h->cfg;
   const int T = B * c.horizon, G = h->num_sms;
-  if (!h->persist_ok || T > h->persist_T || T > G) return false;
+  if (!h->persist_ok || T > h->persist_T) return false;
   PersistArgs a{};
   a.L = c.n_layers; a.D = c.width; a.F = c.mlp_width; a.S = h->S; a.T = T; a.BN = round_up(T, 16);
-  a.B = B; a.H = c.horizon; a.P = P; a.d_a = c.action_dim; a.d_h = c.head_dim; a.n_kv = c.n_kv_heads;
+  a.B = B; a.H = c.horizon; a.Hp = h->Hp; a.P = P; a.d_a = c.action_dim; a.d_h = c.head_dim;
+  a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads;
   a.group = c.n_q_heads / c.n_kv_heads; a.qdim = h->qdim; a.kvdim = h->kvdim; a.qkvdim = h->qkvdim;
   a.nqt = cdiv(a.group * c.horizon, 128);
-  a.nch = cdiv(P + c.horizon, 128);
+  a.npch = cdiv(P, 128);
+  a.nch = a.npch + cdiv(c.horizon, 128);
   a.att_units = B * c.n_kv_heads * a.nqt * a.nch;
-  if ((size_t)a.att_units > h->p_units) return false;
+  if ((size_t)a.att_units > h->p_units || a.nch > 16) return false;
+  // attention CTAs: one per unit, at most a quarter of the SMs
+  a.n_att = a.att_units < G / 4 ? a.att_units : G / 4;
+  const int GL = G - a.n_att;
+  if (T > GL) return false;
   const int NK[4][2] = {{h->qkvdim, c.width}, {c.width, h->qdim}, {c.mlp_width, c.width}, {c.width, c.mlp_width}};
+  int work = 0;
   for (int ph = 0; ph < 4; ++ph) {
     a.N[ph] = NK[ph][0];
     a.nkb[ph] = NK[ph][1] / 64;
     a.U[ph] = (NK[ph][0] / 128) * a.nkb[ph];
-    for (int cta = 0; cta < G; ++cta) {  // limits of every CTA's unit range
-      const int u0 = (int)((long)a.U[ph] * cta / G), u1 = (int)((long)a.U[ph] * (cta + 1) / G);
+    for (int cta = 0; cta < GL; ++cta) {  // limits of every linear CTA's unit range
+      const int u0 = (int)((long)a.U[ph] * cta / GL), u1 = (int)((long)a.U[ph] * (cta + 1) / GL);
       if (u1 <= u0) continue;
       const int len = u1 - u0, ntiles = len < a.nkb[ph] ? len : a.nkb[ph];
       const int nseg = (u1 - 1) / a.nkb[ph] - u0 / a.nkb[ph] + 1;
-      if (ntiles > 4 || nseg * a.BN > 256) return false;
+      // TMEM columns of the segment accumulators; column constants in the head-row buffer
+      if (nseg * a.BN > 256 || ntiles > 5 || 6 * 64 > c.width) return false;
+      const int stg = ntiles * a.BN * 256 > nseg * a.BN * 512 ? ntiles * a.BN * 256 : nseg * a.BN * 512;
+      const int need = ntiles * a.BN * 128 + stg;
+      if (need > work) work = need;
     }
   }
+  a.work_bytes = work;
+  if (persist_ring_stages(c.width, work) < 4) return false;
   a.eps = c.rms_eps;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
   a.win = h->win; a.wout = h->wout; a.modtab = h->modtab; a.modf = h->modf; a.cqkv = h->cqkv; a.cup = h->cup;
-  a.h = h->h; a.accq = h->p_accq; a.accu = h->p_accu; a.rms = h->p_rms; a.opart = h->p_opart; a.oml = h->p_oml;
+  a.h = h->h; a.accq = h->p_accq; a.accu = h->p_accu; a.rms = h->p_rms;
+  a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vs = (bf16*)h->vs; a.o = (bf16*)h->act;
+  a.opart = h->p_opart; a.oml = h->p_oml;
   a.bar = h->p_bar; a.stop = (int*)(h->p_bar + 1); a.status = h->d_status; a.abort = h->d_abort;
   *pa = a;
   return true;
@@ -711,13 +726,27 @@ vla_status enqueue_persist(vla_expert* h, const void* kc, const void* vc, const 
   const vla_expert_config& c = h->cfg;
   PersistArgs a = base;
   a.noise = noise; a.actions = actions; a.vtap = tap;
+#ifdef VLA_PERSIST_TRACE
+  a.trace = h->tl;
+#endif
   const int dh = c.head_dim, nkv = c.n_kv_heads, L = c.n_layers, P = a.P, B = a.B, P8 = round_up(P, 8);
-  CUtensorMap tmW[4] = {h->tm_wqkv, h->tm_wo, h->tm_wup, h->tm_wdown};
-  CUtensorMap tmK, tmVt;
-  if (tc_encode_3d_bf16(&tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, 128) ||
-      tc_encode_3d_bf16(&tmVt, vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh))
+  CUtensorMap m[15];
+  m[0] = h->tm_wqkv; m[1] = h->tm_wo; m[2] = h->tm_wup; m[3] = h->tm_wdown;
+  if (tc_encode_3d_bf16(&m[4], kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64, 128) ||
+      tc_encode_3d_bf16(&m[5], vc, P, dh, (uint64_t)L * B * nkv, (uint64_t)P8 * 2, (uint64_t)dh * P8 * 2, 64, dh) ||
+      tc_encode_3d_bf16(&m[6], h->ks, dh, c.horizon, (uint64_t)B * nkv, (uint64_t)dh * 2,
+                        (uint64_t)c.horizon * dh * 2, 64, 128) ||
+      tc_encode_3d_bf16(&m[7], h->vs, c.horizon, dh, (uint64_t)B * nkv, (uint64_t)h->Hp * 2,
+                        (uint64_t)dh * h->Hp * 2, 64, dh) ||
+      tc_encode_2d_bf16(&m[8], h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
+      tc_encode_2d_f32(&m[9], h->h, c.width, a.T, 64, a.BN) ||
+      tc_encode_2d_f32(&m[10], h->p_accu, c.mlp_width, a.T, 64, a.BN) ||
+      tc_encode_2d_bf16(&m[11], h->act, h->qdim, a.T, 64, a.BN) ||
+      tc_encode_2d_f32(&m[12], h->p_accq, h->qkvdim, a.T, 128, a.T) ||
+      tc_encode_2d_f32(&m[13], h->h, c.width, a.T, 128, a.T) ||
+      tc_encode_2d_f32(&m[14], h->p_accu, c.mlp_width, a.T, 128, a.T))
     return VLA_ERR_CUDA;
-  VLA_CK(launch_persist(tmW, &tmK, &tmVt, a, h->num_sms, st));
+  VLA_CK(launch_persist(m, a, h->num_sms, st));
   return VLA_OK;
 }
 
@@ -763,7 +792,7 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   h->qkvdim = h->qdim + 2 * h->kvdim;
   h->Hp = round_up(cfg->horizon, 8);
   h->fused = fused_supported(*cfg, h->f32, w2a8, h->use_tc);
-#ifdef VLA_TIMELINE
+#if defined(VLA_TIMELINE) || defined(VLA_PERSIST_TRACE)
   VLA_CK(cudaMalloc((void**)&h->tl, (size_t)20 * 4096 * 16 * 8));
   VLA_CK(cudaMemset(h->tl, 0, (size_t)20 * 4096 * 16 * 8));
 #endif
@@ -902,9 +931,9 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
   }
   // persistent few-token solver: W beta vectors, accumulators, attention partials
   const int dh = c.head_dim;
-  if (h->fused && !h->w2a8 && !h->f32 && !(c.flags & VLA_FLAG_NO_PERSIST) && (dh == 64 || dh == 128 || dh == 256) &&
+  if (h->fused && !h->w2a8 && !h->f32 && (c.flags & VLA_FLAG_PERSIST) && (dh == 64 || dh == 128 || dh == 256) &&
       D % 128 == 0 && c.mlp_width % 128 == 0 && h->qkvdim % 128 == 0 && h->qdim % 64 == 0 && c.action_dim <= 64 &&
-      persist_ring_stages(D) >= 4 && persist_smem_bytes(D) <= 227 * 1024) {
+      persist_att_fits(dh) && persist_smem_bytes(D) <= 227 * 1024) {
     int occ = 0;
     VLA_CK(persist_init());
     VLA_CK(persist_blocks_per_sm(D, &occ));
@@ -914,12 +943,14 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
     if (Bmax >= 1) {
       h->persist_T = Tp;
       const int group = c.n_q_heads / c.n_kv_heads;
-      h->p_units = (size_t)Bmax * c.n_kv_heads * cdiv(group * c.horizon, 128) * cdiv(c.max_prefix + c.horizon, 128);
+      h->p_units = (size_t)Bmax * c.n_kv_heads * cdiv(group * c.horizon, 128) *
+                   (cdiv(c.max_prefix, 128) + cdiv(c.horizon, 128));
       if ((s = dalloc(&h->cqkv, (size_t)S * L * h->qkvdim * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->cup, (size_t)S * L * F * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_accq, (size_t)Tp * h->qkvdim * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_accu, (size_t)Tp * F * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_rms, (size_t)2 * Tp * 4)) != VLA_OK) return s;
+      // chunk partials [B*n_kv*nch][group*H] rows (at most 128 per unit)
       if ((s = dalloc(&h->p_opart, h->p_units * 128 * dh * 2)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_oml, h->p_units * 128 * sizeof(float2))) != VLA_OK) return s;
       if ((s = dalloc(&h->p_bar, 64)) != VLA_OK) return s;
@@ -972,7 +1003,7 @@ const char* vla_version(void) { return "0.1.0"; }
 
 const char* vla_last_error(void) { return g_last_error; }
 
-#ifdef VLA_TIMELINE
+#if defined(VLA_TIMELINE) || defined(VLA_PERSIST_TRACE)
 // Copies the event trace (20 slots x 4096 CTAs x 16 events, ns) to the host.
 int vla_debug_timeline(vla_expert* h, void* dst, size_t bytes) {
   if (!h || !h->tl || bytes > (size_t)20 * 4096 * 16 * 8) return 1;
@@ -1164,7 +1195,7 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
     return VLA_ERR_INVALID_ARG;
   if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
-  // Few tokens (bf16): the whole solve is one persistent kernel launch.
+  // Few tokens (bf16) with VLA_FLAG_PERSIST: the whole solve is one persistent kernel launch.
   PersistArgs pa;
   if (!w2a8 && !h->tap && !(h->cfg.flags & (VLA_FLAG_SIMT_GEMM | VLA_FLAG_ATTN_SPLIT | VLA_FLAG_ATTN_STREAM |
                                             VLA_FLAG_LINEAR_SPLIT | VLA_FLAG_LINEAR_WIDE)) &&

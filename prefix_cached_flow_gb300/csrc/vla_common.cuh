@@ -650,9 +650,11 @@ int tc_encode_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
 
 // Persistent whole-solve kernel for few tokens (k_solver_persist.cu).
 struct PersistArgs {
-  int L, D, F, S, T, BN, B, H, P, d_a, d_h, n_kv, group, qdim, kvdim, qkvdim;
-  int nqt, nch, att_units;        // attention: query tiles per (b, g), key chunks, units
+  int L, D, F, S, T, BN, B, H, Hp, P, d_a, d_h, n_q, n_kv, group, qdim, kvdim, qkvdim;
+  int n_att;                      // attention CTAs (the last n_att of the grid)
+  int nqt, npch, nch, att_units;  // query tiles per (b, g), cached-key chunks, all chunks, units
   int U[4], nkb[4], N[4];         // linear phases (qkv, o, up, down): units, K blocks, rows
+  int work_bytes;                 // linear CTAs' operand + staging region
   float eps, scale_log2;
   const float* win;     // [D][d_a]
   const float* wout;    // [d_a][D]
@@ -667,23 +669,31 @@ struct PersistArgs {
   float* accq;          // [T][qkvdim]
   float* accu;          // [T][F]
   float* rms;           // [2][T]
-  bf16* opart;          // [att_units][128][d_h]
-  float2* oml;          // [att_units][128]
+  bf16* q;              // [B][n_q][H][d_h]
+  bf16* ks;             // [B][n_kv][H][d_h]
+  bf16* vs;             // [B][n_kv][d_h][Hp]
+  bf16* o;              // [T][qdim]
+  bf16* opart;          // [B*n_kv*nch][group*H][d_h]
+  float2* oml;          // [B*n_kv*nch][group*H]
   unsigned* bar;        // grid barrier counter; bar[1] is the stop word
   int* stop;
   int* status;
   const volatile int* abort;
+  unsigned long long* trace;  // phase trace (-DVLA_PERSIST_TRACE builds), else unused
 };
 size_t persist_smem_bytes(int D);
-int persist_ring_stages(int D);
+int persist_ring_stages(int D, int work_bytes);
+bool persist_att_fits(int dh);
 cudaError_t persist_init();
 cudaError_t persist_blocks_per_sm(int D, int* n);
-// tmW[4]: bf16 weight maps (box 64 x 128) of [W_q;W_k;W_v], W_o, W_up, W_down;
-// tmK over K_C {d_h, P, L*B*n_kv} (box 64 x 128); tmVt over V_C^T {P, d_h,
-// L*B*n_kv} (box 64 x d_h).  Clears the barrier words, then one cooperative
-// launch of `grid` CTAs.
-cudaError_t launch_persist(const CUtensorMap* tmW, const CUtensorMap* tmK, const CUtensorMap* tmVt,
-                           const PersistArgs& a, int grid, cudaStream_t st);
+// maps[15]: bf16 weights [W_q;W_k;W_v], W_o, W_up, W_down (box 64 x 128);
+// K_C {d_h, P, L*B*n_kv} (box 64 x 128); V_C^T {P, d_h, L*B*n_kv} (box 64 x
+// d_h); k_s {d_h, H, B*n_kv} (box 64 x 128); v_s^T {H, d_h, B*n_kv} (box 64 x
+// d_h); q [B*n_q*H][d_h] (box 64 x 128); h and acc_up fp32 (box 64 x BN, no
+// swizzle); o bf16 (box 64 x BN); acc_qkv, h, acc_up fp32 (box 128 x BN, no
+// swizzle) for the reductions.  Clears the barrier words, then one
+// cooperative launch of `grid` CTAs.
+cudaError_t launch_persist(const CUtensorMap* maps, const PersistArgs& a, int grid, cudaStream_t st);
 
 // Expert kernels (k_expert.cu).
 struct ExpertDims {
