@@ -56,6 +56,12 @@ typedef enum {
 
 typedef enum { VLA_DTYPE_F32 = 0, VLA_DTYPE_BF16 = 1 } vla_dtype;
 
+/* Time convention of the solver schedule (§III-A): FORWARD integrates
+ * tau_k = k / S from 0 to 1 (GR00T); REVERSE integrates tau_k = 1 - k / S from
+ * 1 to 0 (SmolVLA, pi0): the network is evaluated at the reversed time and the
+ * velocity sign change enters Eq. (1) through tau_{k+1} - tau_k = -1/S. */
+typedef enum { VLA_SCHEDULE_FORWARD = 0, VLA_SCHEDULE_REVERSE = 1 } vla_schedule;
+
 /* Diagnostic flags for vla_expert_config.flags. */
 #define VLA_FLAG_SIMT_GEMM 1u  /* run bf16 GEMMs on the CUDA-core kernel instead of tcgen05 */
 #define VLA_FLAG_NO_GRAPH 2u   /* enqueue the solver kernels directly instead of one graph launch */
@@ -81,6 +87,7 @@ typedef struct {
   int dtype;       /* vla_dtype of weights, Z and the K/V cache (W2A8: BF16) */
   float rms_eps;   /* RMSNorm epsilon (1e-6) */
   unsigned flags;  /* VLA_FLAG_* (0 for normal use) */
+  int schedule;    /* vla_schedule */
 } vla_expert_config;
 
 /* Dense weights, device pointers of the config dtype, shapes [..][out][in]. */
@@ -131,7 +138,7 @@ typedef struct {
 typedef struct vla_expert vla_expert;
 
 /* Create an expert handle for a fixed solver length n_steps = S with the
- * uniform schedule tau_k = k / S (integration 0 -> 1, dt = 1/S).
+ * uniform schedule of cfg->schedule (tau_k = k / S, dt = 1/S; or reverse).
  * Copies and repacks the weights into handle-owned device memory (the caller
  * may free its copies once the call returns), precomputes the time
  * conditioning table for every tau_k, and allocates the workspace for
@@ -184,6 +191,42 @@ vla_status vla_action_denoise(vla_expert* h, const void* Kc_dev, const void* Vc_
 vla_status vla_action_denoise_w2a8(vla_expert* h, const void* Kc_dev, const void* Vc_dev, int B,
                                    int P, const float* noise_dev, float* actions_dev,
                                    float* vel_tap_dev, void* stream);
+
+/* Per-request options (§III-C: requests carry inputs plus optional noise and
+ * masks):
+ *   prefix_mask_dev  NULL (every cached key visible) or uint32 [B][(P+31)/32]
+ *                    device bits: bit p % 32 of word p / 32 of observation b
+ *                    set = prefix key p visible (M = 0 in Eq. 2), clear =
+ *                    hidden (M = -inf).  The action tokens' own keys are always
+ *                    visible, so every query row keeps at least one key.  4-byte
+ *                    aligned.  A per-observation prefix length P_b is the mask
+ *                    with bits [0, P_b) set.
+ *   noise_dev        X^0 [B][H][d_a] fp32, or NULL: the library draws X^0 ~ N(0, I)
+ *                    from `seed` (vla_noise_fill's stream) into a handle-owned
+ *                    buffer (allocated by the first such call)
+ *   seed             the Philox key when noise_dev is NULL
+ *   noise_out_dev    NULL, or [B][H][d_a] fp32 receiving the drawn X^0 */
+typedef struct {
+  const uint32_t* prefix_mask_dev;
+  const float* noise_dev;
+  unsigned long long seed;
+  float* noise_out_dev;
+} vla_request;
+
+/* Eq. 1 with the per-request options above; dense or W2A8 by the handle.
+ * Otherwise as vla_action_denoise (one graph launch per (B, P, pointers,
+ * mask)). */
+vla_status vla_action_denoise_ex(vla_expert* h, const void* Kc_dev, const void* Vc_dev, int B, int P,
+                                 const vla_request* req, float* actions_dev, float* vel_tap_dev, void* stream);
+
+/* n standard normals into out_dev (fp32): element e is normal (e mod 4) of
+ * Philox4x64-10 block e / 4 (Salmon et al., SC 2011) under key (seed, 0) and
+ * counter (e / 4, 0, 0, 0); words (x0, x1) and (x2, x3) of a block each give
+ * two normals by the Box-Muller transform in fp64:
+ * sqrt(-2 ln u1) (cos 2 pi u2, sin 2 pi u2), u1 = ((x0 >> 11) + 1) 2^-53,
+ * u2 = (x1 >> 11) 2^-53.  The noise the solver draws for a request is this
+ * stream over [B][H][d_a]. */
+vla_status vla_noise_fill(unsigned long long seed, size_t n, float* out_dev, void* stream);
 
 /* One whole request from host memory: copies Z and the noise to the device,
  * builds the prefix cache, runs the solver and copies X^S back, then

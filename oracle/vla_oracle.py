@@ -62,7 +62,7 @@ __all__ = [
     "time_conditioning", "prefix_kv", "joint_attention", "velocity", "schedule",
     "denoise", "denoise_recompute", "quantize_rows", "pack_ternary",
     "unpack_ternary", "bf16_rne", "ternary_linear", "velocity_w2a8", "with_unpacked",
-    "denoise_w2a8", "parity_metrics",
+    "denoise_w2a8", "parity_metrics", "philox4x64", "gaussian_noise", "prefix_mask_bits",
 ]
 
 
@@ -197,19 +197,29 @@ def velocity(x, tau, Kc, Vc, w: dict, cfg, taps=None, prefix_visible=None):
                    taps, prefix_visible)
 
 
-def schedule(S: int) -> np.ndarray:
-    """tau_0..tau_S = k / S (0 -> 1)."""
-    return np.arange(S + 1, dtype=F64) / S
+def schedule(S: int, reverse: bool = False) -> np.ndarray:
+    """tau_0..tau_S: k / S (integration 0 -> 1), or 1 - k / S when reverse.
+
+    The reverse convention (§III-A: 1 -> 0, as SmolVLA and pi0 integrate)
+    evaluates the network at the reversed time; its velocity sign change is
+    the negative step tau_{k+1} - tau_k = -1/S in Eq. (1)."""
+    k = np.arange(S + 1, dtype=F64)
+    return 1.0 - k / S if reverse else k / S
 
 
-def denoise(noise, Kc, Vc, w: dict, cfg, S: int | None = None, vel=velocity):
-    """Eq. (1) over S steps from X^0 = noise; returns (X^S, [v_0 .. v_{S-1}])."""
+def denoise(noise, Kc, Vc, w: dict, cfg, S: int | None = None, vel=velocity, reverse: bool | None = None,
+            prefix_visible=None):
+    """Eq. (1) over S steps from X^0 = noise; returns (X^S, [v_0 .. v_{S-1}]).
+
+    reverse defaults to the config's schedule; prefix_visible (bool [B, P])
+    hides prefix keys (M = -inf in Eq. 2)."""
     S = cfg.S if S is None else S
-    tau = schedule(S)
+    reverse = getattr(cfg, "reverse", False) if reverse is None else reverse
+    tau = schedule(S, reverse)
     x = np.asarray(noise, dtype=F64)
     vs = []
     for k in range(S):
-        v = vel(x, tau[k], Kc, Vc, w, cfg)
+        v = vel(x, tau[k], Kc, Vc, w, cfg, prefix_visible=prefix_visible)
         vs.append(v)
         x = x + (tau[k + 1] - tau[k]) * v
     return x, np.stack(vs)
@@ -219,7 +229,7 @@ def denoise_recompute(noise, Z, w: dict, cfg, S: int | None = None):
     """Eq. (1) with the conditioning K/V recomputed inside every solver step
     (the baseline that the prefix cache removes, §III-B Eq. (3))."""
     S = cfg.S if S is None else S
-    tau = schedule(S)
+    tau = schedule(S, getattr(cfg, "reverse", False))
     x = np.asarray(noise, dtype=F64)
     vs = []
     for k in range(S):
@@ -301,7 +311,7 @@ def ternary_linear(a, alpha, packed, beta, q=None):
     return bf16_rne(y), acc
 
 
-def velocity_w2a8(x, tau, Kc, Vc, w: dict, cfg, taps=None):
+def velocity_w2a8(x, tau, Kc, Vc, w: dict, cfg, taps=None, prefix_visible=None):
     """The velocity network with the six per-layer maps replaced by Eq. (4)."""
     mods = time_conditioning(w, cfg, tau)
 
@@ -314,7 +324,7 @@ def velocity_w2a8(x, tau, Kc, Vc, w: dict, cfg, taps=None):
         y, _ = ternary_linear(a, alpha, w[name][l], w["beta_" + name][l], q)
         return y.astype(F64).reshape(shp[:-1] + (y.shape[-1],))
 
-    return _expert(x, mods, Kc, Vc, w, cfg, lin, taps)
+    return _expert(x, mods, Kc, Vc, w, cfg, lin, taps, prefix_visible)
 
 
 def with_unpacked(w: dict) -> dict:
@@ -327,8 +337,66 @@ def with_unpacked(w: dict) -> dict:
     return out
 
 
-def denoise_w2a8(noise, Kc, Vc, w: dict, cfg, S: int | None = None):
-    return denoise(noise, Kc, Vc, w, cfg, S, vel=velocity_w2a8)
+def denoise_w2a8(noise, Kc, Vc, w: dict, cfg, S: int | None = None, reverse: bool | None = None,
+                 prefix_visible=None):
+    return denoise(noise, Kc, Vc, w, cfg, S, vel=velocity_w2a8, reverse=reverse, prefix_visible=prefix_visible)
+
+
+# ----------------------------------------------------------------------------
+# In-library seeded noise (§III-C: requests carry optional noise; without it
+# the runtime draws X^0 ~ N(0, I) itself)
+# ----------------------------------------------------------------------------
+
+_M64 = (1 << 64) - 1
+
+
+def philox4x64(counter, key, rounds: int = 10):
+    """Philox4x64-R (Salmon et al., "Parallel random numbers: as easy as 1, 2,
+    3", SC 2011): counter of four and key of two 64-bit words -> four 64-bit
+    words.  Each round multiplies counter words 0 and 2 by the two Philox
+    multipliers, crosses the high halves (xored with the key) and the low
+    halves over the four words, and bumps the key by the Weyl constants."""
+    c = [int(v) & _M64 for v in counter]
+    k = [int(v) & _M64 for v in key]
+    for _ in range(rounds):
+        p0 = 0xD2E7470EE14C6C93 * c[0]
+        p1 = 0xCA5A826395121157 * c[2]
+        c = [(p1 >> 64) ^ c[1] ^ k[0], p1 & _M64, (p0 >> 64) ^ c[3] ^ k[1], p0 & _M64]
+        k = [(k[0] + 0x9E3779B97F4A7C15) & _M64, (k[1] + 0xBB67AE8584CAA73B) & _M64]
+    return c
+
+
+def gaussian_noise(seed: int, shape) -> np.ndarray:
+    """X^0 drawn from the seed: element e of the flattened request (row-major
+    [B][H][d_a]) is normal (e mod 4) of Philox4x64-10 block e // 4 under key
+    (seed, 0) and counter (e // 4, 0, 0, 0); words (x0, x1) and (x2, x3) of a
+    block each give two normals by the Box-Muller transform,
+    u1 = ((x0 >> 11) + 1) 2^-53, u2 = (x1 >> 11) 2^-53,
+    sqrt(-2 ln u1) (cos 2 pi u2, sin 2 pi u2), in fp64, stored as fp32."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=F64)
+    for blk in range((n + 3) // 4):
+        x = philox4x64([blk, 0, 0, 0], [seed, 0])
+        for p in range(2):
+            u1 = ((x[2 * p] >> 11) + 1) * 2.0 ** -53
+            u2 = (x[2 * p + 1] >> 11) * 2.0 ** -53
+            r = math.sqrt(-2.0 * math.log(u1))
+            for j, z in enumerate((r * math.cos(2.0 * math.pi * u2), r * math.sin(2.0 * math.pi * u2))):
+                e = blk * 4 + 2 * p + j
+                if e < n:
+                    out[e] = z
+    return out.astype(np.float32).reshape(shape)
+
+
+def prefix_mask_bits(prefix_visible) -> np.ndarray:
+    """bool [B, P] -> the library's bit mask uint32 [B, ceil(P / 32)]: bit
+    (p mod 32) of word p // 32 is 1 when prefix key p is visible."""
+    v = np.asarray(prefix_visible, dtype=bool)
+    B, P = v.shape
+    words = np.zeros((B, (P + 31) // 32), dtype=np.uint64)
+    for p in range(P):
+        words[:, p // 32] |= v[:, p].astype(np.uint64) << np.uint64(p % 32)
+    return words.astype(np.uint32)
 
 
 # ----------------------------------------------------------------------------

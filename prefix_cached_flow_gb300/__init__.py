@@ -5,4 +5,4 @@ Python binding plus the in-tree build step.
 """
 from .binding import (DTYPE_BF16, DTYPE_F32, EXPORTED, FLAG_ATTN_SPLIT, FLAG_ATTN_STREAM, FLAG_NO_GRAPH,  # noqa: F401
                       FLAG_LINEAR_SPLIT, FLAG_LINEAR_WIDE, FLAG_PERSIST, FLAG_SIMT_GEMM, LIB_PATH, Expert,
-                      VlaError, gelu_forms, lib, quantize_rows, ternary_gemm, upload_weights)
+                      VlaError, gelu_forms, lib, noise_fill, quantize_rows, ternary_gemm, upload_weights)

@@ -30,7 +30,7 @@ EXPORTED = ("vla_expert_create", "vla_expert_create_w2a8", "vla_expert_destroy",
             "vla_expert_poll_status", "vla_expert_set_abort", "vla_w2a8_quantize_rows",
             "vla_w2a8_ternary_gemm", "vla_expert_launch_count", "vla_status_string", "vla_version", "vla_last_error",
             "vla_expert_set_wait_limit", "vla_expert_check_wait_timeout", "vla_expert_w2a8_tap_bytes",
-            "vla_expert_set_w2a8_tap", "vla_debug_gelu_forms")
+            "vla_expert_set_w2a8_tap", "vla_debug_gelu_forms", "vla_action_denoise_ex", "vla_noise_fill")
 
 
 class VlaError(RuntimeError):
@@ -43,13 +43,19 @@ class VlaConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n_layers", "width", "mlp_width", "n_q_heads", "n_kv_heads", "head_dim", "vlm_hidden", "action_dim",
         "horizon", "time_dim", "max_batch", "max_prefix", "dtype")] + [("rms_eps", ctypes.c_float),
-                                                                         ("flags", ctypes.c_uint)]
+                                                                         ("flags", ctypes.c_uint),
+                                                                         ("schedule", ctypes.c_int)]
 
 
 DENSE_FIELDS = ("wk_pre", "wv_pre", "wq", "wk", "wv", "wo", "wup", "wdown", "wmod", "win", "wout", "wt1", "wt2",
                 "wmod_f")
 W2A8_FIELDS = ("wk_pre", "wv_pre", "wq", "wk", "wv", "wo", "wup", "wdown", "beta_wq", "beta_wk", "beta_wv",
                "beta_wo", "beta_wup", "beta_wdown", "wmod", "win", "wout", "wt1", "wt2", "wmod_f")
+
+
+class VlaRequest(ctypes.Structure):
+    _fields_ = [("prefix_mask_dev", ctypes.c_void_p), ("noise_dev", ctypes.c_void_p), ("seed", ctypes.c_ulonglong),
+                ("noise_out_dev", ctypes.c_void_p)]
 
 
 class VlaWeights(ctypes.Structure):
@@ -91,6 +97,8 @@ def lib() -> ctypes.CDLL:
         "vla_expert_w2a8_tap_bytes": [vp, ci, ctypes.POINTER(ctypes.c_size_t)],
         "vla_expert_set_w2a8_tap": [vp, ci, vp, ctypes.c_size_t],
         "vla_debug_gelu_forms": [vp, ci, vp, vp, vp],
+        "vla_action_denoise_ex": [vp, vp, vp, ci, ci, ctypes.POINTER(VlaRequest), vp, vp, vp],
+        "vla_noise_fill": [ctypes.c_ulonglong, ctypes.c_size_t, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -156,7 +164,8 @@ class Expert:
         c = VlaConfig(n_layers=cfg.L, width=cfg.D, mlp_width=cfg.F, n_q_heads=cfg.n_q, n_kv_heads=cfg.n_kv,
                       head_dim=cfg.d_h, vlm_hidden=cfg.d_vlm, action_dim=cfg.d_a, horizon=cfg.H, time_dim=cfg.d_t,
                       max_batch=max_batch or cfg.B, max_prefix=max_prefix or cfg.P,
-                      dtype=DTYPE_F32 if cfg.dtype == "f32" else DTYPE_BF16, rms_eps=cfg.eps, flags=flags)
+                      dtype=DTYPE_F32 if cfg.dtype == "f32" else DTYPE_BF16, rms_eps=cfg.eps, flags=flags,
+                      schedule=1 if getattr(cfg, "reverse", False) else 0)
         self._c = c
         h = ctypes.c_void_p()
         if self.w2a8:
@@ -198,6 +207,21 @@ class Expert:
         fn = lib().vla_action_denoise_w2a8 if self.w2a8 else lib().vla_action_denoise
         _check(fn(self._h, _ptr(Kc), _ptr(Vc), B, P, _ptr(noise), _ptr(actions), _ptr(vel_tap), _stream(stream)),
                "vla_action_denoise")
+        return actions
+
+    def denoise_ex(self, Kc, Vc, B, prefix_mask=None, noise=None, seed=0, noise_out=None, actions=None,
+                   vel_tap=None, stream=None):
+        """Eq. 1 with request options: prefix_mask uint32 [B, ceil(P/32)]
+        (device), noise (device) or None for in-library noise from `seed`."""
+        c = self.cfg
+        P = Kc.shape[3]
+        if actions is None:
+            actions = torch.empty((B, c.H, c.d_a), dtype=torch.float32, device="cuda")
+        req = VlaRequest(prefix_mask_dev=None if prefix_mask is None else prefix_mask.data_ptr(),
+                         noise_dev=None if noise is None else noise.data_ptr(), seed=int(seed),
+                         noise_out_dev=None if noise_out is None else noise_out.data_ptr())
+        _check(lib().vla_action_denoise_ex(self._h, _ptr(Kc), _ptr(Vc), B, P, ctypes.byref(req), _ptr(actions),
+                                           _ptr(vel_tap), _stream(stream)), "vla_action_denoise_ex")
         return actions
 
     def policy_step_host(self, Z_host, noise_host, actions_host, stream=None):
@@ -287,6 +311,13 @@ def np_prod(shape):
     for d in shape:
         n *= int(d)
     return n
+
+
+def noise_fill(seed: int, n: int, stream=None):
+    """The library's seeded X^0 stream: n fp32 normals on the device."""
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    _check(lib().vla_noise_fill(int(seed), n, _ptr(out), _stream(stream)), "vla_noise_fill")
+    return out
 
 
 def gelu_forms(x, stream=None):

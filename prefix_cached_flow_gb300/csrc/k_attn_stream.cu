@@ -105,10 +105,14 @@ __device__ __forceinline__ void tma_load_3d_s(void* dst, const void* map, uint64
 // Row maximum of 32 S values; with MASK only keys (base + u) below nk count.
 // The unmasked form uses the three-input max (two new values per op).
 template <bool MASK>
-__device__ __forceinline__ void max32(float (&mx)[4], const uint32_t* r, int base, int nk) {
+__device__ __forceinline__ void max32(float (&mx)[4], const uint32_t* r, int base, int nk, const uint32_t* mw) {
   if (MASK) {
 #pragma unroll
-    for (int u = 0; u < 32; ++u) mx[u & 3] = fmaxf(mx[u & 3], base + u < nk ? __uint_as_float(r[u]) : -INFINITY);
+    for (int u = 0; u < 32; ++u) {
+      const int j = base + u;
+      const bool v = j < nk && ((mw[j >> 5] >> (j & 31)) & 1u);
+      mx[u & 3] = fmaxf(mx[u & 3], v ? __uint_as_float(r[u]) : -INFINITY);
+    }
   } else {
 #pragma unroll
     for (int u = 0; u < 32; u += 2) {
@@ -128,15 +132,17 @@ __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
 // bf16 pairs into pk, their fp32 sum returned.  Without MASK every key is
 // valid (a full chunk) and the scale and the sum run on fp32 pairs.
 template <bool MASK>
-__device__ __forceinline__ float probs64(const uint32_t* sr, uint32_t* pk, float c, float nm, int base, int nk) {
+__device__ __forceinline__ float probs64(const uint32_t* sr, uint32_t* pk, float c, float nm, int base, int nk,
+                                         const uint32_t* mw) {
   if (MASK) {
     float lv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 64; u += 2) {
       float p0 = fast_exp2(fmaf(__uint_as_float(sr[u]), c, nm));
       float p1 = fast_exp2(fmaf(__uint_as_float(sr[u + 1]), c, nm));
-      p0 = base + u < nk ? p0 : 0.f;
-      p1 = base + u + 1 < nk ? p1 : 0.f;
+      const int j0 = base + u, j1 = j0 + 1;
+      p0 = (j0 < nk && ((mw[j0 >> 5] >> (j0 & 31)) & 1u)) ? p0 : 0.f;
+      p1 = (j1 < nk && ((mw[j1 >> 5] >> (j1 & 31)) & 1u)) ? p1 : 0.f;
       lv[u & 3] += p0;
       lv[(u + 1) & 3] += p1;
       pk[u >> 1] = pack_bf16x2(p0, p1);
@@ -378,23 +384,28 @@ __global__ void __launch_bounds__(352, 1)
       for (int q = 0; q < 4; ++q) tmem_wait16(sr + q * 16);
       tmem_wait16(ot);
       tmem_wait16(ot + 16);
-      const bool fullc = nk == KB;  // the same for the whole CTA
+      // visibility of the chunk's 128 keys (prefix chunks under a mask)
+      uint32_t mw[4];
+      const uint32_t* mrow = (j < n_pre && a.pmask) ? a.pmask + (size_t)b * a.pmw : nullptr;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mw[q] = prefix_mask_window(mrow, a.pmw, j * KB + q * 32);
+      const bool fullc = nk == KB && (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;  // the same for the whole CTA
       float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (fullc) {
-        max32<false>(mxv, sr, 0, 0);
-        max32<false>(mxv, sr + 32, 0, 0);
-        max32<false>(mxv, ot, 0, 0);
+        max32<false>(mxv, sr, 0, 0, mw);
+        max32<false>(mxv, sr + 32, 0, 0, mw);
+        max32<false>(mxv, ot, 0, 0, mw);
       } else {
-        max32<true>(mxv, sr, own0, nk);
-        max32<true>(mxv, sr + 32, own0 + 32, nk);
-        max32<true>(mxv, ot, oth0, nk);
+        max32<true>(mxv, sr, own0, nk, mw);
+        max32<true>(mxv, sr + 32, own0 + 32, nk, mw);
+        max32<true>(mxv, ot, oth0, nk, mw);
       }
       tmem_ld16_nowait(trow + s_col + (uint32_t)(oth0 + 32), ot);
       tmem_ld16_nowait(trow + s_col + (uint32_t)(oth0 + 48), ot + 16);
       tmem_wait16(ot);
       tmem_wait16(ot + 16);
-      if (fullc) max32<false>(mxv, ot, 0, 0);
-      else max32<true>(mxv, ot, oth0 + 32, nk);
+      if (fullc) max32<false>(mxv, ot, 0, 0, mw);
+      else max32<true>(mxv, ot, oth0 + 32, nk, mw);
       // S is no longer needed: the next chunk's S MMAs may overwrite it.
       tc_fence_before();
       mbar_arrive(&bars[B_SC]);
@@ -434,7 +445,8 @@ __global__ void __launch_bounds__(352, 1)
       // Probabilities of this half's 64 keys, packed in bf16 pairs.
       const float nm = -m_used;
       uint32_t pk[32];
-      l += fullc ? probs64<false>(sr, pk, a.scale_log2, nm, 0, 0) : probs64<true>(sr, pk, a.scale_log2, nm, own0, nk);
+      l += fullc ? probs64<false>(sr, pk, a.scale_log2, nm, 0, 0, mw)
+                 : probs64<true>(sr, pk, a.scale_log2, nm, own0, nk, mw);
       // The P tile is free once P_{j-1} V_{j-1} has completed.
       if (j >= 1 && !waited_pv && !__all_sync(~0u, mbar_wait(&bars[B_PV], (uint32_t)(j - 1) & 1u, a.status))) {
         ok = false;

@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(128, 1)
   const int row = warp * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
   float m = -INFINITY, l = 0.f;
+  const uint32_t* mrow = (suffix || !a.pmask) ? nullptr : a.pmask + (size_t)b * a.pmw;
   if (ok && nk > 0) {
     // Two passes over TMEM in 32-column pieces.  Every CTA runs this code
     // once, so it is kept compact (rolled loops whose bodies repeat, instead
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(128, 1)
       tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
       tmem_wait16(r);
       tmem_wait16(r + 16);
-      if (c0 + 32 <= nk) {  // a full piece (uniform over the CTA): three-input max, no masks
+      const uint32_t mb = prefix_mask_window(mrow, a.pmw, key0 + c0);
+      if (c0 + 32 <= nk && mb == 0xFFFFFFFFu) {  // a full visible piece (uniform over the CTA): no masks
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
           float& mm = mxv[(u >> 1) & 3];
@@ -179,7 +181,8 @@ __global__ void __launch_bounds__(128, 1)
         }
       } else {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) mxv[u & 3] = fmaxf(mxv[u & 3], c0 + u < nk ? __uint_as_float(r[u]) : -INFINITY);
+        for (int u = 0; u < 32; ++u)
+          mxv[u & 3] = fmaxf(mxv[u & 3], (c0 + u < nk && ((mb >> u) & 1u)) ? __uint_as_float(r[u]) : -INFINITY);
       }
     }
     m = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])) * a.scale_log2;  // the scale is positive
@@ -194,6 +197,8 @@ __global__ void __launch_bounds__(128, 1)
       tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
       tmem_wait16(r);
       tmem_wait16(r + 16);
+      const uint32_t mb = prefix_mask_window(mrow, a.pmw, key0 + c0);
+      const bool masked = c0 + 32 > nk || mb != 0xFFFFFFFFu;  // the last, partial piece or hidden keys
 #pragma unroll
       for (int q = 0; q < 4; ++q) {  // 8-key chunks
         float p[8];
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(128, 1)
         for (int u = 0; u < 8; ++u) {
           const int j = c0 + q * 8 + u;
           p[u] = fast_exp2(fmaf(__uint_as_float(r[q * 8 + u]), a.scale_log2, nm));
-          if (c0 + 32 > nk) p[u] = j < nk ? p[u] : 0.f;  // only the last, partial piece is masked
+          if (masked) p[u] = (j < nk && ((mb >> (q * 8 + u)) & 1u)) ? p[u] : 0.f;
           lv[u & 3] += p[u];
         }
         uint4 pk;

@@ -31,15 +31,52 @@ int embed_split(const ExpertDims& d) {
 // ---------------------------------------------------------------------------
 // Time conditioning table (built once per handle; tau_k = k / S)
 // ---------------------------------------------------------------------------
-__global__ void k_time_embed(float* e, int S, int d_t) {
+__global__ void k_time_embed(float* e, int S, int d_t, int reverse) {
   const int k = blockIdx.x;
   const int half = d_t / 2;
-  const double tau = (double)k / (double)S;
+  const double tau = reverse ? 1.0 - (double)k / (double)S : (double)k / (double)S;
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     const double omega = pow(10000.0, -(double)i / (double)half);
     const double arg = 1000.0 * tau * omega;
     e[(size_t)k * d_t + i] = (float)sin(arg);
     e[(size_t)k * d_t + half + i] = (float)cos(arg);
+  }
+}
+
+// X^0 ~ N(0, I) from a seed: element e is normal (e mod 4) of Philox4x64-10
+// block e / 4 (key (seed, 0), counter (e / 4, 0, 0, 0); Salmon et al., SC
+// 2011), each pair of 64-bit words giving two normals by the Box-Muller
+// transform in fp64.  One thread per block of four.
+__device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t a0 = 0xD2E7470EE14C6C93ull, a1 = 0xCA5A826395121157ull;
+    const uint64_t hi0 = __umul64hi(a0, c[0]), lo0 = a0 * c[0];
+    const uint64_t hi1 = __umul64hi(a1, c[2]), lo1 = a1 * c[2];
+    const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+    k0 += 0x9E3779B97F4A7C15ull;
+    k1 += 0xBB67AE8584CAA73Bull;
+  }
+}
+__global__ void k_noise(unsigned long long seed, size_t n, float* out) {
+  const size_t blk = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (blk * 4 >= n) return;
+  uint64_t c[4] = {(uint64_t)blk, 0ull, 0ull, 0ull};
+  philox4x64_10(c, (uint64_t)seed, 0ull);
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const double u1 = (double)((c[2 * p] >> 11) + 1) * 0x1p-53;
+    const double u2 = (double)(c[2 * p + 1] >> 11) * 0x1p-53;
+    const double r = sqrt(-2.0 * log(u1));
+    double sn, cs;
+    sincos(2.0 * 3.14159265358979323846 * u2, &sn, &cs);
+    const size_t e = blk * 4 + 2 * p;
+    if (e < n) out[e] = (float)(r * cs);
+    if (e + 1 < n) out[e + 1] = (float)(r * sn);
   }
 }
 
@@ -173,6 +210,8 @@ __global__ void k_attn_part(ExpertDims d, StepBufs b, const TC* Kc, const TC* Vc
     const float* kr = Ks + r * (dh + 1);
     float s = 0.f;
     for (int e = 0; e < dh; ++e) s += qr[e] * kr[e];
+    const int kk = k0 + r;  // a hidden prefix key: M = -inf in Eq. (2)
+    if (b.pmask && kk < d.P && !((__ldg(b.pmask + (size_t)bb * b.pmw + (kk >> 5)) >> (kk & 31)) & 1u)) s = -INFINITY;
     S[t * chunk + r] = s;
   }
   __syncthreads();
@@ -184,7 +223,7 @@ __global__ void k_attn_part(ExpertDims d, StepBufs b, const TC* Kc, const TC* Vc
     m = warp_max(m);
     float l = 0.f;
     for (int r = lane; r < nk; r += 32) {
-      const float p = expf(S[t * chunk + r] - m);
+      const float p = m == -INFINITY ? 0.f : expf(S[t * chunk + r] - m);  // a chunk of hidden keys
       S[t * chunk + r] = p;
       l += p;
     }
@@ -870,8 +909,14 @@ cudaError_t launch_head_fused(const ExpertDims& d, const StepBufs& b, int step, 
                     args);
 }
 
-cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st) {
-  k_time_embed<<<S, 128, 0, st>>>(e, S, d_t);
+cudaError_t launch_time_embed(float* e, int S, int d_t, int reverse, cudaStream_t st) {
+  k_time_embed<<<S, 128, 0, st>>>(e, S, d_t, reverse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_noise(unsigned long long seed, size_t n, float* out, cudaStream_t st) {
+  const size_t blocks = (n + 3) / 4;
+  k_noise<<<(unsigned)((blocks + 255) / 256), 256, 0, st>>>(seed, n, out);
   return cudaGetLastError();
 }
 

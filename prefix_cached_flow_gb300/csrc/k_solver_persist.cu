@@ -612,10 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) tmem_ld16(taddr + (uint32_t)(q * 16), sv + q * 16);
         const bool live = row < rows;
+        // visibility of the chunk's keys (prefix chunks under a mask)
+        uint32_t mw[4];
+        const uint32_t* mrow = (pre && a.pmask) ? a.pmask + (size_t)b * a.pmw : nullptr;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mw[q] = prefix_mask_window(mrow, a.pmw, k0 + q * 32);
+        auto vis = [&](int j) { return j < nkeys && ((mw[j >> 5] >> (j & 31)) & 1u); };
         float mx = -INFINITY;
 #pragma unroll
         for (int j = 0; j < kKC; ++j)
-          if (j < nkeys) mx = fmaxf(mx, sv[j] * a.scale_log2);
+          if (vis(j)) mx = fmaxf(mx, sv[j] * a.scale_log2);
         if (!live) mx = 0.f;
         float lsum = 0.f;
 #pragma unroll
@@ -624,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int j = c8 * 8 + e;
-            p[e] = (live && j < nkeys) ? fast_exp2(sv[j] * a.scale_log2 - mx) : 0.f;
+            p[e] = (live && vis(j)) ? fast_exp2(sv[j] * a.scale_log2 - mx) : 0.f;
           }
           const uint4 pk = pack8(p);
           // the sum uses the bf16 values the P V product multiplies
@@ -705,13 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
         float M = -INFINITY;
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch)
-          if (ch < a.nch) M = fmaxf(M, ml[ch].x);
+          if (ch < a.nch && ml[ch].y > 0.f) M = fmaxf(M, ml[ch].x);
         float den = 0.f, v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch)
-          if (ch < a.nch) {
+          if (ch < a.nch && ml[ch].y > 0.f) {  // a chunk of hidden keys contributes nothing
             const float w = fast_exp2(ml[ch].x - M);
             den += w * ml[ch].y;
             float o[8];
@@ -730,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
     // and the Euler update; one warp per (token, output) pair, all its loads
     // in flight together --------------------------------------------------------
     auto head_velocity = [&](int k) {
-      const float dt = (float)((double)(k + 1) / a.S - (double)k / a.S);
+      const float dt = a.dt_sign * (float)((double)(k + 1) / a.S - (double)k / a.S);
       const float* x_in = k == 0 ? a.noise : a.actions;
       const float* gf = a.modf + (size_t)k * 2 * D;
       const float* bf = gf + D;

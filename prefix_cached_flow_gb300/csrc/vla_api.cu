@@ -22,6 +22,7 @@ namespace {
 
 struct GraphEntry {
   int B, P;
+  const uint32_t* pmask;
   const void* kc;
   const void* vc;
   const float* noise;
@@ -43,6 +44,7 @@ struct GemmPlan {
 };
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
+
 int round_up(int a, int b) { return cdiv(a, b) * b; }
 
 }  // namespace
@@ -105,6 +107,11 @@ struct vla_expert {
   cudaStream_t cap_stream = nullptr;
   std::vector<GraphEntry> graphs;
   uint64_t tick = 0;
+  // request options of the call being enqueued (prefix mask) and the buffer
+  // for in-library noise
+  const uint32_t* pmask = nullptr;
+  int pmw = 0;
+  float* noise_buf = nullptr;
   // persistent whole-solve kernel for few tokens (k_solver_persist.cu)
   bool persist_ok = false;
   int persist_T = 0;         // tokens its buffers hold
@@ -130,6 +137,13 @@ struct vla_expert {
 };
 
 namespace {
+
+// tau_{k+1} - tau_k of the handle's schedule: 1/S, or -1/S for the reverse
+// (1 -> 0) convention, whose velocity sign change enters Eq. (1) here.
+float step_dt(const vla_expert* h, int k) {
+  const double d = (double)(k + 1) / h->S - (double)k / h->S;
+  return (float)(h->cfg.schedule == VLA_SCHEDULE_REVERSE ? -d : d);
+}
 
 vla_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return VLA_OK;
@@ -227,6 +241,8 @@ StepBufs make_bufs(const vla_expert* h, int P) {
   b.q = h->q; b.ks = h->ks; b.vs = h->vs; b.opart = h->opart; b.ml = h->ml;
   b.attn_chunk = h->attn_chunk;
   b.n_chunks = cdiv(P + h->cfg.horizon, h->attn_chunk);
+  b.pmask = h->pmask;
+  b.pmw = h->pmw;
   return b;
 }
 
@@ -274,7 +290,7 @@ vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B,
   const DevCtl ctl{h->d_status, h->d_abort};
   for (int k = 0; k < h->S; ++k) {
     const float* x_in = k == 0 ? noise : actions;
-    const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    const float dt = step_dt(h, k);
     VLA_CK(launch_embed_norm(d, sb, k, x_in, ctl, st));
     for (int l = 0; l < c.n_layers; ++l) {
       VLA_CK(run_linear(h, 0, l, T, pl[0], xmap[0], st));
@@ -466,6 +482,7 @@ vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, con
   aa.kc_s = round_up(c.horizon, 16);
   aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
   aa.o = (bf16*)o; aa.o32 = o32; aa.xo = h->xo; aa.status = h->d_status;
+  aa.pmask = h->pmask; aa.pmw = h->pmw;
   const unsigned fl = c.flags;
   const bool stream_ok = dh == 64 || dh == 128 || dh == 256;
   ap->stream = stream_ok && ((fl & VLA_FLAG_ATTN_STREAM) ||
@@ -525,7 +542,7 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   const float* modt = h->modtab;
   for (int k = 0; k < h->S; ++k) {
     const float* x_in = k == 0 ? noise : actions;
-    const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    const float dt = step_dt(h, k);
     VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
     int n_ss = embed_ss_slots(d);  // slots of ss2 currently valid
     for (int l = 0; l < L; ++l) {
@@ -601,7 +618,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
   tap_sizes(h, B, tsz);
   for (int k = 0; k < h->S; ++k) {
     const float* x_in = k == 0 ? noise : actions;
-    const float dt = (float)((double)(k + 1) / h->S - (double)k / h->S);
+    const float dt = step_dt(h, k);
     const bool tapping = h->tap && k == h->tap_step;
     // tap: copy workspace tensor `src` into tensor `i` of layer `l`
     auto cp = [&](int l, int i, const void* src) -> cudaError_t {
@@ -711,12 +728,14 @@ bool persist_plan(const vla_expert* h, int B, int P, PersistArgs* pa) {
   a.work_bytes = work;
   if (persist_ring_stages(c.width, work) < 4) return false;
   a.eps = c.rms_eps;
+  a.dt_sign = c.schedule == VLA_SCHEDULE_REVERSE ? -1.f : 1.f;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
   a.win = h->win; a.wout = h->wout; a.modtab = h->modtab; a.modf = h->modf; a.cqkv = h->cqkv; a.cup = h->cup;
   a.h = h->h; a.accq = h->p_accq; a.accu = h->p_accu; a.rms = h->p_rms;
   a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vs = (bf16*)h->vs; a.o = (bf16*)h->act;
   a.opart = h->p_opart; a.oml = h->p_oml;
   a.bar = h->p_bar; a.stop = (int*)(h->p_bar + 1); a.status = h->d_status; a.abort = h->d_abort;
+  a.pmask = h->pmask; a.pmw = h->pmw;
   *pa = a;
   return true;
 }
@@ -757,6 +776,7 @@ vla_status validate_config(const vla_expert_config* c, int n_steps, bool w2a8) {
       c->max_batch < 1 || c->max_prefix < 1 || !(c->rms_eps > 0.f))
     return VLA_ERR_INVALID_ARG;
   if (c->dtype != VLA_DTYPE_F32 && c->dtype != VLA_DTYPE_BF16) return VLA_ERR_INVALID_ARG;
+  if (c->schedule != VLA_SCHEDULE_FORWARD && c->schedule != VLA_SCHEDULE_REVERSE) return VLA_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0 || c->time_dim % 2 != 0) return VLA_ERR_SHAPE;
   if (w2a8 && c->dtype != VLA_DTYPE_BF16) return VLA_ERR_INVALID_ARG;
   const int qdim = c->n_q_heads * c->head_dim;
@@ -831,7 +851,7 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
   if ((s = dalloc(&cc, (size_t)S * D * 4)) != VLA_OK) { cudaFree(e); cudaFree(c1); return s; }
   if ((s = dalloc(&h->modtab, (size_t)S * L * 4 * D * 4)) != VLA_OK) return s;
   if ((s = dalloc(&h->modf, (size_t)S * 2 * D * 4)) != VLA_OK) return s;
-  cudaError_t err = launch_time_embed(e, S, d_t, st);
+  cudaError_t err = launch_time_embed(e, S, d_t, c.schedule == VLA_SCHEDULE_REVERSE, st);
   if (err == cudaSuccess) err = launch_gemm_simt(0, e, d_t, wb, wt1, d_t, S, D, d_t, 1, c1, 0, D, nullptr, st);
   if (err == cudaSuccess) err = launch_silu(c1, (size_t)S * D, st);
   if (err == cudaSuccess) err = launch_gemm_simt(0, c1, D, wb, wt2, D, S, D, D, 1, cc, 0, D, nullptr, st);
@@ -1019,7 +1039,7 @@ void vla_expert_destroy(vla_expert* h) {
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
                   h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf,
-                  h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar};
+                  h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar, h->noise_buf};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -1188,13 +1208,16 @@ vla_status vla_prefix_kv_build(vla_expert* h, const void* Z, int B, int P, void*
 }
 
 static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const void* Vc, int B, int P,
-                               const float* noise, float* actions, float* tap, void* stream) {
+                               const float* noise, float* actions, float* tap, void* stream,
+                               const uint32_t* pmask = nullptr) {
   if (!h || h->w2a8 != w2a8) return VLA_ERR_INVALID_ARG;
   if (!Kc || !Vc || !noise || !actions || !aligned16(Kc) || !aligned16(Vc) || !aligned16(noise) ||
-      !aligned16(actions) || (tap && !aligned16(tap)))
+      !aligned16(actions) || (tap && !aligned16(tap)) || (pmask && ((uintptr_t)pmask & 3u)))
     return VLA_ERR_INVALID_ARG;
   if (B < 1 || B > h->cfg.max_batch || P < 1 || P > h->cfg.max_prefix) return VLA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
+  h->pmask = pmask;
+  h->pmw = (P + 31) / 32;
   // Few tokens (bf16) with VLA_FLAG_PERSIST: the whole solve is one persistent kernel launch.
   PersistArgs pa;
   if (!w2a8 && !h->tap && !(h->cfg.flags & (VLA_FLAG_SIMT_GEMM | VLA_FLAG_ATTN_SPLIT | VLA_FLAG_ATTN_STREAM |
@@ -1210,7 +1233,8 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
   if ((h->cfg.flags & VLA_FLAG_NO_GRAPH) || h->tap) return enqueue(st);
   GraphEntry* hit = nullptr;
   for (auto& g : h->graphs)
-    if (g.B == B && g.P == P && g.kc == Kc && g.vc == Vc && g.noise == noise && g.actions == actions && g.tap == tap)
+    if (g.B == B && g.P == P && g.pmask == pmask && g.kc == Kc && g.vc == Vc && g.noise == noise &&
+        g.actions == actions && g.tap == tap)
       hit = &g;
   if (!hit) {
     if ((int)h->graphs.size() >= kMaxGraphs) {
@@ -1233,7 +1257,7 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
     e = cudaGraphInstantiate(&exec, graph, 0);
     cudaGraphDestroy(graph);
     VLA_CK(e);
-    h->graphs.push_back(GraphEntry{B, P, Kc, Vc, noise, actions, tap, exec, 0});
+    h->graphs.push_back(GraphEntry{B, P, pmask, Kc, Vc, noise, actions, tap, exec, 0});
     hit = &h->graphs.back();
   }
   hit->last_use = ++h->tick;
@@ -1249,6 +1273,35 @@ vla_status vla_action_denoise(vla_expert* h, const void* Kc, const void* Vc, int
 vla_status vla_action_denoise_w2a8(vla_expert* h, const void* Kc, const void* Vc, int B, int P, const float* noise,
                                    float* actions, float* tap, void* stream) {
   return denoise_impl(h, true, Kc, Vc, B, P, noise, actions, tap, stream);
+}
+
+vla_status vla_noise_fill(unsigned long long seed, size_t n, float* out, void* stream) {
+  if (!out || n < 1) return VLA_ERR_INVALID_ARG;
+  VLA_CK(launch_noise(seed, n, out, (cudaStream_t)stream));
+  return VLA_OK;
+}
+
+vla_status vla_action_denoise_ex(vla_expert* h, const void* Kc, const void* Vc, int B, int P, const vla_request* req,
+                                 float* actions, float* tap, void* stream) {
+  if (!h || !req) return VLA_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.max_batch) return VLA_ERR_INVALID_ARG;
+  const float* noise = req->noise_dev;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!noise) {
+    // X^0 drawn in the library from the seed, into a handle-owned buffer
+    const size_t n = (size_t)B * h->cfg.horizon * h->cfg.action_dim;
+    if (!h->noise_buf) {
+      vla_status s = dalloc(&h->noise_buf, (size_t)h->cfg.max_batch * h->cfg.horizon * h->cfg.action_dim * 4);
+      if (s != VLA_OK) return s;
+    }
+    VLA_CK(launch_noise(req->seed, n, h->noise_buf, st));
+    if (req->noise_out_dev) {
+      if (!aligned16(req->noise_out_dev)) return VLA_ERR_INVALID_ARG;
+      VLA_CK(cudaMemcpyAsync(req->noise_out_dev, h->noise_buf, n * 4, cudaMemcpyDeviceToDevice, st));
+    }
+    noise = h->noise_buf;
+  }
+  return denoise_impl(h, h->w2a8, Kc, Vc, B, P, noise, actions, tap, stream, req->prefix_mask_dev);
 }
 
 vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kernels) {

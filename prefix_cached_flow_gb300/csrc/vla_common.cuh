@@ -149,6 +149,18 @@ __device__ __forceinline__ float gelu_exact(float x) {
   return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
 }
 
+// Visibility bits of prefix keys [start, start + 32) of one observation from
+// its mask row (nw words; bit p % 32 of word p / 32 set = key p visible, the
+// additive mask M of Eq. (2) being 0 there and -inf elsewhere).  Keys past
+// the row read as hidden; a null row is all visible.
+__device__ __forceinline__ uint32_t prefix_mask_window(const uint32_t* row, int nw, int start) {
+  if (!row) return 0xFFFFFFFFu;
+  const int w = start >> 5, sh = start & 31;
+  const uint32_t lo = (w >= 0 && w < nw) ? __ldg(row + w) : 0u;
+  const uint32_t hi = (w + 1 >= 0 && w + 1 < nw) ? __ldg(row + w + 1) : 0u;
+  return sh ? (lo >> sh) | (hi << (32 - sh)) : lo;
+}
+
 // ---------------------------------------------------------------------------
 // PTX: shared-memory addresses, mbarriers, TMA
 // ---------------------------------------------------------------------------
@@ -619,6 +631,8 @@ struct AttnArgs {
   int kc_s;          // action-key tile (H rounded up to 16, <= 128)
   float scale_log2;  // log2(e) / sqrt(d_h)
   bf16* o;           // [B*H][n_q*d_h] output
+  const uint32_t* pmask;  // prefix visibility bits [B][pmw] (null: every prefix key visible)
+  int pmw;                // mask words per observation, (P + 31) / 32
   bf16* xo;          // L2 exchange of scaled partial O: [tile][rank][d_h/8][128][8] bf16
   float* o32;        // when set, o is written in fp32 here instead of bf16 (W2A8 quantises it next)
   int* status;
@@ -655,7 +669,7 @@ struct PersistArgs {
   int nqt, npch, nch, att_units;  // query tiles per (b, g), cached-key chunks, all chunks, units
   int U[4], nkb[4], N[4];         // linear phases (qkv, o, up, down): units, K blocks, rows
   int work_bytes;                 // linear CTAs' operand + staging region
-  float eps, scale_log2;
+  float eps, scale_log2, dt_sign;
   const float* win;     // [D][d_a]
   const float* wout;    // [d_a][D]
   const float* modtab;  // [S][L][4][D]
@@ -679,6 +693,8 @@ struct PersistArgs {
   int* stop;
   int* status;
   const volatile int* abort;
+  const uint32_t* pmask;      // prefix visibility bits [B][pmw] (null: all visible)
+  int pmw;
   unsigned long long* trace;  // phase trace (-DVLA_PERSIST_TRACE builds), else unused
 };
 size_t persist_smem_bytes(int D);
@@ -725,9 +741,14 @@ struct StepBufs {
   float* opart;         // attention partial outputs
   float* ml;            // attention partial (max, sum)
   int attn_chunk, n_chunks;
+  const uint32_t* pmask;  // prefix visibility bits [B][pmw] (null: all visible)
+  int pmw;
 };
 
-cudaError_t launch_time_embed(float* e, int S, int d_t, cudaStream_t st);
+// tau_k = k / S, or 1 - k / S when reverse.
+cudaError_t launch_time_embed(float* e, int S, int d_t, int reverse, cudaStream_t st);
+// n normals of the seeded Philox4x64-10 / Box-Muller stream (X^0).
+cudaError_t launch_noise(unsigned long long seed, size_t n, float* out, cudaStream_t st);
 cudaError_t launch_silu(float* x, size_t n, cudaStream_t st);
 cudaError_t launch_embed_norm(const ExpertDims& d, const StepBufs& b, int step, const float* x_in, DevCtl ctl,
                               cudaStream_t st);

@@ -484,3 +484,94 @@ def test_w2a8_unpacked_cache_is_same_function():
     v1 = O.velocity_w2a8(noise, 0.5, Kc, Vc, w, cfg)
     v2 = O.velocity_w2a8(noise, 0.5, Kc, Vc, O.with_unpacked(w), cfg)
     assert np.array_equal(v1, v2)
+
+
+# ---------------------------------------------------------- request options (§III-A, §III-C)
+
+def test_philox_matches_library_philox():
+    """The oracle's Philox4x64-10 against numpy's Philox bit generator (an
+    independent implementation of the same published generator; numpy's
+    n-th block of four words uses counter n + 1)."""
+    for seed in (0, 1, 12345, 2 ** 63 + 5):
+        raw = np.random.Philox(key=seed).random_raw(16)
+        for n in range(4):
+            got = O.philox4x64([n + 1, 0, 0, 0], [seed, 0])
+            assert [int(x) for x in raw[4 * n:4 * n + 4]] == got
+
+
+def test_gaussian_noise_inverts_to_the_generator_words():
+    """Box-Muller run backwards: for each pair (z0, z1) of the stream,
+    exp(-(z0^2 + z1^2) / 2) is the first uniform and atan2(z1, z0) / 2 pi
+    (mod 1) the second, both formed from numpy's Philox words."""
+    seed = 99
+    z = O.gaussian_noise(seed, (4000,)).astype(np.float64)
+    # numpy's generator increments its counter before each block: start it one
+    # below zero so that its first block is counter 0
+    top = np.iinfo(np.uint64).max
+    words = np.random.Philox(key=seed, counter=[top, top, top, top]).random_raw(4000).astype(np.uint64)
+    z = z.reshape(-1, 2)
+    w = words.reshape(-1, 2)
+    u1 = ((w[:, 0] >> np.uint64(11)) + np.uint64(1)).astype(np.float64) * 2.0 ** -53
+    u2 = (w[:, 1] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    r2 = z[:, 0] ** 2 + z[:, 1] ** 2
+    np.testing.assert_allclose(np.exp(-r2 / 2), u1, rtol=2e-6 * (1 + r2.max()), atol=1e-7)
+    ang = np.mod(np.arctan2(z[:, 1], z[:, 0]) / (2 * np.pi), 1.0)
+    d = np.abs(ang - u2)
+    assert np.all(np.minimum(d, 1 - d) <= 1e-6)
+
+
+def test_gaussian_noise_is_standard_normal_and_prefix_stable():
+    from scipy import stats
+    z = O.gaussian_noise(7, (20000,)).astype(np.float64)
+    assert stats.kstest(z, "norm").pvalue > 1e-3
+    assert abs(z.mean()) < 0.03 and abs(z.std() - 1) < 0.03
+    a = O.gaussian_noise(3, (4, 5, 7))
+    b = O.gaussian_noise(3, (1, 5, 7))
+    assert np.array_equal(a[:1], b)
+
+
+def test_prefix_mask_bits_vs_packbits():
+    rng = np.random.default_rng(3)
+    v = rng.random((3, 77)) < 0.5
+    words = O.prefix_mask_bits(v)
+    ref = np.packbits(np.pad(v, ((0, 0), (0, 96 - 77))), axis=1, bitorder="little").view("<u4")
+    assert np.array_equal(words, ref)
+
+
+def test_reverse_schedule_constant_field_endpoint():
+    """tau runs 1 -> 0: with a tau-independent, token-independent velocity
+    field the solve ends at X^0 + (tau_S - tau_0) v = X^0 - v (the sign
+    change of the reverse convention)."""
+    cfg = PIN.replace(reverse=True)
+    w, Z, noise = _setup(cfg, zero=("win", "wt1", "wt2", "wmod", "wmod_f"))
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    xS, vs = O.denoise(noise, Kc, Vc, w, cfg)
+    assert np.allclose(vs, vs[0:1], atol=1e-13, rtol=0)
+    np.testing.assert_allclose(xS, noise - vs[0], rtol=0, atol=1e-12)
+    assert np.array_equal(O.schedule(4, True), np.array([1.0, 0.75, 0.5, 0.25, 0.0]))
+
+
+def test_reverse_schedule_evaluates_the_reversed_time():
+    cfg = PIN.replace(reverse=True)
+    w, Z, noise = _setup(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    _, vs = O.denoise(noise, Kc, Vc, w, cfg)
+    np.testing.assert_allclose(vs[0], O.velocity(noise, 1.0, Kc, Vc, w, cfg), rtol=0, atol=1e-13)
+    x1 = noise - vs[0] / cfg.S
+    np.testing.assert_allclose(vs[1], O.velocity(x1, 1.0 - 1.0 / cfg.S, Kc, Vc, w, cfg), rtol=0, atol=1e-12)
+
+
+def test_hidden_prefix_keys_equal_deleted_keys():
+    """M = -inf on a prefix key (Eq. 2) is the same as removing the key from
+    the cache, for every observation independently; hiding every prefix key
+    leaves attention over the action tokens alone."""
+    cfg = PIN.replace(B=2, P=10)
+    w, Z, noise = _setup(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    vis = np.array([[1, 0, 1, 1, 0, 0, 1, 0, 1, 1], [0] * 10], dtype=bool)
+    xS, _ = O.denoise(noise, Kc, Vc, w, cfg, prefix_visible=vis)
+    for b in range(2):
+        keep = np.flatnonzero(vis[b])
+        xb, _ = O.denoise(noise[b:b + 1], Kc[:, b:b + 1][:, :, :, keep], Vc[:, b:b + 1][:, :, :, keep], w,
+                          cfg.replace(B=1))
+        np.testing.assert_allclose(xS[b:b + 1], xb, rtol=0, atol=1e-12)

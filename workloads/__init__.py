@@ -69,6 +69,7 @@ class ExpertConfig:
     dtype: str = "bf16"  # "f32" or "bf16": storage type of weights, Z, K/V cache
     w2a8: bool = False
     eps: float = 1e-6
+    reverse: bool = False  # integration direction of the schedule: 0 -> 1, or 1 -> 0
 
     def replace(self, **kw) -> "ExpertConfig":
         return dataclasses.replace(self, **kw)
