@@ -48,7 +48,7 @@
 //
 // Attention unit: S = Q K^T on tcgen05 (Q, K by TMA from the bf16 workspace
 // and the cache), softmax in fp32 (one row per thread), P in bf16, O = P V on
-// tcgen05; the unit writes its unnormalised O (bf16) with the row maximum m
+// tcgen05; the unit writes its unnormalised O (fp32) with the row maximum m
 // and sum l, and B3 forms o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 //
 // Warp roles (256 threads): warp 0 lane 0 streams weights; warp 1 lane 0
@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
         if (!mbar_wait(odone, par, a.status)) *s_fail = 1;
         tc_fence_after();
         const uint32_t taddr = tO + ((uint32_t)((warp - 4) * 32) << 16);
-        bf16* dst = a.opart + (((size_t)(zs * a.nch + ch)) * (a.group * a.H) + qt * 128 + row) * dh;
+        float* dst = a.opart + (((size_t)(zs * a.nch + ch)) * (a.group * a.H) + qt * 128 + row) * dh;
         for (int c0 = 0; c0 < dh; c0 += 32) {
           uint32_t r[32];
           tmem_ld16_nowait(taddr + (uint32_t)c0, r);
@@ -673,12 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
           tmem_wait16(r + 16);
           if (row < rows) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float v[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[q * 8 + e]);
-              __stcg((uint4*)(dst + c0 + q * 8), pack8(v));
-            }
+            for (int q = 0; q < 8; ++q)
+              __stcg((uint4*)(dst + c0 + q * 4), make_uint4(r[q * 4], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
           }
         }
         tc_fence_before();
@@ -701,13 +697,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
         const int r = jj * a.H + i;
         const size_t base = (size_t)(b * a.n_kv + g) * a.nch;
         float2 ml[16];
-        uint4 ov[16];
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch)
-          if (ch < a.nch) {
-            ml[ch] = __ldcg(&a.oml[(base + ch) * GH + r]);
-            ov[ch] = __ldcg((const uint4*)(a.opart + ((base + ch) * GH + r) * a.d_h + d));
-          }
+          if (ch < a.nch) ml[ch] = __ldcg(&a.oml[(base + ch) * GH + r]);
         float M = -INFINITY;
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch)
@@ -720,10 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
           if (ch < a.nch && ml[ch].y > 0.f) {  // a chunk of hidden keys contributes nothing
             const float w = fast_exp2(ml[ch].x - M);
             den += w * ml[ch].y;
-            float o[8];
-            unpack8(ov[ch], o);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] += w * o[e];
+            const float* op = a.opart + ((base + ch) * GH + r) * a.d_h + d;
+            const float4 o0 = ldcg4(op), o1 = ldcg4(op + 4);
+            v[0] += w * o0.x; v[1] += w * o0.y; v[2] += w * o0.z; v[3] += w * o0.w;
+            v[4] += w * o1.x; v[5] += w * o1.y; v[6] += w * o1.z; v[7] += w * o1.w;
           }
         const float inv = 1.f / den;
 #pragma unroll

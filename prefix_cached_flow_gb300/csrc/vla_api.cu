@@ -120,7 +120,7 @@ struct vla_expert {
   float* p_accq = nullptr;
   float* p_accu = nullptr;
   float* p_rms = nullptr;
-  bf16* p_opart = nullptr;
+  float* p_opart = nullptr;
   float2* p_oml = nullptr;
   unsigned* p_bar = nullptr;
   size_t p_units = 0;
@@ -971,7 +971,7 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
       if ((s = dalloc(&h->p_accu, (size_t)Tp * F * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_rms, (size_t)2 * Tp * 4)) != VLA_OK) return s;
       // chunk partials [B*n_kv*nch][group*H] rows (at most 128 per unit)
-      if ((s = dalloc(&h->p_opart, h->p_units * 128 * dh * 2)) != VLA_OK) return s;
+      if ((s = dalloc(&h->p_opart, h->p_units * 128 * dh * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_oml, h->p_units * 128 * sizeof(float2))) != VLA_OK) return s;
       if ((s = dalloc(&h->p_bar, 64)) != VLA_OK) return s;
       VLA_CK(cudaMemset(h->p_bar, 0, 64));

@@ -687,7 +687,7 @@ struct PersistArgs {
   bf16* ks;             // [B][n_kv][H][d_h]
   bf16* vs;             // [B][n_kv][d_h][Hp]
   bf16* o;              // [T][qdim]
-  bf16* opart;          // [B*n_kv*nch][group*H][d_h]
+  float* opart;         // [B*n_kv*nch][group*H][d_h] unnormalised chunk outputs
   float2* oml;          // [B*n_kv*nch][group*H]
   unsigned* bar;        // grid barrier counter; bar[1] is the stop word
   int* stop;
