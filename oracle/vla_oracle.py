@@ -63,6 +63,7 @@ __all__ = [
     "denoise", "denoise_recompute", "quantize_rows", "pack_ternary",
     "unpack_ternary", "bf16_rne", "ternary_linear", "velocity_w2a8", "with_unpacked",
     "denoise_w2a8", "parity_metrics", "philox4x64", "gaussian_noise", "prefix_mask_bits",
+    "row_scales", "prefix_kv_w2a8",
 ]
 
 
@@ -121,8 +122,11 @@ def prefix_kv(Z, w: dict, cfg):
     """Z [B, P, d_vlm] -> K_C, V_C [L, B, n_kv, P, d_h] (fp64).
 
     Token-wise projection of the raw prefix hidden states: no mask, no
-    positions, so no causal structure can leak into the cache.
+    positions, so no causal structure can leak into the cache.  Ternary
+    (packed) prefix maps take the Eq. (4) path, prefix_kv_w2a8.
     """
+    if np.asarray(w["wk_pre"]).dtype == np.uint8:
+        return prefix_kv_w2a8(Z, w, cfg)
     Z = np.asarray(Z, dtype=F64)
     B, P, _ = Z.shape
     K = np.empty((cfg.L, B, cfg.n_kv, P, cfg.d_h), dtype=F64)
@@ -292,10 +296,22 @@ def bf16_rne(x):
     return (keep << np.uint64(16)).astype(np.uint32).view(np.float32)
 
 
-def ternary_linear(a, alpha, packed, beta, q=None):
-    """y_mn = alpha_m beta sum_j a_mj q_nj; returns (bf16-rounded y as fp32, int64 acc).
+def row_scales(beta, N: int):
+    """The checkpoint scale of every output row n: beta_{g(n)} of Eq. (4)
+    (§III-D) with groups of N / len(beta) consecutive rows; a scalar is one
+    scale for the whole tensor."""
+    b = np.asarray(beta, dtype=np.float32)
+    if b.ndim == 0:
+        return b
+    assert N % b.size == 0
+    return np.repeat(b.ravel(), N // b.size)
 
-    a int8 [M, K], alpha fp32 [M], packed uint8 [N, K/4], beta fp32 scalar;
+
+def ternary_linear(a, alpha, packed, beta, q=None):
+    """y_mn = alpha_m beta_{g(n)} sum_j a_mj q_nj; returns (bf16-rounded y as fp32, int64 acc).
+
+    a int8 [M, K], alpha fp32 [M], packed uint8 [N, K/4], beta an fp32
+    scalar (per tensor) or [groups] (per group of N / groups output rows);
     q optionally the already unpacked int8 [N, K] (same values, saves decoding).
     The integer dot products are formed with fp64 products and sums of
     integers below 2^53, which are exact, then checked to be integral.
@@ -307,8 +323,24 @@ def ternary_linear(a, alpha, packed, beta, q=None):
     acc = acc64.astype(np.int64)
     assert np.array_equal(acc.astype(F64), acc64)
     assert np.all(np.abs(acc) < (1 << 24))
-    y = (acc.astype(np.float32) * np.asarray(alpha, dtype=np.float32)[:, None]) * np.float32(beta)
+    y = (acc.astype(np.float32) * np.asarray(alpha, dtype=np.float32)[:, None]) * row_scales(beta, acc.shape[1])
     return bf16_rne(y), acc
+
+
+def prefix_kv_w2a8(Z, w: dict, cfg):
+    """Eq. (2) with ternary prefix maps through Eq. (4): every prefix token
+    row of Z is quantised once (shared by W_K and W_V of every layer), and
+    K_C^l = bf16((acc alpha) beta), V_C^l likewise, returned as fp64."""
+    Z = np.asarray(Z, dtype=np.float32)
+    B, P, d = Z.shape
+    a, alpha = quantize_rows(Z.reshape(B * P, d))
+    K = np.empty((cfg.L, B, cfg.n_kv, P, cfg.d_h), dtype=F64)
+    V = np.empty_like(K)
+    for l in range(cfg.L):
+        for name, dst in (("wk_pre", K), ("wv_pre", V)):
+            y, _ = ternary_linear(a, alpha, w[name][l], w["beta_" + name][l])
+            dst[l] = y.astype(F64).reshape(B, P, cfg.n_kv, cfg.d_h).transpose(0, 2, 1, 3)
+    return K, V
 
 
 def velocity_w2a8(x, tau, Kc, Vc, w: dict, cfg, taps=None, prefix_visible=None):

@@ -384,7 +384,9 @@ def _torch_w2a8_map(u, packed, beta):
     a = torch.clamp(torch.round(u32 / alpha), -128, 127)
     q = _torch_unpack_ternary(packed).to(torch.float64)
     acc = a.to(torch.float64) @ q.transpose(0, 1)
-    y = (acc.to(torch.float32) * alpha) * torch.tensor(float(beta), dtype=torch.float32)
+    b = torch.from_numpy(np.atleast_1d(np.asarray(beta, dtype=np.float32)))
+    b = torch.repeat_interleave(b, acc.shape[1] // b.numel())  # one scale per group of output rows
+    y = (acc.to(torch.float32) * alpha) * b
     return y.to(torch.bfloat16).to(torch.float64)
 
 
@@ -575,3 +577,48 @@ def test_hidden_prefix_keys_equal_deleted_keys():
         xb, _ = O.denoise(noise[b:b + 1], Kc[:, b:b + 1][:, :, :, keep], Vc[:, b:b + 1][:, :, :, keep], w,
                           cfg.replace(B=1))
         np.testing.assert_allclose(xS[b:b + 1], xb, rtol=0, atol=1e-12)
+
+
+
+# ---------------------------------------------------------- W2A8 scale groups and ternary prefix maps (§III-D)
+
+def test_ternary_linear_group_scales_are_blockwise_tensor_scales():
+    """beta_{g(n)} per group of rows == the (pinned) per-tensor product on
+    each block of rows with that block's scale."""
+    rng = np.random.default_rng(21)
+    a = rng.integers(-127, 128, size=(5, 64)).astype(np.int8)
+    q = rng.integers(-1, 2, size=(32, 64)).astype(np.int8)
+    packed = O.pack_ternary(q)
+    alpha = rng.uniform(1e-3, 1.0, 5).astype(np.float32)
+    beta = rng.uniform(0.01, 0.1, 4).astype(np.float32)
+    y, acc = O.ternary_linear(a, alpha, packed, beta)
+    for g in range(4):
+        yg, ag = O.ternary_linear(a, alpha, packed[8 * g:8 * g + 8], beta[g])
+        assert np.array_equal(y[:, 8 * g:8 * g + 8], yg) and np.array_equal(acc[:, 8 * g:8 * g + 8], ag)
+
+
+def test_prefix_kv_w2a8_vs_library_routines():
+    """Ternary prefix maps: K_C, V_C equal, bit for bit, an independent torch
+    restatement of Eq. (4) on the prefix rows with per-group scales."""
+    cfg = PIN.replace(w2a8=True, dtype="bf16", w2a8_prefix=True, beta_group=4)
+    w = make_weights(cfg)
+    assert w["wk_pre"].dtype == np.uint8 and w["beta_wk_pre"].shape == (cfg.L, cfg.kvdim // 4)
+    Z, _ = make_observations(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    Zt = torch.from_numpy(Z.astype(np.float64)).reshape(-1, cfg.d_vlm)
+    for l in range(cfg.L):
+        for name, ref in (("wk_pre", Kc), ("wv_pre", Vc)):
+            y = _torch_w2a8_map(Zt, w[name][l], w["beta_" + name][l]).numpy()
+            y = y.reshape(cfg.B, cfg.P, cfg.n_kv, cfg.d_h).transpose(0, 2, 1, 3)
+            assert np.array_equal(y, ref[l])
+
+
+def test_w2a8_velocity_group_scales_vs_library_routines():
+    cfg = PIN.replace(w2a8=True, dtype="bf16", L=2, beta_group=8)
+    w = make_weights(cfg)
+    assert w["beta_wq"].shape == (cfg.L, cfg.qdim // 8)
+    Z, noise = make_observations(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    v = O.velocity_w2a8(noise, 0.4, Kc, Vc, w, cfg)
+    ref = _torch_velocity_w2a8(noise.astype(np.float64), 0.4, Kc, Vc, w, cfg)
+    np.testing.assert_allclose(v, ref, rtol=0, atol=1e-9)

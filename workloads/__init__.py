@@ -70,6 +70,8 @@ class ExpertConfig:
     w2a8: bool = False
     eps: float = 1e-6
     reverse: bool = False  # integration direction of the schedule: 0 -> 1, or 1 -> 0
+    beta_group: int = 0    # W2A8: output rows per weight-scale group (0: one scale per tensor)
+    w2a8_prefix: bool = False  # W2A8: the prefix K/V maps are ternary too
 
     def replace(self, **kw) -> "ExpertConfig":
         return dataclasses.replace(self, **kw)
@@ -160,7 +162,9 @@ def make_weights(cfg: ExpertConfig, zero: tuple = ()) -> dict:
     packed four per byte, code of input index j at bits 2*(j mod 4) of byte
     j // 4 (little-endian within the byte); key ``<name>`` holds the packed
     uint8 [L, out, in/4] array and ``beta_<name>`` the fp32 per-tensor scale
-    [L].  The scale is the expected absmean of an N(0, 1/fan_in) latent,
+    [L] (or, with ``beta_group`` > 0, one scale per group of that many output
+    rows, [L, out / beta_group]; with ``w2a8_prefix`` the prefix maps W_K, W_V
+    are ternary as well).  The scale is the expected absmean of an N(0, 1/fan_in) latent,
     sqrt(2/pi)/sqrt(fan_in), with a seeded +-5% jitter per (layer, tensor) so
     that a mixed-up scale index is visible.
 
@@ -173,14 +177,15 @@ def make_weights(cfg: ExpertConfig, zero: tuple = ()) -> dict:
     for name in WEIGHT_NAMES:
         shp = shapes[name]
         fan_in = shp[-1]
-        if cfg.w2a8 and name in TERNARY_NAMES:
+        if cfg.w2a8 and (name in TERNARY_NAMES or (cfg.w2a8_prefix and name in ("wk_pre", "wv_pre"))):
             if fan_in % 4:
                 raise ValueError(f"{name}: fan_in {fan_in} not a multiple of 4")
             codes = rng_t.integers(0, 3, size=shp, dtype=np.uint8)
             c = codes.reshape(shp[:-1] + (fan_in // 4, 4))
             packed = (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
+            groups = (cfg.L,) if cfg.beta_group == 0 else (cfg.L, shp[-2] // cfg.beta_group)
             beta = (math.sqrt(2.0 / math.pi) / math.sqrt(fan_in)) * (
-                1.0 + 0.05 * rng_t.uniform(-1.0, 1.0, size=(cfg.L,)))
+                1.0 + 0.05 * rng_t.uniform(-1.0, 1.0, size=groups))
             if name in zero:
                 packed = np.full_like(packed, 0x55)  # every code 1 -> q = 0
             out[name] = np.ascontiguousarray(packed)
