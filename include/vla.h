@@ -110,8 +110,15 @@ typedef struct {
 
 /* W2A8 weights: the six per-layer maps W_q, W_k, W_v, W_o, W_up, W_down are
  * ternary, packed uint8 [L][out][in/4] (code q+1 of input index j at bits
- * 2*(j mod 4) of byte j/4; code 3 is invalid), each with an fp32 scale per
- * layer (device pointer to [L] floats).  Everything else is bf16. */
+ * 2*(j mod 4) of byte j/4; code 3 is invalid), each with fp32 scales
+ * beta_{g(n)} of Eq. (4): with beta_group == 0 one scale per tensor and layer
+ * ([L] floats), else one per group of beta_group consecutive output rows
+ * ([L][out / beta_group] floats; beta_group must divide every map's rows, a
+ * multiple of 4).  The prefix maps are bf16 (wk_pre, wv_pre) unless
+ * wk_pre_t / wv_pre_t are given: then they are ternary too ([L][n_kv*d_h]
+ * [d_vlm/4], scales beta_wk_pre / beta_wv_pre grouped like the others, wk_pre
+ * and wv_pre ignored) and vla_prefix_kv_build quantises each prefix row of Z
+ * per Eq. (4) before the ternary product.  Everything else is bf16. */
 typedef struct {
   const void* wk_pre;
   const void* wv_pre;
@@ -133,6 +140,11 @@ typedef struct {
   const void* wt1;
   const void* wt2;
   const void* wmod_f;
+  int beta_group;          /* 0: per-tensor scales; else output rows per scale group */
+  const uint8_t* wk_pre_t; /* NULL, or ternary prefix W_K [L][n_kv*d_h][d_vlm/4] */
+  const uint8_t* wv_pre_t; /* NULL, or ternary prefix W_V (both or neither) */
+  const float* beta_wk_pre;
+  const float* beta_wv_pre;
 } vla_expert_weights_w2a8;
 
 typedef struct vla_expert vla_expert;

@@ -62,8 +62,12 @@ class VlaWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in DENSE_FIELDS]
 
 
+W2A8_PREFIX_FIELDS = ("wk_pre_t", "wv_pre_t", "beta_wk_pre", "beta_wv_pre")
+
+
 class VlaWeightsW2A8(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in W2A8_FIELDS]
+    _fields_ = [(n, ctypes.c_void_p) for n in W2A8_FIELDS] + [("beta_group", ctypes.c_int)] + [
+        (n, ctypes.c_void_p) for n in W2A8_PREFIX_FIELDS]
 
 
 _lib = None
@@ -143,7 +147,7 @@ def upload_weights(w: dict, dtype: str, w2a8: bool, device="cuda") -> dict:
     are already bf16-representable)."""
     out = {}
     for k, v in w.items():
-        if k not in DENSE_FIELDS and k not in W2A8_FIELDS:
+        if k not in DENSE_FIELDS and k not in W2A8_FIELDS and k not in ("beta_wk_pre", "beta_wv_pre"):
             continue
         t = torch.from_numpy(v)
         if t.dtype == torch.float32 and not k.startswith("beta_"):
@@ -169,7 +173,12 @@ class Expert:
         self._c = c
         h = ctypes.c_void_p()
         if self.w2a8:
-            ws = VlaWeightsW2A8(**{n: weights[n].data_ptr() for n in W2A8_FIELDS})
+            fields = {n: weights[n].data_ptr() for n in W2A8_FIELDS if n in weights}
+            if weights["wk_pre"].dtype == torch.uint8:  # ternary prefix maps
+                fields.update(wk_pre_t=weights["wk_pre"].data_ptr(), wv_pre_t=weights["wv_pre"].data_ptr(),
+                              beta_wk_pre=weights["beta_wk_pre"].data_ptr(),
+                              beta_wv_pre=weights["beta_wv_pre"].data_ptr(), wk_pre=0, wv_pre=0)
+            ws = VlaWeightsW2A8(**fields, beta_group=int(getattr(cfg, "beta_group", 0)))
             st = lib().vla_expert_create_w2a8(ctypes.byref(c), ctypes.byref(ws), self.S, _stream(stream),
                                               ctypes.byref(h))
         else:

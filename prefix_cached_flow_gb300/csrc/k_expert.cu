@@ -733,6 +733,26 @@ __global__ void k_quant_rows_v(int K, const float* x, void* codes, float* alpha)
   if (threadIdx.x == 0) alpha[t] = al;
 }
 
+// Eq. (4) on bf16 rows (the prefix hidden states Z of the W2A8 prefix build):
+// the same row quantiser on the exact fp32 values of the bf16 inputs.
+__global__ void k_quant_rows_bf16(int K, const bf16* x, bf16* codes, float* alpha) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + K;
+  const int t = blockIdx.x;
+  for (int i = threadIdx.x; i < K; i += blockDim.x) row[i] = __bfloat162float(x[(size_t)t * K + i]);
+  __syncthreads();
+  const float al = quantize_row_block(row, K, nullptr, codes + (size_t)t * K, red);
+  if (threadIdx.x == 0) alpha[t] = al;
+}
+
+// Per-output-row weight scales from per-group ones (beta_{g(n)} of Eq. (4)):
+// dst[l * stride + off + n] = src[l * (N / G) + n / G].
+__global__ void k_expand_scales(float* dst, const float* src, int L, int N, int G, int stride, int off) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x, l = blockIdx.y;
+  if (n < N && l < L) dst[(size_t)l * stride + off + n] = src[(size_t)l * (N / G) + n / G];
+}
+
 // A bounded wait that cannot be satisfied: the mbarrier expects two arrivals
 // and gets one.  The wait runs out after the handle's limit, latches
 // VLA_DEV_TIMEOUT and the kernel returns (nothing is left in flight).
@@ -787,6 +807,8 @@ cudaError_t expert_kernels_init() {
   e = set_max_dyn_smem(k_reduce_gelu<bf16>);
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_quant_norm);
+  if (e != cudaSuccess) return e;
+  e = set_max_dyn_smem(k_quant_rows_bf16);
   if (e != cudaSuccess) return e;
   e = set_max_dyn_smem(k_quant_rows<false>);
   if (e != cudaSuccess) return e;
@@ -882,6 +904,19 @@ cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* 
 
 cudaError_t launch_quant_rows_i8(int T, int K, const float* x, int8_t* codes, float* alpha, cudaStream_t st) {
   return launch_quant_rows_any(T, K, x, codes, true, alpha, st);
+}
+
+cudaError_t launch_quant_rows_bf16(int T, int K, const bf16* x, bf16* codes, float* alpha, cudaStream_t st) {
+  const size_t smem = (size_t)(K + 32) * sizeof(float);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  k_quant_rows_bf16<<<T, 256, smem, st>>>(K, x, codes, alpha);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand_scales(float* dst, const float* src, int L, int N, int G, int stride, int off,
+                                 cudaStream_t st) {
+  k_expand_scales<<<dim3((N + 255) / 256, L), 256, 0, st>>>(dst, src, L, N, G, stride, off);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_expire_wait(int* status, cudaStream_t st) {

@@ -332,9 +332,11 @@ __global__ void __launch_bounds__(128, 1)
     const int n = m0 + row;
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
     float* wss = (float*)(smem + Ls.wss);
-    int slot = g.beta_slot;
+    int slot = 0;
     if (EPI == EPI_QKV) slot = n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2);
-    const float be = AMODE == 1 ? (g.wbeta ? g.wbeta[g.layer * 6 + slot] : g.beta_val) : 0.f;
+    const float be = (AMODE == 1 && n < g.N)
+                         ? (g.wbeta ? g.wbeta[(size_t)g.layer * g.beta_stride + g.beta_off + n] : g.beta_val)
+                         : 0.f;
     for (int c0 = 0; c0 < tcols; c0 += 16) {
       float v[16];
       if (ok) {
@@ -367,6 +369,16 @@ __global__ void __launch_bounds__(128, 1)
           } else if (EPI == EPI_W2A8_OUT) {
             g.yout[(size_t)t * g.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
             if (g.accout) g.accout[(size_t)t * g.N + n] = (int32_t)v[j];
+          } else if (EPI == EPI_KV) {
+            // prefix cache (Eq. 2): row n = [layer][K | V][kv head][d], token t = [b][p]
+            const int kl = n / (2 * g.kvdim), rem = n - kl * 2 * g.kvdim, kw = rem / g.kvdim;
+            const int r2 = rem - kw * g.kvdim, gk = r2 / g.d_h, d = r2 - gk * g.d_h;
+            const int b = t / g.kv_P, p = t - b * g.kv_P;
+            const size_t head = ((size_t)kl * g.kv_B + b) * g.n_kv + gk;
+            if (kw == 0)
+              g.kc_out[(head * g.kv_P + p) * g.d_h + d] = __float2bfloat16_rn(y);
+            else
+              g.vc_out[(head * g.d_h + d) * g.kv_P8 + p] = __float2bfloat16_rn(y);
           } else {  // EPI_QKV
             const int b = t / g.H, i = t - b * g.H;
             const bf16 bv = __float2bfloat16_rn(y);
@@ -433,12 +445,13 @@ __global__ void __launch_bounds__(128, 1)
     const float4 raw = acc;
     if (AMODE == 1 && valid) {
       // Eq. (4): exact integer accumulators scaled to bf16
-      const int slot = EPI == EPI_QKV ? (n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2)) : g.beta_slot;
-      const float al = g.alpha[t], be = g.wbeta ? g.wbeta[g.layer * 6 + slot] : g.beta_val;
-      acc.x = w2a8_scale(acc.x, al, be);
-      acc.y = w2a8_scale(acc.y, al, be);
-      acc.z = w2a8_scale(acc.z, al, be);
-      acc.w = w2a8_scale(acc.w, al, be);
+      const float al = g.alpha[t];
+      const float4 be = g.wbeta ? *(const float4*)(g.wbeta + (size_t)g.layer * g.beta_stride + g.beta_off + n)
+                                : make_float4(g.beta_val, g.beta_val, g.beta_val, g.beta_val);
+      acc.x = w2a8_scale(acc.x, al, be.x);
+      acc.y = w2a8_scale(acc.y, al, be.y);
+      acc.z = w2a8_scale(acc.z, al, be.z);
+      acc.w = w2a8_scale(acc.w, al, be.w);
       if (EPI != EPI_W2A8_OUT && g.accout)  // diagnostic tap of the exact accumulators
         *(int4*)(g.accout + (size_t)t * g.N + n) = make_int4((int)raw.x, (int)raw.y, (int)raw.z, (int)raw.w);
     }
@@ -612,6 +625,7 @@ cudaError_t linear_kernels_init() {
   if (e == cudaSuccess) e = init_one<EPI_RESID, 1, 0>();
   if (e == cudaSuccess) e = init_one<EPI_GELU, 1, 0>();
   if (e == cudaSuccess) e = init_one<EPI_W2A8_OUT, 1, 0>();
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_linear<EPI_KV, 1, 0, 1>);
   return e;
 }
 
@@ -638,6 +652,7 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
   VLA_LIN_CASE(EPI_GELU, 1, 0)
   VLA_LIN_CASE(EPI_W2A8_OUT, 1, 0)
 #undef VLA_LIN_CASE
+  if (g.epi == EPI_KV) fn = (g.amode == 1 && C == 1) ? k_linear<EPI_KV, 1, 0, 1> : nullptr;
   if (!fn) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles_n, tiles_t, C);

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
     const int hbn = BN / 2;
-    int slot = g.beta_slot;
+    int slot = 0;  // q, k or v (EPI_QKV), from the tile's rows
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
       const int buf = lt & 1;

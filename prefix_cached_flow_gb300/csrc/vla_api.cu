@@ -68,7 +68,13 @@ struct vla_expert {
   void* wo = nullptr;       // [L][D][qdim]
   void* wup = nullptr;      // [L][F][D]
   void* wdown = nullptr;    // [L][D][F]
-  float* beta = nullptr;    // [L][6] (W2A8)
+  float* beta = nullptr;    // [L][6] per-tensor scales (W2A8, CUDA-core path)
+  float* beta_rows = nullptr;  // [L][qkvdim + D + F + D] per-output-row scales (W2A8)
+  int beta_stride = 0, beta_group = 0;
+  bool tpre = false;             // ternary prefix maps (W2A8 prefix build)
+  float* beta_pre_rows = nullptr;  // [L][2 kvdim] their per-row scales
+  void* zcodes = nullptr;          // Eq. (4) codes of the prefix rows (bf16 carriers)
+  float* zalpha = nullptr;
   float* win = nullptr;     // [D][d_a]
   float* wout = nullptr;    // [d_a][D]
   float* modtab = nullptr;  // [S][L][4][D]
@@ -399,7 +405,7 @@ LinArgs lin_args(const vla_expert* h, const LinPlan& p, int N, int T, int layer)
   a.xpart = h->xpart; a.xss = h->xss;
   a.layer = layer;
   if (h->w2a8) {
-    a.amode = 1; a.w2a8 = 1; a.alpha = h->alpha; a.wbeta = h->beta;
+    a.amode = 1; a.w2a8 = 1; a.alpha = h->alpha; a.wbeta = h->beta_rows; a.beta_stride = h->beta_stride;
   }
   return a;
 }
@@ -654,7 +660,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       VLA_CK(cp(l, 10, h->alpha));
       a = lin_args(h, po, D, T, l);
       a.tl = tls(2);
-      a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_slot = 3;  // the quantiser reads h itself
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_off = h->qkvdim;  // the quantiser reads h itself
       a.accout = (int32_t*)tp(l, 11);
       VLA_CK(launch_linear(&h->tm_wo, &tm_o, &tmH, a, po.tiles_n, po.tiles_t, po.C, st));
       VLA_CK(cp(l, 12, h->h));
@@ -663,7 +669,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       VLA_CK(cp(l, 15, h->alpha));
       a = lin_args(h, pu, F, T, l);
       a.tl = tls(3);
-      a.epi = EPI_GELU; a.g32 = h->f32buf; a.ldg = F; a.beta_slot = 4;
+      a.epi = EPI_GELU; a.g32 = h->f32buf; a.ldg = F; a.beta_off = h->qkvdim + D;
       a.accout = (int32_t*)tp(l, 16);
       VLA_CK(launch_linear(&h->tm_wup, &tm_u, &tmH, a, pu.tiles_n, pu.tiles_t, pu.C, st));
       VLA_CK(cp(l, 17, h->f32buf));
@@ -672,7 +678,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       VLA_CK(cp(l, 19, h->alpha));
       a = lin_args(h, pd, D, T, l);
       a.tl = tls(4);
-      a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_slot = 5;
+      a.epi = EPI_RESID; a.h = h->h; a.ss_out = nullptr; a.beta_off = h->qkvdim + D + F;
       a.accout = (int32_t*)tp(l, 20);
       VLA_CK(launch_linear(&h->tm_wdown, &tm_g, &tmH, a, pd.tiles_n, pd.tiles_t, pd.C, st));
       VLA_CK(cp(l, 21, h->h));
@@ -1039,7 +1045,8 @@ void vla_expert_destroy(vla_expert* h) {
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
                   h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf,
-                  h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar, h->noise_buf};
+                  h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar, h->noise_buf,
+                  h->beta_rows, h->beta_pre_rows, h->zcodes, h->zalpha};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -1100,11 +1107,23 @@ vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert
                                   void* stream, vla_expert** out) {
   if (!out || !w) return VLA_ERR_INVALID_ARG;
   *out = nullptr;
-  const void* ptrs[] = {w->wk_pre, w->wv_pre, w->wq, w->wk, w->wv, w->wo, w->wup, w->wdown, w->beta_wq,
+  const bool tpre = w->wk_pre_t || w->wv_pre_t;  // ternary prefix maps
+  if (tpre && (!w->wk_pre_t || !w->wv_pre_t || !w->beta_wk_pre || !w->beta_wv_pre)) return VLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->wq, w->wk, w->wv, w->wo, w->wup, w->wdown, w->beta_wq,
                         w->beta_wk, w->beta_wv, w->beta_wo, w->beta_wup, w->beta_wdown, w->wmod, w->win,
                         w->wout, w->wt1, w->wt2, w->wmod_f};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return VLA_ERR_INVALID_ARG;
+  if (tpre) {
+    if (!aligned16(w->wk_pre_t) || !aligned16(w->wv_pre_t) || !aligned16(w->beta_wk_pre) || !aligned16(w->beta_wv_pre))
+      return VLA_ERR_INVALID_ARG;
+  } else if (!w->wk_pre || !w->wv_pre || !aligned16(w->wk_pre) || !aligned16(w->wv_pre)) {
+    return VLA_ERR_INVALID_ARG;
+  }
+  if (cfg) {  // scale groups must divide every map's rows
+    const int G = w->beta_group, qd = cfg->n_q_heads * cfg->head_dim, kd = cfg->n_kv_heads * cfg->head_dim;
+    if (G < 0 || (G > 0 && (G % 4 || qd % G || kd % G || cfg->width % G || cfg->mlp_width % G))) return VLA_ERR_SHAPE;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   vla_expert* h = nullptr;
   vla_status s = create_common(cfg, n_steps, true, st, &h);
@@ -1113,35 +1132,55 @@ vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert
     return s;
   }
   const vla_expert_config& c = *cfg;
-  const int L = c.n_layers, D = c.width, F = c.mlp_width;
-  const size_t kvb = (size_t)h->kvdim * c.vlm_hidden * 2;
+  const int L = c.n_layers, D = c.width, F = c.mlp_width, G = w->beta_group;
+  const size_t kvb = tpre ? (size_t)h->kvdim * (c.vlm_hidden / 4) : (size_t)h->kvdim * c.vlm_hidden * 2;
   const size_t qb = (size_t)h->qdim * (D / 4), kb = (size_t)h->kvdim * (D / 4);
   const size_t ob = (size_t)D * (h->qdim / 4), ub = (size_t)F * (D / 4), db = (size_t)D * (F / 4);
+  h->beta_stride = h->qkvdim + D + F + D;
   if ((s = dalloc(&h->wkv_pre, 2 * kvb * L)) != VLA_OK || (s = dalloc(&h->wqkv, (qb + 2 * kb) * L)) != VLA_OK ||
       (s = dalloc(&h->wo, ob * L)) != VLA_OK || (s = dalloc(&h->wup, ub * L)) != VLA_OK ||
-      (s = dalloc(&h->wdown, db * L)) != VLA_OK || (s = dalloc(&h->beta, (size_t)L * 6 * 4)) != VLA_OK) {
+      (s = dalloc(&h->wdown, db * L)) != VLA_OK || (s = dalloc(&h->beta, (size_t)L * 6 * 4)) != VLA_OK ||
+      (s = dalloc(&h->beta_rows, (size_t)L * h->beta_stride * 4)) != VLA_OK ||
+      (tpre && (s = dalloc(&h->beta_pre_rows, (size_t)L * 2 * h->kvdim * 4)) != VLA_OK)) {
     vla_expert_destroy(h);
     return s;
   }
-  cudaError_t e = stack_rows(h->wkv_pre, 2 * kvb, w->wk_pre, kvb, L, 0, st);
-  if (e == cudaSuccess) e = stack_rows(h->wkv_pre, 2 * kvb, w->wv_pre, kvb, L, kvb, st);
+  h->beta_group = G;
+  h->tpre = tpre;
+  cudaError_t e = stack_rows(h->wkv_pre, 2 * kvb, tpre ? (const void*)w->wk_pre_t : w->wk_pre, kvb, L, 0, st);
+  if (e == cudaSuccess)
+    e = stack_rows(h->wkv_pre, 2 * kvb, tpre ? (const void*)w->wv_pre_t : w->wv_pre, kvb, L, kvb, st);
   if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wq, qb, L, 0, st);
   if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wk, kb, L, qb, st);
   if (e == cudaSuccess) e = stack_rows(h->wqkv, qb + 2 * kb, w->wv, kb, L, qb + kb, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(h->wo, w->wo, ob * L, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(h->wup, w->wup, ub * L, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(h->wdown, w->wdown, db * L, cudaMemcpyDeviceToDevice, st);
+  // scales: per output row, [L][q | k | v | o | up | down rows] (beta_{g(n)} of Eq. 4)
   const float* betas[6] = {w->beta_wq, w->beta_wk, w->beta_wv, w->beta_wo, w->beta_wup, w->beta_wdown};
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
-    e = cudaMemcpy2DAsync(h->beta + i, 6 * sizeof(float), betas[i], sizeof(float), sizeof(float), L,
-                          cudaMemcpyDeviceToDevice, st);
+  const int rows[6] = {h->qdim, h->kvdim, h->kvdim, D, F, D};
+  int off = 0;
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) {
+    e = launch_expand_scales(h->beta_rows, betas[i], L, rows[i], G ? G : rows[i], h->beta_stride, off, st);
+    off += rows[i];
+  }
+  if (G == 0)  // per-tensor table of the CUDA-core path
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+      e = cudaMemcpy2DAsync(h->beta + i, 6 * sizeof(float), betas[i], sizeof(float), sizeof(float), L,
+                            cudaMemcpyDeviceToDevice, st);
+  if (tpre && e == cudaSuccess) {  // prefix rows [L][K | V][kvdim]
+    e = launch_expand_scales(h->beta_pre_rows, w->beta_wk_pre, L, h->kvdim, G ? G : h->kvdim, 2 * h->kvdim, 0, st);
+    if (e == cudaSuccess)
+      e = launch_expand_scales(h->beta_pre_rows, w->beta_wv_pre, L, h->kvdim, G ? G : h->kvdim, 2 * h->kvdim,
+                               h->kvdim, st);
+  }
   // reject packed bytes that hold the invalid code 3
   int* bad = nullptr;
   if (e == cudaSuccess) e = cudaMalloc((void**)&bad, sizeof(int));
   if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), st);
-  const void* packed[4] = {h->wqkv, h->wo, h->wup, h->wdown};
-  const size_t pbytes[4] = {(qb + 2 * kb) * L, ob * L, ub * L, db * L};
-  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+  const void* packed[5] = {h->wqkv, h->wo, h->wup, h->wdown, h->wkv_pre};
+  const size_t pbytes[5] = {(qb + 2 * kb) * L, ob * L, ub * L, db * L, 2 * kvb * L};
+  for (int i = 0; i < (tpre ? 5 : 4) && e == cudaSuccess; ++i)
     e = launch_check_ternary_codes((const uint8_t*)packed[i], pbytes[i], bad, st);
   int hbad = 0;
   if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
@@ -1154,6 +1193,14 @@ vla_status vla_expert_create_w2a8(const vla_expert_config* cfg, const vla_expert
   if (hbad) {
     vla_expert_destroy(h);
     return VLA_ERR_INVALID_ARG;
+  }
+  if (tpre) {
+    // the prefix rows' Eq. (4) codes (bf16 carriers) and scales for max_batch x max_prefix tokens
+    const size_t rowsz = (size_t)c.max_batch * c.max_prefix;
+    if ((s = dalloc(&h->zcodes, rowsz * c.vlm_hidden * 2)) != VLA_OK || (s = dalloc(&h->zalpha, rowsz * 4)) != VLA_OK) {
+      vla_expert_destroy(h);
+      return s;
+    }
   }
   s = finish_create(h, w->wt1, w->wt2, w->wmod, w->wmod_f, w->win, w->wout, st);
   if (s != VLA_OK) {
@@ -1178,6 +1225,28 @@ vla_status vla_prefix_kv_build(vla_expert* h, const void* Z, int B, int P, void*
   cudaStream_t st = (cudaStream_t)stream;
   const int BP = B * P, N = c.n_layers * 2 * h->kvdim, K = c.vlm_hidden;
   KvScatter kv{Kc, Vc, c.n_layers, B, c.n_kv_heads, P, c.head_dim, round_up(P, 8)};
+  if (h->tpre) {
+    // Ternary prefix maps (Eq. 4): quantise every prefix row of Z once, then
+    // one packed-ternary product over all layers' K and V rows with the
+    // cache scatter in its epilogue (no split: hundreds of row tiles).
+    VLA_CK(launch_quant_rows_bf16(BP, K, (const bf16*)Z, (bf16*)h->zcodes, h->zalpha, st));
+    LinArgs g{};
+    g.N = N; g.T = BP; g.a_row0 = 0; g.KS = K; g.BN = BP >= 256 ? 256 : round_up(BP < 16 ? 16 : BP, 16);
+    const int per_stage = 128 * 128 + g.BN * 128 + 128 * 16;
+    g.stages = (200 * 1024) / per_stage;
+    if (g.stages > 8) g.stages = 8;
+    if (g.stages > K / 64) g.stages = K / 64;
+    g.bmode = 0; g.amode = 1; g.w2a8 = 1; g.epi = EPI_KV;
+    g.alpha = h->zalpha; g.wbeta = h->beta_pre_rows; g.beta_stride = 0; g.beta_off = 0; g.layer = 0;
+    g.n_kv = c.n_kv_heads; g.d_h = c.head_dim; g.kvdim = h->kvdim;
+    g.kc_out = (bf16*)Kc; g.vc_out = (bf16*)Vc; g.kv_B = B; g.kv_P = P; g.kv_P8 = round_up(P, 8);
+    g.status = h->d_status; g.D = K;
+    CUtensorMap tmA, tmB;
+    if (tc_encode_2d_u8(&tmA, h->wkv_pre, K / 4, N, 16, 128) || tc_encode_2d_bf16(&tmB, h->zcodes, K, BP, 64, g.BN))
+      return VLA_ERR_CUDA;
+    VLA_CK(launch_linear(&tmA, &tmB, &tmB, g, cdiv(N, 128), cdiv(BP, g.BN), 1, st));
+    return VLA_OK;
+  }
   if (!h->use_tc) {
     VLA_CK(launch_gemm_simt(!h->f32, Z, K, !h->f32, h->wkv_pre, K, BP, N, K, 1, nullptr, 0, 0, &kv, st));
     return VLA_OK;
@@ -1228,6 +1297,7 @@ static vla_status denoise_impl(vla_expert* h, bool w2a8, const void* Kc, const v
     if (h->fused)
       return h->w2a8 ? enqueue_denoise_w2a8_fused(h, Kc, Vc, B, P, noise, actions, tap, s2)
                      : enqueue_denoise_fused(h, Kc, Vc, B, P, noise, actions, tap, s2);
+    if (h->w2a8 && h->beta_group) return VLA_ERR_UNSUPPORTED;  // the CUDA-core W2A8 path has per-tensor scales
     return enqueue_denoise(h, Kc, Vc, B, P, noise, actions, tap, s2);
   };
   if ((h->cfg.flags & VLA_FLAG_NO_GRAPH) || h->tap) return enqueue(st);

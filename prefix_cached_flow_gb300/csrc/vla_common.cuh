@@ -565,10 +565,11 @@ struct LinArgs {
   // W2A8 (Eq. 4): the accumulators are exact integers; y = bf16((acc * alpha_t) * beta)
   int w2a8;
   const float* alpha;  // [T] per-token activation scales
-  const float* wbeta;  // [L][6] per-tensor weight scales (q, k, v, o, up, down); null: beta_val
+  const float* wbeta;  // per-output-row weight scales beta_{g(n)}: row n of this map at
+                       // wbeta[layer * beta_stride + beta_off + n]; null: beta_val for every row
   float beta_val;
   int layer;
-  int beta_slot;       // 3 (o), 4 (up), 5 (down); QKV picks 0/1/2 by output row
+  int beta_stride, beta_off;
   float* g32;          // EPI_GELU with W2A8: fp32 GeLU output [T][ldg] (quantised next)
   uint16_t* yout;      // EPI_W2A8_OUT: bf16 bits [T][N]
   int32_t* accout;     // EPI_W2A8_OUT: int32 accumulators [T][N] (nullable)
@@ -607,6 +608,9 @@ cudaError_t linear_kernels_init();
 // tmH: fp32 map over h [T][D] with box 64 x BN (no swizzle), used by bmode 1.
 cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& g,
                           int tiles_n, int tiles_t, int C, cudaStream_t st);
+
+// cudaError_t launch_linear also takes EPI_KV with packed ternary weights
+// (AMODE 1, no split): the W2A8 prefix cache build.
 
 // Persistent many-token linear kernel (k_linear_wide.cu): same LinArgs and
 // epilogues (EPI_QKV, EPI_RESID, EPI_GELU, and EPI_KV for the prefix K/V
@@ -781,6 +785,11 @@ cudaError_t launch_quant_norm(const ExpertDims& d, const float* h, const float* 
 cudaError_t launch_quant_rows(int T, int K, const float* x, bf16* codes, float* alpha, cudaStream_t st);
 // The same quantiser writing int8 codes (the standalone Eq. (4) entry point).
 cudaError_t launch_quant_rows_i8(int T, int K, const float* x, int8_t* codes, float* alpha, cudaStream_t st);
+// Eq. (4) on bf16 rows (W2A8 prefix build): bf16 carriers of the codes and alpha.
+cudaError_t launch_quant_rows_bf16(int T, int K, const bf16* x, bf16* codes, float* alpha, cudaStream_t st);
+// dst[l * stride + off + n] = src[l * (N / G) + n / G] for n < N, l < L.
+cudaError_t launch_expand_scales(float* dst, const float* src, int L, int N, int G, int stride, int off,
+                                 cudaStream_t st);
 // One kernel whose bounded wait cannot be satisfied (exercises the timeout latch).
 cudaError_t launch_expire_wait(int* status, cudaStream_t st);
 cudaError_t launch_i8_to_bf16(const int8_t* a, bf16* out, size_t n, cudaStream_t st);

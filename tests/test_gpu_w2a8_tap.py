@@ -70,9 +70,10 @@ def _ternary(w, name, l, a, alpha, beta):
     return y, acc
 
 
-@pytest.mark.parametrize("name,step", [("w2a8_b1", 1), ("w2a8_b16", 3)])
-def test_w2a8_solver_ops_bit_exact(name, step):
-    cfg = CONFIGS[name]
+@pytest.mark.parametrize("name,step,group", [("w2a8_b1", 1, 0), ("w2a8_b16", 3, 0), ("w2a8_b1", 2, 128)])
+def test_w2a8_solver_ops_bit_exact(name, step, group):
+    """group > 0: one weight scale per group of that many output rows."""
+    cfg = CONFIGS[name].replace(beta_group=group)
     w, recs, kc, vc, x, tau = _run_tapped(cfg, step)
     B, H, D = cfg.B, cfg.H, cfg.D
     T = B * H
