@@ -88,6 +88,10 @@ typedef struct {
   float rms_eps;   /* RMSNorm epsilon (1e-6) */
   unsigned flags;  /* VLA_FLAG_* (0 for normal use) */
   int schedule;    /* vla_schedule */
+  int cross_every; /* 0: every layer is joint attention over [K_C ; action keys]; k > 0: layers l with
+                      l mod k == k - 1 are cross-attention layers whose queries see the cached prefix
+                      keys only (the alternating joint / cross design, §III-B); their W_k, W_v rows
+                      are unused.  A prefix mask must then leave each observation a visible key. */
 } vla_expert_config;
 
 /* Dense weights, device pointers of the config dtype, shapes [..][out][in]. */
@@ -360,6 +364,18 @@ vla_status vla_w2a8_ternary_gemm_noalloc(const int8_t* a_dev, const float* alpha
  * |error| <= 1.5e-7, with approximate reciprocal and exponential), both for
  * n fp32 inputs x_dev into exact_dev and fast_dev. */
 vla_status vla_debug_gelu_forms(const float* x_dev, int n, float* exact_dev, float* fast_dev, void* stream);
+
+/* Selected FFN neurons (the rMuscle Action Cache: during the memory-bound
+ * denoising loop the expert evaluates only chosen MLP neurons).  idx_dev
+ * int32 [L][F_sel]: strictly increasing neuron indices in [0, F) per layer.
+ * Builds handle-owned compact copies of the selected rows of W_up and
+ * columns of W_down (allocated by the first selection), after which every
+ * denoise call on this handle streams only those (MLP width F_sel); F_sel = 0
+ * restores the full MLP.  F_sel must be a multiple of 128.  Dense bf16
+ * handles on the tensor-core path only (else VLA_ERR_UNSUPPORTED); bad
+ * indices -> VLA_ERR_INVALID_ARG with the previous state kept.  Synchronises
+ * `stream`; drops the handle's captured graphs. */
+vla_status vla_expert_select_ffn(vla_expert* h, const int32_t* idx_dev, int F_sel, void* stream);
 
 /* Number of kernels one denoise call launches for batch B and prefix P
  * (all of them inside the one graph launch).  Host-only arithmetic. */

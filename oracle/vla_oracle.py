@@ -63,7 +63,7 @@ __all__ = [
     "denoise", "denoise_recompute", "quantize_rows", "pack_ternary",
     "unpack_ternary", "bf16_rne", "ternary_linear", "velocity_w2a8", "with_unpacked",
     "denoise_w2a8", "parity_metrics", "philox4x64", "gaussian_noise", "prefix_mask_bits",
-    "row_scales", "prefix_kv_w2a8",
+    "row_scales", "prefix_kv_w2a8", "select_ffn_neurons",
 ]
 
 
@@ -137,24 +137,25 @@ def prefix_kv(Z, w: dict, cfg):
     return K, V
 
 
-def joint_attention(q, k_s, v_s, Kc, Vc, prefix_visible=None):
+def joint_attention(q, k_s, v_s, Kc, Vc, prefix_visible=None, suffix: bool = True):
     """Eq. (2) per head with suffix keys/values appended to the cached prefix.
 
     q [B, H, n_q, d_h]; k_s, v_s [B, H, n_kv, d_h]; Kc, Vc [B, n_kv, P, d_h].
     prefix_visible: optional bool [B, P]; a hidden prefix key gets M = -inf.
-    Suffix keys are always visible.  Two passes per query row: the row
-    maximum, then the exponentials, their sum and the weighted values.
+    Suffix keys are always visible; suffix=False gives cross-attention (the
+    queries see the cached prefix keys only).  Two passes per query row: the
+    row maximum, then the exponentials, their sum and the weighted values.
     """
     B, H, n_q, d_h = q.shape
-    n_kv = k_s.shape[2]
+    n_kv = Kc.shape[1]
     group = n_q // n_kv
     scale = 1.0 / math.sqrt(d_h)
     o = np.empty((B, H, n_q, d_h), dtype=F64)
     for b in range(B):
         for j in range(n_q):
             g = j // group
-            keys = np.concatenate([Kc[b, g], k_s[b, :, g]], axis=0)
-            vals = np.concatenate([Vc[b, g], v_s[b, :, g]], axis=0)
+            keys = np.concatenate([Kc[b, g], k_s[b, :, g]], axis=0) if suffix else Kc[b, g]
+            vals = np.concatenate([Vc[b, g], v_s[b, :, g]], axis=0) if suffix else Vc[b, g]
             s = (q[b, :, j] @ keys.T) * scale  # [H, P + H]
             if prefix_visible is not None:
                 M = np.zeros(keys.shape[0], dtype=F64)
@@ -182,7 +183,11 @@ def _expert(x, mods, Kc, Vc, w, cfg, lin, taps=None, prefix_visible=None):
         q = lin(u, "wq", l).reshape(B, H, cfg.n_q, cfg.d_h)
         ks = lin(u, "wk", l).reshape(B, H, cfg.n_kv, cfg.d_h)
         vs = lin(u, "wv", l).reshape(B, H, cfg.n_kv, cfg.d_h)
-        o = joint_attention(q, ks, vs, Kc[l], Vc[l], prefix_visible).reshape(B, H, cfg.qdim)
+        # the alternating joint / cross design: every cross_every-th layer
+        # attends to the cached prefix only
+        ce = getattr(cfg, "cross_every", 0)
+        cross = ce > 0 and l % ce == ce - 1
+        o = joint_attention(q, ks, vs, Kc[l], Vc[l], prefix_visible, suffix=not cross).reshape(B, H, cfg.qdim)
         if taps is not None:
             taps.setdefault("attn", []).append(o)
         h = h + lin(o, "wo", l)
@@ -199,6 +204,19 @@ def velocity(x, tau, Kc, Vc, w: dict, cfg, taps=None, prefix_visible=None):
     mods = time_conditioning(w, cfg, tau)
     return _expert(x, mods, Kc, Vc, w, cfg, lambda u, n, l: linear(u, w[n][l]),
                    taps, prefix_visible)
+
+
+def select_ffn_neurons(w: dict, idx) -> dict:
+    """The expert with only the selected FFN neurons of every layer
+    (rMuscle's Action Cache: the memory-bound denoising loop evaluates a
+    subset of MLP neurons): idx [L][F_sel] neuron indices; W_up keeps rows
+    idx[l], W_down keeps columns idx[l].  Returns a weight dict whose MLP width
+    is F_sel; every other weight is shared."""
+    out = dict(w)
+    idx = np.asarray(idx)
+    out["wup"] = np.stack([w["wup"][l][idx[l]] for l in range(idx.shape[0])])
+    out["wdown"] = np.stack([w["wdown"][l][:, idx[l]] for l in range(idx.shape[0])])
+    return out
 
 
 def schedule(S: int, reverse: bool = False) -> np.ndarray:

@@ -30,7 +30,8 @@ EXPORTED = ("vla_expert_create", "vla_expert_create_w2a8", "vla_expert_destroy",
             "vla_expert_poll_status", "vla_expert_set_abort", "vla_w2a8_quantize_rows",
             "vla_w2a8_ternary_gemm", "vla_expert_launch_count", "vla_status_string", "vla_version", "vla_last_error",
             "vla_expert_set_wait_limit", "vla_expert_check_wait_timeout", "vla_expert_w2a8_tap_bytes",
-            "vla_expert_set_w2a8_tap", "vla_debug_gelu_forms", "vla_action_denoise_ex", "vla_noise_fill")
+            "vla_expert_set_w2a8_tap", "vla_debug_gelu_forms", "vla_action_denoise_ex", "vla_noise_fill",
+            "vla_expert_select_ffn")
 
 
 class VlaError(RuntimeError):
@@ -44,7 +45,8 @@ class VlaConfig(ctypes.Structure):
         "n_layers", "width", "mlp_width", "n_q_heads", "n_kv_heads", "head_dim", "vlm_hidden", "action_dim",
         "horizon", "time_dim", "max_batch", "max_prefix", "dtype")] + [("rms_eps", ctypes.c_float),
                                                                          ("flags", ctypes.c_uint),
-                                                                         ("schedule", ctypes.c_int)]
+                                                                         ("schedule", ctypes.c_int),
+                                                                         ("cross_every", ctypes.c_int)]
 
 
 DENSE_FIELDS = ("wk_pre", "wv_pre", "wq", "wk", "wv", "wo", "wup", "wdown", "wmod", "win", "wout", "wt1", "wt2",
@@ -103,6 +105,7 @@ def lib() -> ctypes.CDLL:
         "vla_debug_gelu_forms": [vp, ci, vp, vp, vp],
         "vla_action_denoise_ex": [vp, vp, vp, ci, ci, ctypes.POINTER(VlaRequest), vp, vp, vp],
         "vla_noise_fill": [ctypes.c_ulonglong, ctypes.c_size_t, vp, vp],
+        "vla_expert_select_ffn": [vp, vp, ci, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -169,7 +172,8 @@ class Expert:
                       head_dim=cfg.d_h, vlm_hidden=cfg.d_vlm, action_dim=cfg.d_a, horizon=cfg.H, time_dim=cfg.d_t,
                       max_batch=max_batch or cfg.B, max_prefix=max_prefix or cfg.P,
                       dtype=DTYPE_F32 if cfg.dtype == "f32" else DTYPE_BF16, rms_eps=cfg.eps, flags=flags,
-                      schedule=1 if getattr(cfg, "reverse", False) else 0)
+                      schedule=1 if getattr(cfg, "reverse", False) else 0,
+                      cross_every=int(getattr(cfg, "cross_every", 0)))
         self._c = c
         h = ctypes.c_void_p()
         if self.w2a8:
@@ -238,6 +242,15 @@ class Expert:
         _check(lib().vla_policy_step_host(self._h, _ptr(Z_host), B, P, _ptr(noise_host), _ptr(actions_host),
                                           _stream(stream)), "vla_policy_step_host")
         return actions_host
+
+    def select_ffn(self, idx=None, stream=None):
+        """Evaluate only the FFN neurons idx (int32 [L, F_sel] on the device);
+        None restores the full MLP."""
+        if idx is None:
+            _check(lib().vla_expert_select_ffn(self._h, None, 0, _stream(stream)), "vla_expert_select_ffn")
+        else:
+            _check(lib().vla_expert_select_ffn(self._h, _ptr(idx), idx.shape[1], _stream(stream)),
+                   "vla_expert_select_ffn")
 
     def launch_count(self, B: int, P: int) -> int:
         n = ctypes.c_int()

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(352, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, bg = blockIdx.y;
   const int b = bg / a.n_kv, gk = bg - b * a.n_kv;
-  const int n_pre = (a.P + KB - 1) / KB, n_suf = (a.H + KB - 1) / KB;
+  const int n_pre = (a.P + KB - 1) / KB, n_suf = a.no_suffix ? 0 : (a.H + KB - 1) / KB;  // cross layers: none
   const int nch = n_pre + n_suf;
   // TMEM: O (d_h columns), S (KB columns), Q (d_h / 2 columns of bf16 pairs).
   const uint32_t ncols = dh + KB + dh / 2 <= 256 ? 256u : 512u;

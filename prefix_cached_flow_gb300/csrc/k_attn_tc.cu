@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(128, 1)
   const int rank = blockIdx.x, qt = blockIdx.y, bg = blockIdx.z;
   const int b = bg / a.n_kv, gk = bg - b * a.n_kv;
   const int key0 = suffix ? 0 : rank * a.kc;
-  const int avail = (suffix ? a.H : a.P) - key0;
+  const int avail = (suffix ? (a.no_suffix ? 0 : a.H) : a.P) - key0;  // cross layers: no action keys
   const int nk = avail < 0 ? 0 : (avail < kc ? avail : kc);
   uint32_t ncols = 32;
   while (ncols < (uint32_t)dh || ncols < (uint32_t)kc) ncols <<= 1;

@@ -179,7 +179,7 @@ __global__ void k_attn_part(ExpertDims d, StepBufs b, const TC* Kc, const TC* Vc
   float* S = Vs + chunk * dh;         // [H][chunk]
   const int c = blockIdx.x, j = blockIdx.y, bb = blockIdx.z;
   const int g = j / (d.n_q / d.n_kv);
-  const int nkeys = d.P + H;
+  const int nkeys = d.P + (b.no_suffix ? 0 : H);  // cross-attention layers: the cached keys only
   const int k0 = c * chunk;
   const int nk = min(chunk, nkeys - k0);
   const float scale = rsqrtf((float)dh);
@@ -753,6 +753,34 @@ __global__ void k_expand_scales(float* dst, const float* src, int L, int N, int 
   if (n < N && l < L) dst[(size_t)l * stride + off + n] = src[(size_t)l * (N / G) + n / G];
 }
 
+// Selected FFN neurons (rMuscle's Action Cache): compact copies of the rows of
+// W_up and the columns of W_down that idx [L][Fs] names (checked first by
+// k_check_ffn_idx: every index in [0, F) and above its predecessor).
+__global__ void k_check_ffn_idx(const int32_t* idx, int L, int F, int Fs, int* bad) {
+  const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  if (i >= (size_t)L * Fs) return;
+  const int j = (int)(i % Fs);
+  const int n = idx[i];
+  if (n < 0 || n >= F || (j > 0 && n <= idx[i - 1])) atomicExch(bad, 1);
+}
+__global__ void k_gather_up(const bf16* w, bf16* dst, const int32_t* idx, int L, int F, int D, int Fs) {
+  const int j = blockIdx.x, l = blockIdx.y;
+  const int n = idx[(size_t)l * Fs + j];
+  if (n < 0 || n >= F) return;
+  const uint4* src = (const uint4*)(w + ((size_t)l * F + n) * D);
+  uint4* out = (uint4*)(dst + ((size_t)l * Fs + j) * D);
+  for (int i = threadIdx.x; i < D / 8; i += blockDim.x) out[i] = src[i];
+}
+__global__ void k_gather_down(const bf16* w, bf16* dst, const int32_t* idx, int L, int F, int D, int Fs) {
+  const int d = blockIdx.x, l = blockIdx.y;
+  const bf16* src = w + ((size_t)l * D + d) * F;
+  bf16* out = dst + ((size_t)l * D + d) * Fs;
+  for (int j = threadIdx.x; j < Fs; j += blockDim.x) {
+    const int n = idx[(size_t)l * Fs + j];
+    out[j] = (n >= 0 && n < F) ? src[n] : __float2bfloat16_rn(0.f);
+  }
+}
+
 // A bounded wait that cannot be satisfied: the mbarrier expects two arrivals
 // and gets one.  The wait runs out after the handle's limit, latches
 // VLA_DEV_TIMEOUT and the kernel returns (nothing is left in flight).
@@ -916,6 +944,21 @@ cudaError_t launch_quant_rows_bf16(int T, int K, const bf16* x, bf16* codes, flo
 cudaError_t launch_expand_scales(float* dst, const float* src, int L, int N, int G, int stride, int off,
                                  cudaStream_t st) {
   k_expand_scales<<<dim3((N + 255) / 256, L), 256, 0, st>>>(dst, src, L, N, G, stride, off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_check_ffn_idx(const int32_t* idx, int L, int F, int Fs, int* bad, cudaStream_t st) {
+  const size_t n = (size_t)L * Fs;
+  k_check_ffn_idx<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx, L, F, Fs, bad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_ffn(const bf16* wup, const bf16* wdown, bf16* up_sel, bf16* down_sel, const int32_t* idx,
+                              int L, int F, int D, int Fs, cudaStream_t st) {
+  k_gather_up<<<dim3(Fs, L), 128, 0, st>>>(wup, up_sel, idx, L, F, D, Fs);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_gather_down<<<dim3(D, L), 256, 0, st>>>(wdown, down_sel, idx, L, F, D, Fs);
   return cudaGetLastError();
 }
 

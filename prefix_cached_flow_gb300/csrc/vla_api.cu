@@ -113,6 +113,12 @@ struct vla_expert {
   cudaStream_t cap_stream = nullptr;
   std::vector<GraphEntry> graphs;
   uint64_t tick = 0;
+  // selected FFN neurons: effective MLP width and the compact weight copies
+  int F_eff = 0;
+  void* wup_full = nullptr;
+  void* wdown_full = nullptr;
+  void* wup_sel = nullptr;
+  void* wdown_sel = nullptr;
   // request options of the call being enqueued (prefix mask) and the buffer
   // for in-library noise
   const uint32_t* pmask = nullptr;
@@ -143,6 +149,13 @@ struct vla_expert {
 };
 
 namespace {
+
+// Layer l attends to the cached prefix keys only (a cross-attention layer of
+// the alternating joint / cross design) when cross_every > 0 and l mod
+// cross_every == cross_every - 1.
+bool is_cross(const vla_expert_config& c, int l) {
+  return c.cross_every > 0 && l % c.cross_every == c.cross_every - 1;
+}
 
 // tau_{k+1} - tau_k of the handle's schedule: 1/S, or -1/S for the reverse
 // (1 -> 0) convention, whose velocity sign change enters Eq. (1) here.
@@ -218,7 +231,7 @@ GemmPlan plan_gemm(const vla_expert* h, int N, int K, int T) {
 }
 
 void gemm_dims(const vla_expert* h, int which, int* N, int* K) {
-  const int D = h->cfg.width, F = h->cfg.mlp_width;
+  const int D = h->cfg.width, F = h->F_eff;
   switch (which) {
     case 0: *N = h->qkvdim; *K = D; break;
     case 1: *N = D; *K = h->qdim; break;
@@ -230,7 +243,7 @@ void gemm_dims(const vla_expert* h, int which, int* N, int* K) {
 ExpertDims make_dims(const vla_expert* h, int B, int P) {
   ExpertDims d;
   const vla_expert_config& c = h->cfg;
-  d.L = c.n_layers; d.D = c.width; d.F = c.mlp_width; d.n_q = c.n_q_heads; d.n_kv = c.n_kv_heads;
+  d.L = c.n_layers; d.D = c.width; d.F = h->F_eff; d.n_q = c.n_q_heads; d.n_kv = c.n_kv_heads;
   d.d_h = c.head_dim; d.d_a = c.action_dim; d.H = c.horizon; d.B = B; d.P = P; d.S = h->S; d.d_t = c.time_dim;
   d.eps = c.rms_eps; d.qdim = h->qdim; d.kvdim = h->kvdim; d.qkvdim = h->qkvdim;
   d.f32 = h->f32 ? 1 : 0;
@@ -288,7 +301,7 @@ vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B,
   }
   CUtensorMap tmX[3];  // activations [T][K] for K = D, qdim, F
   if (h->use_tc && !h->w2a8) {
-    const int ks[3] = {c.width, h->qdim, c.mlp_width};
+    const int ks[3] = {c.width, h->qdim, h->F_eff};
     for (int i = 0; i < 3; ++i)
       if (tc_encode_2d_bf16(&tmX[i], h->act, ks[i], T, 64, pl[0].BN) != 0) return VLA_ERR_CUDA;
   }
@@ -301,7 +314,9 @@ vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B,
     for (int l = 0; l < c.n_layers; ++l) {
       VLA_CK(run_linear(h, 0, l, T, pl[0], xmap[0], st));
       VLA_CK(launch_reduce_qkv(d, sb, l, pl[0].splits, st));
-      VLA_CK(launch_attention(d, sb, l, kc, vc, st));
+      StepBufs sbl = sb;
+      sbl.no_suffix = is_cross(c, l) ? 1 : 0;
+      VLA_CK(launch_attention(d, sbl, l, kc, vc, st));
       VLA_CK(run_linear(h, 1, l, T, pl[1], xmap[1], st));
       VLA_CK(launch_reduce_norm(d, sb, k, l, 3, l, 1, pl[1].splits, st));
       VLA_CK(run_linear(h, 2, l, T, pl[2], xmap[2], st));
@@ -507,9 +522,11 @@ vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, con
   return VLA_OK;
 }
 
-vla_status enqueue_attention(const AttnPlan& ap, int layer, unsigned long long* tl, cudaStream_t st) {
+vla_status enqueue_attention(const vla_expert* h, const AttnPlan& ap, int layer, unsigned long long* tl,
+                             cudaStream_t st) {
   AttnArgs aa = ap.aa;
   aa.layer = layer;
+  aa.no_suffix = is_cross(h->cfg, layer) ? 1 : 0;
   aa.tl = tl;
   if (ap.stream) {
     VLA_CK(launch_attn_stream(&ap.tmQ, &ap.tmK, &ap.tmVt, &ap.tmKs, &ap.tmVs, aa, st));
@@ -530,7 +547,7 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   const vla_expert_config& c = h->cfg;
   const ExpertDims d = make_dims(h, B, P);
   const StepBufs sb = make_bufs(h, P);
-  const int T = B * c.horizon, D = c.width, F = c.mlp_width, L = c.n_layers;
+  const int T = B * c.horizon, D = c.width, F = h->F_eff, L = c.n_layers;
   const LinPlan pq = plan_linear(h, h->qkvdim, D, T, true);
   const LinPlan po = plan_linear(h, D, h->qdim, T, false);
   const LinPlan pu = plan_linear(h, F, D, T, true);
@@ -572,7 +589,7 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       }
       VLA_CK(run_lin(&h->tm_wqkv, &tm_uq, &tmH, a, pq, st));
       // attention
-      VLA_ST(enqueue_attention(ap, l, tls(1), st));
+      VLA_ST(enqueue_attention(h, ap, l, tls(1), st));
       // O projection + residual
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
@@ -607,7 +624,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
   const vla_expert_config& c = h->cfg;
   const ExpertDims d = make_dims(h, B, P);
   const StepBufs sb = make_bufs(h, P);
-  const int T = B * c.horizon, D = c.width, F = c.mlp_width, L = c.n_layers, Q = h->qdim;
+  const int T = B * c.horizon, D = c.width, F = h->F_eff, L = c.n_layers, Q = h->qdim;
   const LinPlan pq = plan_linear(h, h->qkvdim, D, T, false);
   const LinPlan po = plan_linear(h, D, Q, T, false);
   const LinPlan pu = plan_linear(h, F, D, T, false);
@@ -653,7 +670,7 @@ vla_status enqueue_denoise_w2a8_fused(vla_expert* h, const void* kc, const void*
       VLA_CK(cp(l, 5, h->q));
       VLA_CK(cp(l, 6, h->ks));
       VLA_CK(cp(l, 7, h->vs));
-      VLA_ST(enqueue_attention(ap, l, tls(1), st));
+      VLA_ST(enqueue_attention(h, ap, l, tls(1), st));
       VLA_CK(cp(l, 8, h->f32buf));
       VLA_CK(launch_quant_rows(T, Q, h->f32buf, act, h->alpha, st));
       VLA_CK(cp(l, 9, act));
@@ -698,7 +715,7 @@ constexpr int kPersistMaxT = 64;
 bool persist_plan(const vla_expert* h, int B, int P, PersistArgs* pa) {
   const vla_expert_config& c = h->cfg;
   const int T = B * c.horizon, G = h->num_sms;
-  if (!h->persist_ok || T > h->persist_T) return false;
+  if (!h->persist_ok || T > h->persist_T || h->F_eff != c.mlp_width || c.cross_every) return false;
   PersistArgs a{};
   a.L = c.n_layers; a.D = c.width; a.F = c.mlp_width; a.S = h->S; a.T = T; a.BN = round_up(T, 16);
   a.B = B; a.H = c.horizon; a.Hp = h->Hp; a.P = P; a.d_a = c.action_dim; a.d_h = c.head_dim;
@@ -783,6 +800,7 @@ vla_status validate_config(const vla_expert_config* c, int n_steps, bool w2a8) {
     return VLA_ERR_INVALID_ARG;
   if (c->dtype != VLA_DTYPE_F32 && c->dtype != VLA_DTYPE_BF16) return VLA_ERR_INVALID_ARG;
   if (c->schedule != VLA_SCHEDULE_FORWARD && c->schedule != VLA_SCHEDULE_REVERSE) return VLA_ERR_INVALID_ARG;
+  if (c->cross_every < 0) return VLA_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0 || c->time_dim % 2 != 0) return VLA_ERR_SHAPE;
   if (w2a8 && c->dtype != VLA_DTYPE_BF16) return VLA_ERR_INVALID_ARG;
   const int qdim = c->n_q_heads * c->head_dim;
@@ -822,6 +840,7 @@ vla_status create_common(const vla_expert_config* cfg, int n_steps, bool w2a8, c
   VLA_CK(cudaMalloc((void**)&h->tl, (size_t)20 * 4096 * 16 * 8));
   VLA_CK(cudaMemset(h->tl, 0, (size_t)20 * 4096 * 16 * 8));
 #endif
+  h->F_eff = cfg->mlp_width;
   h->Kmax = cfg->width;
   if (cfg->mlp_width > h->Kmax) h->Kmax = cfg->mlp_width;
   if (h->qdim > h->Kmax) h->Kmax = h->qdim;
@@ -1041,12 +1060,16 @@ void vla_expert_destroy(vla_expert* h) {
   if (!h) return;
   cudaDeviceSynchronize();
   for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  if (h->wup_full) {  // a neuron selection is or was active: free the full weights
+    h->wup = h->wup_full;
+    h->wdown = h->wdown_full;
+  }
   void* ptrs[] = {h->wkv_pre, h->wqkv, h->wo,   h->wup,   h->wdown, h->beta,  h->win,     h->wout,
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
                   h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf,
                   h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar, h->noise_buf,
-                  h->beta_rows, h->beta_pre_rows, h->zcodes, h->zalpha};
+                  h->beta_rows, h->beta_pre_rows, h->zcodes, h->zalpha, h->wup_sel, h->wdown_sel};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -1345,6 +1368,57 @@ vla_status vla_action_denoise_w2a8(vla_expert* h, const void* Kc, const void* Vc
   return denoise_impl(h, true, Kc, Vc, B, P, noise, actions, tap, stream);
 }
 
+vla_status vla_expert_select_ffn(vla_expert* h, const int32_t* idx, int F_sel, void* stream) {
+  if (!h) return VLA_ERR_INVALID_ARG;
+  const vla_expert_config& c = h->cfg;
+  const int L = c.n_layers, D = c.width, F = c.mlp_width;
+  if (h->w2a8 || h->f32 || !h->fused) return VLA_ERR_UNSUPPORTED;
+  if (F_sel < 0 || F_sel > F || F_sel % 128 || (F_sel > 0 && (!idx || ((uintptr_t)idx & 3u)))) return VLA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!h->wup_full) {
+    h->wup_full = h->wup;
+    h->wdown_full = h->wdown;
+  }
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);  // graphs hold the old weight maps
+  h->graphs.clear();
+  if (F_sel == 0 || F_sel == F) {
+    if (F_sel == F) {
+      // every neuron: still validate and apply the order given
+    } else {
+      h->F_eff = F;
+      h->wup = h->wup_full;
+      h->wdown = h->wdown_full;
+      if (tc_encode_2d_bf16(&h->tm_wup, h->wup, D, (uint64_t)L * F, 64, 128) ||
+          tc_encode_2d_bf16(&h->tm_wdown, h->wdown, F, (uint64_t)L * D, 64, 128))
+        return VLA_ERR_CUDA;
+      return VLA_OK;
+    }
+  }
+  vla_status s;
+  if (!h->wup_sel && ((s = dalloc(&h->wup_sel, (size_t)L * F * D * 2)) != VLA_OK ||
+                      (s = dalloc(&h->wdown_sel, (size_t)L * D * F * 2)) != VLA_OK))
+    return s;
+  int* bad = nullptr;
+  VLA_CK(cudaMallocAsync((void**)&bad, sizeof(int), st));
+  cudaError_t e = cudaMemsetAsync(bad, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_check_ffn_idx(idx, L, F, F_sel, bad, st);
+  int hbad = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&hbad, bad, sizeof(int), cudaMemcpyDeviceToHost, st);
+  cudaFreeAsync(bad, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  VLA_CK(e);
+  if (hbad) return VLA_ERR_INVALID_ARG;  // nothing changed
+  VLA_CK(launch_gather_ffn((const bf16*)h->wup_full, (const bf16*)h->wdown_full, (bf16*)h->wup_sel,
+                           (bf16*)h->wdown_sel, idx, L, F, D, F_sel, st));
+  h->F_eff = F_sel;
+  h->wup = h->wup_sel;
+  h->wdown = h->wdown_sel;
+  if (tc_encode_2d_bf16(&h->tm_wup, h->wup, D, (uint64_t)L * F_sel, 64, 128) ||
+      tc_encode_2d_bf16(&h->tm_wdown, h->wdown, F_sel, (uint64_t)L * D, 64, 128))
+    return VLA_ERR_CUDA;
+  return VLA_OK;
+}
+
 vla_status vla_noise_fill(unsigned long long seed, size_t n, float* out, void* stream) {
   if (!out || n < 1) return VLA_ERR_INVALID_ARG;
   VLA_CK(launch_noise(seed, n, out, (cudaStream_t)stream));
@@ -1392,7 +1466,7 @@ vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kerne
   } else if (h->fused) {
     const int T = B * h->cfg.horizon;
     const int extra = (plan_linear(h, h->qkvdim, h->cfg.width, T, true).bmode == 0) +
-                      (plan_linear(h, h->cfg.mlp_width, h->cfg.width, T, true).bmode == 0);
+                      (plan_linear(h, h->F_eff, h->cfg.width, T, true).bmode == 0);
     // per step: embed, head; per layer: 4 GEMMs and the attention, plus the
     // standalone norms when the in-GEMM prologue does not fit
     *kernels = h->S * (2 + (5 + extra) * h->cfg.n_layers);

@@ -637,6 +637,7 @@ struct AttnArgs {
   bf16* o;           // [B*H][n_q*d_h] output
   const uint32_t* pmask;  // prefix visibility bits [B][pmw] (null: every prefix key visible)
   int pmw;                // mask words per observation, (P + 31) / 32
+  int no_suffix;          // a cross-attention layer: the cached keys only, no action keys
   bf16* xo;          // L2 exchange of scaled partial O: [tile][rank][d_h/8][128][8] bf16
   float* o32;        // when set, o is written in fp32 here instead of bf16 (W2A8 quantises it next)
   int* status;
@@ -747,6 +748,7 @@ struct StepBufs {
   int attn_chunk, n_chunks;
   const uint32_t* pmask;  // prefix visibility bits [B][pmw] (null: all visible)
   int pmw;
+  int no_suffix;          // attention of a cross-attention layer: cached keys only
 };
 
 // tau_k = k / S, or 1 - k / S when reverse.
@@ -790,6 +792,11 @@ cudaError_t launch_quant_rows_bf16(int T, int K, const bf16* x, bf16* codes, flo
 // dst[l * stride + off + n] = src[l * (N / G) + n / G] for n < N, l < L.
 cudaError_t launch_expand_scales(float* dst, const float* src, int L, int N, int G, int stride, int off,
                                  cudaStream_t st);
+// Sets *bad unless every row of idx [L][Fs] is strictly increasing in [0, F).
+cudaError_t launch_check_ffn_idx(const int32_t* idx, int L, int F, int Fs, int* bad, cudaStream_t st);
+// Compact W_up rows / W_down columns of the selected FFN neurons idx [L][Fs].
+cudaError_t launch_gather_ffn(const bf16* wup, const bf16* wdown, bf16* up_sel, bf16* down_sel, const int32_t* idx,
+                              int L, int F, int D, int Fs, cudaStream_t st);
 // One kernel whose bounded wait cannot be satisfied (exercises the timeout latch).
 cudaError_t launch_expire_wait(int* status, cudaStream_t st);
 cudaError_t launch_i8_to_bf16(const int8_t* a, bf16* out, size_t n, cudaStream_t st);

@@ -622,3 +622,62 @@ def test_w2a8_velocity_group_scales_vs_library_routines():
     v = O.velocity_w2a8(noise, 0.4, Kc, Vc, w, cfg)
     ref = _torch_velocity_w2a8(noise.astype(np.float64), 0.4, Kc, Vc, w, cfg)
     np.testing.assert_allclose(v, ref, rtol=0, atol=1e-9)
+
+
+
+# ---------------------------------------------------------- neuron-selected FFN (rMuscle Action Cache)
+
+def test_selecting_every_neuron_in_any_order_is_the_dense_expert():
+    """MLP hidden units are exchangeable: all F neurons, permuted, give the
+    dense velocity."""
+    w, Z, noise = _setup()
+    Kc, Vc = O.prefix_kv(Z, w, PIN)
+    perm = np.stack([np.random.default_rng(l).permutation(PIN.F) for l in range(PIN.L)])
+    v = O.velocity(noise, 0.3, Kc, Vc, O.select_ffn_neurons(w, perm), PIN)
+    np.testing.assert_allclose(v, O.velocity(noise, 0.3, Kc, Vc, w, PIN), rtol=0, atol=1e-12)
+
+
+def test_selected_neurons_equal_zeroing_the_others():
+    """Evaluating a subset of neurons equals the dense expert whose other
+    neurons' W_down columns are zero (their GeLU outputs then contribute 0)."""
+    w, Z, noise = _setup()
+    Kc, Vc = O.prefix_kv(Z, w, PIN)
+    rng = np.random.default_rng(5)
+    idx = np.stack([np.sort(rng.choice(PIN.F, PIN.F // 3, replace=False)) for _ in range(PIN.L)])
+    wz = dict(w)
+    wz["wdown"] = np.zeros_like(w["wdown"])
+    for l in range(PIN.L):
+        wz["wdown"][l][:, idx[l]] = w["wdown"][l][:, idx[l]]
+    v = O.velocity(noise, 0.6, Kc, Vc, O.select_ffn_neurons(w, idx), PIN)
+    np.testing.assert_allclose(v, O.velocity(noise, 0.6, Kc, Vc, wz, PIN), rtol=0, atol=1e-12)
+
+
+
+# ---------------------------------------------------------- alternating joint / cross attention layers (§III-B)
+
+def test_cross_attention_vs_library_sdpa():
+    """suffix=False: the queries attend to the cached prefix keys only,
+    torch's scaled_dot_product_attention over those keys (GQA)."""
+    rng = np.random.default_rng(31)
+    q, ks, vs, Kc, Vc = _rand_attn(rng)
+    o = O.joint_attention(q, ks, vs, Kc, Vc, suffix=False)
+    T = lambda a: torch.from_numpy(a)
+    ref = tF.scaled_dot_product_attention(T(q).transpose(1, 2), T(Kc), T(Vc), enable_gqa=True).transpose(1, 2)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_cross_layers_ignore_the_action_keys():
+    """In a cross-attention layer the action tokens' W_k, W_v do not enter:
+    zeroing them there leaves the velocity unchanged, while in joint layers
+    it changes it."""
+    cfg = PIN.replace(cross_every=2)
+    w, Z, noise = _setup(cfg)
+    Kc, Vc = O.prefix_kv(Z, w, cfg)
+    v = O.velocity(noise, 0.5, Kc, Vc, w, cfg)
+    w1 = dict(w)
+    w1["wk"] = w["wk"].copy(); w1["wv"] = w["wv"].copy()
+    w1["wk"][1] = 0.0; w1["wv"][1] = 0.0            # layer 1 is a cross layer
+    np.testing.assert_allclose(O.velocity(noise, 0.5, Kc, Vc, w1, cfg), v, rtol=0, atol=1e-14)
+    w0 = dict(w)
+    w0["wk"] = w["wk"].copy(); w0["wk"][0] = 0.0     # layer 0 is a joint layer
+    assert np.max(np.abs(O.velocity(noise, 0.5, Kc, Vc, w0, cfg) - v)) > 1e-6

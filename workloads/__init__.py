@@ -72,6 +72,7 @@ class ExpertConfig:
     reverse: bool = False  # integration direction of the schedule: 0 -> 1, or 1 -> 0
     beta_group: int = 0    # W2A8: output rows per weight-scale group (0: one scale per tensor)
     w2a8_prefix: bool = False  # W2A8: the prefix K/V maps are ternary too
+    cross_every: int = 0   # layers l with l % cross_every == cross_every - 1 attend to the prefix only
 
     def replace(self, **kw) -> "ExpertConfig":
         return dataclasses.replace(self, **kw)
