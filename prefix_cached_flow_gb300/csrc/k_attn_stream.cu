@@ -104,13 +104,19 @@ __device__ __forceinline__ void tma_load_3d_s(void* dst, const void* map, uint64
 
 // Row maximum of 32 S values; with MASK only keys (base + u) below nk count.
 // The unmasked form uses the three-input max (two new values per op).
+// Word j / 32 of a chunk's four visibility words, by selects (no local memory).
+__device__ __forceinline__ uint32_t mword(const uint32_t* mw, int j) {
+  const int q = j >> 5;
+  return q == 0 ? mw[0] : (q == 1 ? mw[1] : (q == 2 ? mw[2] : mw[3]));
+}
+
 template <bool MASK>
 __device__ __forceinline__ void max32(float (&mx)[4], const uint32_t* r, int base, int nk, const uint32_t* mw) {
   if (MASK) {
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int j = base + u;
-      const bool v = j < nk && ((mw[j >> 5] >> (j & 31)) & 1u);
+      const bool v = j < nk && ((mword(mw, j) >> (j & 31)) & 1u);
       mx[u & 3] = fmaxf(mx[u & 3], v ? __uint_as_float(r[u]) : -INFINITY);
     }
   } else {
@@ -141,8 +147,8 @@ __device__ __forceinline__ float probs64(const uint32_t* sr, uint32_t* pk, float
       float p0 = fast_exp2(fmaf(__uint_as_float(sr[u]), c, nm));
       float p1 = fast_exp2(fmaf(__uint_as_float(sr[u + 1]), c, nm));
       const int j0 = base + u, j1 = j0 + 1;
-      p0 = (j0 < nk && ((mw[j0 >> 5] >> (j0 & 31)) & 1u)) ? p0 : 0.f;
-      p1 = (j1 < nk && ((mw[j1 >> 5] >> (j1 & 31)) & 1u)) ? p1 : 0.f;
+      p0 = (j0 < nk && ((mword(mw, j0) >> (j0 & 31)) & 1u)) ? p0 : 0.f;
+      p1 = (j1 < nk && ((mword(mw, j1) >> (j1 & 31)) & 1u)) ? p1 : 0.f;
       lv[u & 3] += p0;
       lv[(u + 1) & 3] += p1;
       pk[u >> 1] = pack_bf16x2(p0, p1);
@@ -168,7 +174,7 @@ __device__ __forceinline__ float probs64(const uint32_t* sr, uint32_t* pk, float
   return a0 + a1;
 }
 
-template <bool O32>
+template <bool O32, bool MASKED>
 __global__ void __launch_bounds__(352, 1)
     k_attn_stream(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmKs,
@@ -385,11 +391,14 @@ __global__ void __launch_bounds__(352, 1)
       tmem_wait16(ot);
       tmem_wait16(ot + 16);
       // visibility of the chunk's 128 keys (prefix chunks under a mask)
-      uint32_t mw[4];
-      const uint32_t* mrow = (j < n_pre && a.pmask) ? a.pmask + (size_t)b * a.pmw : nullptr;
+      // (a separate instantiation: without a mask this costs nothing)
+      uint32_t mw[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+      if (MASKED && j < n_pre) {
+        const uint32_t* mrow = a.pmask + (size_t)b * a.pmw;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) mw[q] = prefix_mask_window(mrow, a.pmw, j * KB + q * 32);
-      const bool fullc = nk == KB && (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;  // the same for the whole CTA
+        for (int q = 0; q < 4; ++q) mw[q] = prefix_mask_window(mrow, a.pmw, j * KB + q * 32);
+      }
+      const bool fullc = nk == KB && (!MASKED || (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu);  // CTA-uniform
       float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (fullc) {
         max32<false>(mxv, sr, 0, 0, mw);
@@ -537,8 +546,10 @@ __global__ void __launch_bounds__(352, 1)
 size_t attn_stream_smem_bytes(int d_h) { return 1024 + stream_layout(d_h).total; }
 
 cudaError_t attn_stream_init() {
-  cudaError_t e = set_max_dyn_smem(k_attn_stream<false>);
-  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_stream<true>);
+  cudaError_t e = set_max_dyn_smem(k_attn_stream<false, false>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_stream<true, false>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_stream<false, true>);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_stream<true, true>);
   return e;
 }
 
@@ -560,6 +571,10 @@ cudaError_t launch_attn_stream(const CUtensorMap* tmQ, const CUtensorMap* tmK, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_stream<true>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
-  return cudaLaunchKernelEx(&cfg, k_attn_stream<false>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  if (a.pmask) {
+    if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_stream<true, true>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+    return cudaLaunchKernelEx(&cfg, k_attn_stream<false, true>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  }
+  if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_stream<true, false>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  return cudaLaunchKernelEx(&cfg, k_attn_stream<false, false>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
 }

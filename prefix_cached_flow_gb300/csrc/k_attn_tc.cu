@@ -54,7 +54,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
-template <bool O32, int CS>
+template <bool O32, int CS, bool MASKED>
 __global__ void __launch_bounds__(128, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ CUtensorMap tmKs,
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(128, 1)
   const int row = warp * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
   float m = -INFINITY, l = 0.f;
-  const uint32_t* mrow = (suffix || !a.pmask) ? nullptr : a.pmask + (size_t)b * a.pmw;
+  const uint32_t* mrow = (!MASKED || suffix) ? nullptr : a.pmask + (size_t)b * a.pmw;
   if (ok && nk > 0) {
     // Two passes over TMEM in 32-column pieces.  Every CTA runs this code
     // once, so it is kept compact (rolled loops whose bodies repeat, instead
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(128, 1)
       tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
       tmem_wait16(r);
       tmem_wait16(r + 16);
-      const uint32_t mb = prefix_mask_window(mrow, a.pmw, key0 + c0);
+      const uint32_t mb = MASKED ? prefix_mask_window(mrow, a.pmw, key0 + c0) : 0xFFFFFFFFu;
       if (c0 + 32 <= nk && mb == 0xFFFFFFFFu) {  // a full visible piece (uniform over the CTA): no masks
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(128, 1)
       tmem_ld16_nowait(taddr + (uint32_t)(c0 + 16), r + 16);
       tmem_wait16(r);
       tmem_wait16(r + 16);
-      const uint32_t mb = prefix_mask_window(mrow, a.pmw, key0 + c0);
+      const uint32_t mb = MASKED ? prefix_mask_window(mrow, a.pmw, key0 + c0) : 0xFFFFFFFFu;
       const bool masked = c0 + 32 > nk || mb != 0xFFFFFFFFu;  // the last, partial piece or hidden keys
 #pragma unroll
       for (int q = 0; q < 4; ++q) {  // 8-key chunks
@@ -314,7 +314,9 @@ __global__ void __launch_bounds__(128, 1)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < CS; ++c) {
-          const bool held = (c8 + h) < q8 && (c == CS - 1 || c * a.kc < a.P);
+          // ranks that held keys: the prefix ranks with keys, the action-key rank
+          // unless this is a cross-attention layer
+          const bool held = (c8 + h) < q8 && (c == CS - 1 ? a.no_suffix == 0 : c * a.kc < a.P);
           v[h][c] = held ? __ldcg((const uint4*)(a.xo + (cl * CS + c) * 128 * (size_t)dh) +
                                   (size_t)(rank * q8 + c8 + h) * 128 + row)
                          : make_uint4(0u, 0u, 0u, 0u);
@@ -364,8 +366,12 @@ size_t attn_tc_smem_bytes(int d_h, int kc) { return 1024 + attn_layout(d_h, kc).
 
 template <bool O32, int CS>
 cudaError_t attn_init_one() {
-  cudaError_t e = set_max_dyn_smem(k_attn_tc<O32, CS>);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_tc<O32, CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = set_max_dyn_smem(k_attn_tc<O32, CS, false>);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_attn_tc<O32, CS, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) e = set_max_dyn_smem(k_attn_tc<O32, CS, true>);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_attn_tc<O32, CS, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
@@ -399,10 +405,15 @@ cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+#define VLA_ATTN_GO(O, C, M) return cudaLaunchKernelEx(&cfg, k_attn_tc<O, C, M>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a)
+  const bool m = a.pmask != nullptr;  // the masked instantiations only when a mask is given
   if (a.cs == 8) {
-    if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_tc<true, 8>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
-    return cudaLaunchKernelEx(&cfg, k_attn_tc<false, 8>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+    if (a.o32) { if (m) VLA_ATTN_GO(true, 8, true); VLA_ATTN_GO(true, 8, false); }
+    if (m) VLA_ATTN_GO(false, 8, true);
+    VLA_ATTN_GO(false, 8, false);
   }
-  if (a.o32) return cudaLaunchKernelEx(&cfg, k_attn_tc<true, 16>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
-  return cudaLaunchKernelEx(&cfg, k_attn_tc<false, 16>, *tmQ, *tmK, *tmVt, *tmKs, *tmVs, a);
+  if (a.o32) { if (m) VLA_ATTN_GO(true, 16, true); VLA_ATTN_GO(true, 16, false); }
+  if (m) VLA_ATTN_GO(false, 16, true);
+  VLA_ATTN_GO(false, 16, false);
+#undef VLA_ATTN_GO
 }

@@ -170,19 +170,25 @@ __device__ __forceinline__ bool grid_sync(const PersistArgs& a, unsigned target,
     __threadfence();
     atomicAdd(a.bar, 1u);
     const uint64_t t0 = globaltimer_ns();
-    const uint64_t lim = wait_limit_ns(a.status);
-    while (true) {
+    uint64_t lim = 0;  // the handle's limit, read only once the wait has lasted 100 us
+    for (uint32_t it = 1;; ++it) {
       unsigned v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.bar) : "memory");
       if (v >= target) break;
-      if (globaltimer_ns() - t0 > lim) {
-        latch_error(a.status, VLA_DEV_TIMEOUT);
-        *fail = 1;
-        break;
-      }
-      if (*(volatile int*)a.status == VLA_DEV_TIMEOUT) {
-        *fail = 1;
-        break;
+      if ((it & 63u) == 0) {
+        const uint64_t el = globaltimer_ns() - t0;
+        if (el > 100000ull) {
+          if (!lim) lim = wait_limit_ns(a.status);
+          if (el > lim) {
+            latch_error(a.status, VLA_DEV_TIMEOUT);
+            *fail = 1;
+            break;
+          }
+          if (*(volatile int*)a.status == VLA_DEV_TIMEOUT) {
+            *fail = 1;
+            break;
+          }
+        }
       }
     }
     __threadfence();
@@ -315,12 +321,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_solver_persist(const __grid_con
               if (it >= R) {
                 const uint32_t par = (uint32_t)((it / R) - 1) & 1u;
                 const uint64_t t0 = globaltimer_ns();
-                const uint64_t lim = wait_limit_ns(a.status);
+                uint64_t lim = 0;  // read once the wait has lasted 100 us
                 while (!mbar_try_wait(&empty[s], par)) {
-                  if (*s_stop || globaltimer_ns() - t0 > lim) {
-                    if (!*s_stop) latch_error(a.status, VLA_DEV_TIMEOUT);
+                  if (*s_stop) {
                     ok = false;
                     break;
+                  }
+                  const uint64_t el = globaltimer_ns() - t0;
+                  if (el > 100000ull) {
+                    if (!lim) lim = wait_limit_ns(a.status);
+                    if (el > lim) {
+                      latch_error(a.status, VLA_DEV_TIMEOUT);
+                      ok = false;
+                      break;
+                    }
                   }
                 }
                 if (!ok) break;

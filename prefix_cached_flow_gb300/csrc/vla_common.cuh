@@ -208,7 +208,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // The status block a handle passes to its kernels: word 0 is the latched
-// error, words 2-3 the bounded-wait limit in ns (0: the default limit).
+// error, words 2-3 the bounded-wait limit in ns (0: the default limit; limits
+// below 100 us act as 100 us).
 __device__ __forceinline__ uint64_t wait_limit_ns(const int* status) {
   if (!status) return VLA_WAIT_LIMIT_NS;
   const uint64_t lim = *(const volatile unsigned long long*)(status + 2);
@@ -221,14 +222,18 @@ __device__ __forceinline__ uint64_t wait_limit_ns(const int* status) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  const uint64_t lim = wait_limit_ns(status);
+  uint64_t lim = 0;  // the handle's limit, read only once a wait has lasted 100 us
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > lim) {
-      latch_error(status, VLA_DEV_TIMEOUT);
-      return false;
+    const uint64_t el = globaltimer_ns() - t0;
+    if (el > 100000ull) {
+      if (!lim) lim = wait_limit_ns(status);
+      if (el > lim) {
+        latch_error(status, VLA_DEV_TIMEOUT);
+        return false;
+      }
     }
     if (status && *(volatile int*)status == VLA_DEV_TIMEOUT) return false;
   }
