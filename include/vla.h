@@ -11,12 +11,13 @@
  *     observation into per-layer keys/values K_C = Z W_K, V_C = Z W_V, reused
  *     by every solver step (cache lifecycle: refreshed per observation, reused
  *     within a request); the action tokens attend to [K_C ; own keys] with
- *     softmax(Q K^T / sqrt(d_k) + M) V (joint attention, M = 0 here).
- *   - §III-D, Eq. (4): ternary weights (four 2-bit codes per byte, one fp32
- *     scale per tensor) with per-row int8 activations, 32-bit integer
- *     accumulation and bf16 output.
- *   - §III-C: requests carry inputs and optional noise; responses carry the
- *     action chunk and its dimensions, or an error.
+ *     softmax(Q K^T / sqrt(d_k) + M) V (joint attention; M = 0 unless a
+ *     request hides prefix keys, see vla_request).
+ *   - §III-D, Eq. (4): ternary weights (four 2-bit codes per byte, fp32
+ *     scales beta_{g(n)} per tensor or per group of output rows) with per-row
+ *     int8 activations, 32-bit integer accumulation and bf16 output.
+ *   - §III-C: requests carry inputs and optional noise and masks; responses
+ *     carry the action chunk and its dimensions, or an error.
  *
  * Conventions for every call:
  *   - Pointers named *_dev are DEVICE pointers owned by the caller; the

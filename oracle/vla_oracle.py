@@ -28,24 +28,44 @@ projection) is not printed on the pages; the readings taken here are:
    no learned gain, no biases anywhere;
  - GeLU is the exact x Phi(x); the MLP is not gated;
  - no positions in prefix or suffix; GQA query head j reads K/V head
-   floor(j / (n_q / n_kv)); key order is prefix then suffix; M = 0;
- - schedule tau_k = k / S, integrated 0 -> 1;
+   floor(j / (n_q / n_kv)); key order is prefix then suffix;
+ - M of Eq. (2): 0 for every action key and for every visible prefix key,
+   -inf for a prefix key a request hides (per-observation visibility; a
+   prefix length P_b is the visibility of keys [0, P_b)); with no mask, M = 0;
+ - schedule tau_k = k / S integrated 0 -> 1, or tau_k = 1 - k / S integrated
+   1 -> 0 (the reverse convention of §III-A: the network sees the reversed
+   time and dt = tau_{k+1} - tau_k = -1/S carries the sign change);
+ - alternating joint / cross layers (§III-B): with cross_every = k > 0, the
+   layers l with l mod k = k - 1 attend to the cached prefix keys only;
  - W2A8: the six per-layer maps W_q, W_k, W_v, W_o, W_up, W_down are ternary
-   with one fp32 scale per tensor; one activation quantisation per GEMM input
-   (shared by Q, K and V); y = bf16_rne((fp32(acc) * alpha) * beta).
+   with fp32 scales beta_{g(n)} per tensor or per group of output rows;
+   optionally the prefix maps W_K, W_V too (each prefix row of Z quantised by
+   Eq. (4) first); one activation quantisation per GEMM input (shared by Q, K
+   and V); y = bf16_rne((fp32(acc) * alpha) * beta_{g(n)});
+ - selected FFN neurons (the rMuscle Action Cache): the MLP restricted to the
+   chosen rows of W_up and columns of W_down;
+ - noise drawn in the library: Philox4x64-10 (Salmon et al., SC 2011) words
+   turned into normals by the Box-Muller transform in fp64.
 
 Precision: fp64 everywhere except Eq. (4), which is pinned to IEEE fp32 so
 that integer codes are reproducible bit for bit.
 
 Pins (tests/test_oracle_pins.py): brute-force softmax; a library attention
-routine; single-visible-key and zero-query closed forms; prefix permutation
-invariance; cache reuse == recompute (bitwise); zero velocity head returns
-the noise (bitwise); constant velocity field closed-form endpoint; one-step
-solve; suffix permutation equivariance; batch independence; GQA == replicated
-MHA; the whole velocity network against library routines (torch fp64);
-quantiser worked ties and error bound; ternary GEMM against int64 brute
-force; bf16 rounding against a library conversion; Eq. (5) special cases.
-No function here is left without a pin.
+routine with GQA and a mask; single-visible-key and zero-query closed forms;
+hidden prefix keys equal deleted keys; prefix permutation invariance; cache
+reuse == recompute (bitwise); zero velocity head returns the noise (bitwise);
+constant velocity field closed-form endpoint, forward and reverse; one-step
+solve; the reverse schedule evaluates the reversed time; suffix permutation
+equivariance; batch independence; GQA == replicated MHA; the whole velocity
+network against library routines (torch fp64), dense and W2A8 (every map's
+scale distinct, per tensor and per group, a swapped pair detected); cross
+layers against a library attention and blind to the action keys; selected
+neurons against zeroed neurons and the dense expert; quantiser worked ties and
+error bound; ternary GEMM against int64 brute force and group scales against
+blockwise tensor scales; the ternary prefix build against library routines;
+bf16 rounding against a library conversion; Philox against numpy's Philox and
+the normals inverted back to the generator words; mask bits against numpy
+packbits; Eq. (5) special cases.  No function here is left without a pin.
 """
 
 from __future__ import annotations
