@@ -380,7 +380,10 @@ __global__ void k_head(ExpertDims d, StepBufs b, int step, int splits, float dt,
 // The D features of a token are split over gridDim.y CTAs (kEmbedSplit at few
 // tokens, for parallelism); CTA y writes its partial sum of squares to slot
 // y of ss_out [slots][T], which the next norm sums in fixed order.
-__global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl) {
+// xt (nullable): also bf16((1 + xgam) h), the first layer's operand of the
+// factored modulated norm (many-token linears).
+__global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl, bf16* xt,
+                           const float* xgam) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
@@ -398,6 +401,7 @@ __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* s
     float acc = 0.f;
     for (int j = 0; j < d.d_a; ++j) acc += xs[j] * w[j];
     b.h[(size_t)t * d.D + i] = acc;
+    if (xt) xt[(size_t)t * d.D + i] = __float2bfloat16_rn((1.f + xgam[i]) * acc);
     ss += acc * acc;
   }
   ss = block_sum(ss, red);
@@ -408,7 +412,8 @@ __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* s
 // W_in row is read once per kMT tokens (the per-token form reads all of W_in
 // for every token).  Same arithmetic per element.
 constexpr int kMT = 16;
-__global__ void k_embed_ss_multi(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl) {
+__global__ void k_embed_ss_multi(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl, bf16* xt,
+                                 const float* xgam) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
@@ -434,10 +439,12 @@ __global__ void k_embed_ss_multi(ExpertDims d, StepBufs b, const float* x_in, fl
 #pragma unroll
       for (int t = 0; t < kMT; ++t) acc[t] += xs[t * d.d_a + j] * wv;
     }
+    const float xg = xt ? 1.f + xgam[i] : 0.f;
 #pragma unroll
     for (int t = 0; t < kMT; ++t)
       if (t < nt) {
         b.h[(size_t)(t0 + t) * d.D + i] = acc[t];
+        if (xt) xt[(size_t)(t0 + t) * d.D + i] = __float2bfloat16_rn(xg * acc[t]);
         ss[t] += acc[t] * acc[t];
       }
   }
@@ -879,10 +886,10 @@ static cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
 int embed_ss_slots(const ExpertDims& d) { return d.B * d.H >= kMultiTokens && d.d_a <= 256 ? 1 : embed_split(d); }
 
 cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float* x_in, float* ss_out, DevCtl ctl,
-                            cudaStream_t st) {
+                            cudaStream_t st, bf16* xt, const float* xgam) {
   ExpertDims dd = d;
   StepBufs bb = b;
-  void* args[] = {&dd, &bb, (void*)&x_in, &ss_out, &ctl};
+  void* args[] = {&dd, &bb, (void*)&x_in, &ss_out, &ctl, &xt, (void*)&xgam};
   const int T = d.B * d.H;
   if (T >= kMultiTokens && d.d_a <= 256)
     return launch_pdl((const void*)k_embed_ss_multi, dim3((T + kMT - 1) / kMT), dim3(kThreads),

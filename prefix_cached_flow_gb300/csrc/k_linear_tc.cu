@@ -317,6 +317,25 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
 
+  // W2A8 scales, fetched while the MMAs run: the thread's weight-scale quad
+  // (the same rows in every epilogue iteration of the split path, since its
+  // quads per column divide 128) and the token scales of its first two
+  // iterations.
+  float4 be_pre = make_float4(0.f, 0.f, 0.f, 0.f);
+  float al_pre[2] = {0.f, 0.f};
+  if (AMODE == 1 && SPLIT) {
+    const int quad = threadIdx.x % qpc;
+    const int n = m0 + rank * RPR + quad * 4;
+    if (n < g.N)
+      be_pre = g.wbeta ? *(const float4*)(g.wbeta + (size_t)g.layer * g.beta_stride + g.beta_off + n)
+                       : make_float4(g.beta_val, g.beta_val, g.beta_val, g.beta_val);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int t = t0 + (threadIdx.x + it * 128) / qpc;
+      if (it < iters && t < g.T) al_pre[it] = g.alpha[t];
+    }
+  }
+
   if (!mbar_wait(done, 0, g.status)) s_fail = 1;
   tc_fence_after();
   __syncthreads();
@@ -438,16 +457,15 @@ __global__ void __launch_bounds__(128, 1)
     col = live ? f / qpc : 0;
     quad = live ? f - col * qpc : 0;
   };
-  auto epilogue = [&](float4 acc, bool live, int col, int quad, float4 hprev, bool have_prev) {
+  auto epilogue = [&](float4 acc, bool live, int col, int quad, float4 hprev, bool have_prev, int it) {
     const int rloc = rank * RPR + quad * 4;
     const int n = m0 + rloc, t = t0 + col;
     const bool valid = live && t < g.T && n < g.N;
     const float4 raw = acc;
     if (AMODE == 1 && valid) {
       // Eq. (4): exact integer accumulators scaled to bf16
-      const float al = g.alpha[t];
-      const float4 be = g.wbeta ? *(const float4*)(g.wbeta + (size_t)g.layer * g.beta_stride + g.beta_off + n)
-                                : make_float4(g.beta_val, g.beta_val, g.beta_val, g.beta_val);
+      const float al = it < 2 ? al_pre[it] : g.alpha[t];
+      const float4 be = be_pre;
       acc.x = w2a8_scale(acc.x, al, be.x);
       acc.y = w2a8_scale(acc.y, al, be.y);
       acc.z = w2a8_scale(acc.z, al, be.z);
@@ -535,8 +553,8 @@ __global__ void __launch_bounds__(128, 1)
       a0.x += v0[c].x; a0.y += v0[c].y; a0.z += v0[c].z; a0.w += v0[c].w;
       a1.x += v1[c].x; a1.y += v1[c].y; a1.z += v1[c].z; a1.w += v1[c].w;
     }
-    if (iters >= 1) epilogue(a0, lv0, cl0, qd0, hpre[0], EPI == EPI_RESID);
-    if (iters >= 2) epilogue(a1, lv1, cl1, qd1, hpre[1], EPI == EPI_RESID);
+    if (iters >= 1) epilogue(a0, lv0, cl0, qd0, hpre[0], EPI == EPI_RESID, 0);
+    if (iters >= 2) epilogue(a1, lv1, cl1, qd1, hpre[1], EPI == EPI_RESID, 1);
   }
   for (int it = 2; it < iters; ++it) {
     bool live;
@@ -553,7 +571,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int c = 0; c < C; ++c) {
       acc.x += v[c].x; acc.y += v[c].y; acc.z += v[c].z; acc.w += v[c].w;
     }
-    epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false);
+    epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false, it);
   }
   VLA_TL(g.tl, 0, 11);
   if (EPI == EPI_RESID && g.ss_out) {

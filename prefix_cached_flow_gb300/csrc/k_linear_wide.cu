@@ -35,6 +35,7 @@ struct WideSmem {
   uint32_t a, b, wss, stg, bars, slot, total;
 };
 constexpr int kStg = 32 * 34;  // bf16 staging elements per epilogue warp (32 x 32 chunk, rows padded to 34)
+constexpr int kMaxSlots = 16;  // per-block sums of squares of a token (D <= 2048)
 
 __host__ __device__ inline WideSmem wide_layout(int BN) {
   WideSmem s;
@@ -257,6 +258,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int hbn = BN / 2;
     int slot = 0;  // q, k or v (EPI_QKV), from the tile's rows
     int lt = 0;
+    // Factored norm (EPI_QKV / EPI_GELU with fn_c): epilogue thread fe owns
+    // token fe of each tile's r table; the per-block sums of squares of the
+    // next tile's token are loaded while the current tile is processed.
+    const int fe = threadIdx.x - 64;
+    float ssn[kMaxSlots];
+    auto fetch_ss = [&](int tl) {
+      const int tt = (tl / tiles_n) * BN + fe;
+      const bool live = g.fn_c && tl < tiles && fe < BN && tt < g.T;
+#pragma unroll
+      for (int sl = 0; sl < kMaxSlots; ++sl)
+        ssn[sl] = (live && sl < g.fn_nss) ? __ldcg(g.fn_ss + (size_t)sl * g.T + tt) : 0.f;
+    };
+    if (EPI == EPI_QKV || EPI == EPI_GELU) fetch_ss(blockIdx.x);
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
       const int buf = lt & 1;
       const int m0 = (tile % tiles_n) * 128, t0 = (tile / tiles_n) * BN;
@@ -272,6 +286,23 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) hb[j] = j < nvv ? hq[(size_t)j * g.D] : 0.f;
       };
+      // Factored norm: the next map's operand scale (EPI_RESID), or this
+      // map's row scales r_t and W beta (EPI_QKV / EPI_GELU), fetched while
+      // the MMAs run.
+      float xg = 0.f, fc = 0.f;
+      if (EPI == EPI_RESID && g.xt_out) xg = 1.f + g.xt_gamma[n];
+      if ((EPI == EPI_QKV || EPI == EPI_GELU) && g.fn_c) {
+        fc = g.fn_c[n];
+        named_bar_sync(3, 32 * kEpiWarps);  // the previous tile's readers of the r table are done
+        if (fe < BN) {  // token fe of this tile: its sums of squares were fetched one tile ahead
+          float ssum = 0.f;
+#pragma unroll
+          for (int sl = 0; sl < kMaxSlots; ++sl) ssum += ssn[sl];
+          wss[fe] = rsqrtf(ssum / (float)g.D + g.eps);
+        }
+        fetch_ss(tile + gridDim.x);
+        named_bar_sync(3, 32 * kEpiWarps);
+      }
       if (EPI == EPI_RESID) {
         // The whole tile's residual rows go to L2 while the MMAs run; the
         // first chunk is loaded into registers.
@@ -306,7 +337,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       // index into (observation, position) without a division per store.
       const int tdiv = EPI == EPI_KV ? g.kv_P : g.H;
       float* wq = wss + ((size_t)(buf * 2 + half) * 4 + quarter) * hbn;  // this warp's column sums
-      for (int c0 = half * hbn; c0 < (half + 1) * hbn; c0 += 32) {
+      const int hend = (half + 1) * hbn;  // BN is a multiple of 16: the last chunk of a half may be partial
+      for (int c0 = half * hbn; c0 < hend; c0 += 32) {
         uint32_t r[32];
         if (okw) {
           tmem_ld16_nowait(tq + (uint32_t)(buf * 256 + c0), r);
@@ -317,21 +349,28 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-        const int nv = okw ? (tcols - c0 < 32 ? tcols - c0 : 32) : 0;  // valid columns in this chunk
+        // valid columns in this chunk (the 32 TMEM columns read stay inside the
+        // tile's 256-column buffer: c0 + 32 <= hbn + 32 * ceil(hbn / 32) <= 256)
+        const int lim = (tcols < hend ? tcols : hend) - c0;
+        const int nv = okw ? (lim < 32 ? lim : 32) : 0;
         if (EPI == EPI_RESID) {
-          const bool more = c0 + 32 < (half + 1) * hbn;
+          const bool more = c0 + 32 < hend;
           float hnxt[32];
           if (more) load_h(c0 + 32, hnxt);
           float hv[32];
           float* hp = g.h + (size_t)(t0 + c0) * g.D + n;
+          bf16* xp = g.xt_out + (size_t)(t0 + c0) * g.D + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             hv[j] = hcur[j] + __uint_as_float(r[j]);
-            if (j < nv) hp[(size_t)j * g.D] = hv[j];
+            if (j < nv) {
+              hp[(size_t)j * g.D] = hv[j];
+              if (g.xt_out) xp[(size_t)j * g.D] = __float2bfloat16_rn(xg * hv[j]);
+            }
             hv[j] = j < nv ? hv[j] * hv[j] : 0.f;
           }
           const float cs = warp_transpose_sum32(hv, lane);
-          wq[c0 - half * hbn + lane] = cs;
+          if (c0 + lane < hend) wq[c0 - half * hbn + lane] = cs;
           if (more) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) hcur[j] = hnxt[j];
@@ -342,12 +381,26 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           // consecutive features inside one head of one of q, k, v.
           bf16* stg = stg_all + (size_t)(warp - 2) * kStg;
           const bool vt = (EPI == EPI_QKV && slot == 2) || (EPI == EPI_KV && kwhich == 1);
+          // the chunk's row scales r_t (factored norm) into registers before
+          // any staging store (c0 is a multiple of 8: 16-byte aligned)
+          float rc[32];
+          if ((EPI == EPI_QKV || EPI == EPI_GELU) && g.fn_c) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 v4 = *(const float4*)(wss + c0 + 4 * q4);
+              rc[4 * q4] = v4.x; rc[4 * q4 + 1] = v4.y; rc[4 * q4 + 2] = v4.z; rc[4 * q4 + 3] = v4.w;
+            }
+          }
           __syncwarp();
           if (!vt) {
             // token-major outputs (g, q, k): [col][row] so a token's 32 features are 64 contiguous bytes
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
               float y0 = __uint_as_float(r[j]), y1 = __uint_as_float(r[j + 1]);
+              if ((EPI == EPI_QKV || EPI == EPI_GELU) && g.fn_c) {
+                y0 = fmaf(rc[j], y0, fc);
+                y1 = fmaf(rc[j + 1], y1, fc);
+              }
               if (EPI == EPI_GELU) gelu_as7126_x2(y0, y1, y0, y1);
               stg[j * 32 + lane] = __float2bfloat16_rn(y0);
               stg[(j + 1) * 32 + lane] = __float2bfloat16_rn(y1);
@@ -389,7 +442,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             // [row][col] (rows padded to 34 elements: conflict-free writes),
             // then one feature row of 32 tokens per warp store.
 #pragma unroll
-            for (int j = 0; j < 32; ++j) stg[lane * 34 + j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+            for (int j = 0; j < 32; ++j) {
+              float y = __uint_as_float(r[j]);
+              if (EPI == EPI_QKV && g.fn_c) y = fmaf(rc[j], y, fc);
+              stg[lane * 34 + j] = __float2bfloat16_rn(y);
+            }
             __syncwarp();
             const int t = t0 + c0 + lane;
             bf16* col;
@@ -452,8 +509,9 @@ cudaError_t linear_wide_init() {
 
 cudaError_t launch_linear_wide(const CUtensorMap* tmA, const CUtensorMap* tmB, const LinArgs& g, int grid,
                                cudaStream_t st) {
-  if (g.BN < 64 || g.BN > 256 || g.BN % 64 || g.KS % 64 || g.KS < 64 || g.N % 128 || g.T < 1 || grid < 1 ||
-      g.amode != 0 || g.w2a8 != 0 ||
+  if (g.BN < 64 || g.BN > 256 || g.BN % 16 || g.KS % 64 || g.KS < 64 || g.N % 128 || g.T < 1 || grid < 1 ||
+      g.amode != 0 || g.w2a8 != 0 || (g.fn_c && (g.fn_nss < 1 || g.fn_nss > kMaxSlots || !g.fn_ss)) ||
+      (g.xt_out && !g.xt_gamma) ||
       (g.epi != EPI_QKV && g.epi != EPI_RESID && g.epi != EPI_GELU && g.epi != EPI_KV))
     return cudaErrorInvalidValue;
   const size_t smem = linear_wide_smem_bytes(g.BN);

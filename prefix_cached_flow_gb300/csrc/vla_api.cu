@@ -129,6 +129,8 @@ struct vla_expert {
   int persist_T = 0;         // tokens its buffers hold
   float* cqkv = nullptr;     // [S][L][qkvdim]  W_qkv beta_a per (step, layer)
   float* cup = nullptr;      // [S][L][F]       W_up beta_m
+  // factored modulated norm of the many-token linears: (1 + gamma) h in bf16
+  bf16* xt = nullptr;        // [max T][D]
   float* p_accq = nullptr;
   float* p_accu = nullptr;
   float* p_rms = nullptr;
@@ -337,17 +339,19 @@ struct LinPlan {
   int grid = 0;       // its CTA count
 };
 
-// Many-token plan: the persistent kernel with 128 x BN tiles, BN in
-// {64, 128, 192, 256} chosen to minimise waves x (BN + 32) (the tile's token
-// columns plus a fixed per-tile cost).  Used when even 128-token tiles give a
+// Many-token plan: the persistent kernel with 128 x BN tiles, BN a multiple
+// of 16 in [64, 256] chosen to minimise waves x (BN + 64) (the tile's token
+// columns plus a fixed per-tile cost of about 64 columns, measured: four
+// waves of 176 took longer than three of 256 for 512 prefix tokens); e.g.
+// 3200 action tokens take QKV tiles of 224 (two waves) instead of 256.  Used when even 128-token tiles give a
 // wave of work for every SM (or always, with VLA_FLAG_LINEAR_WIDE); never for
 // packed ternary weights.
 LinPlan plan_wide(int num_sms, int N, int K, int T) {
   LinPlan p;
   const int tn = N / 128;
   long best = -1;
-  for (int bn = 256; bn >= 64; bn -= 64) {
-    const long cost = (long)cdiv(tn * cdiv(T, bn), num_sms) * (bn + 32);
+  for (int bn = 256; bn >= 64; bn -= 16) {
+    const long cost = (long)cdiv(tn * cdiv(T, bn), num_sms) * (bn + 64);
     if (best < 0 || cost < best) {
       best = cost;
       p.BN = bn;
@@ -402,6 +406,13 @@ LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool p
 LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
   if (!h->w2a8 && wide_applies(h->cfg.flags, h->num_sms, N, K, T)) return plan_wide(h->num_sms, N, K, T);
   return plan_linear_sms(h->num_sms, N, K, T, want_norm && !h->w2a8, h->w2a8);
+}
+
+// The many-token solver folds its modulated norms into the linears when all
+// four maps of a layer run on the many-token kernel (see
+// enqueue_denoise_fused).
+bool factored_norm(const vla_expert* h, const LinPlan& pq, const LinPlan& po, const LinPlan& pu, const LinPlan& pd) {
+  return h->xt && pq.wide && po.wide && pu.wide && pd.wide && h->F_eff == h->cfg.mlp_width;
 }
 
 // One linear layer on the kernel its plan names.
@@ -561,12 +572,20 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   VLA_ST(plan_attention(h, B, P, kc, vc, act, nullptr, &ap));
   CUtensorMap tmH;
   if (tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN)) return VLA_ERR_CUDA;
+  // Many tokens: the modulated norms are factored into the linears
+  // (W u = r W((1 + gamma) h) + W beta): each residual epilogue writes
+  // (1 + gamma) h for the next normed map, whose epilogue applies r and adds
+  // W beta, so no separate norm pass re-reads h.
+  const bool fn = factored_norm(h, pq, po, pu, pd);
+  CUtensorMap tm_xq, tm_xu;
+  if (fn && (tc_encode_2d_bf16(&tm_xq, h->xt, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_xu, h->xt, D, T, 64, pu.BN)))
+    return VLA_ERR_CUDA;
   const DevCtl ctl{h->d_status, h->d_abort};
   const float* modt = h->modtab;
   for (int k = 0; k < h->S; ++k) {
     const float* x_in = k == 0 ? noise : actions;
     const float dt = step_dt(h, k);
-    VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st));
+    VLA_CK(launch_embed_ss(d, sb, x_in, h->ss2, ctl, st, fn ? h->xt : nullptr, modt + (size_t)k * L * 4 * D));
     int n_ss = embed_ss_slots(d);  // slots of ss2 currently valid
     for (int l = 0; l < L; ++l) {
       const float* mod = modt + ((size_t)k * L + l) * 4 * D;  // gamma_a, beta_a, gamma_m, beta_m
@@ -582,30 +601,36 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       LinArgs a = lin_args(h, pq, h->qkvdim, T, l);
       a.tl = tls(0);
       a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
-      if (pq.bmode == 1) {
+      if (fn) {
+        a.fn_c = h->cqkv + ((size_t)k * L + l) * h->qkvdim; a.fn_ss = h->ss2; a.fn_nss = n_ss;
+      } else if (pq.bmode == 1) {
         a.h_in = h->h; a.ss_in = h->ss2; a.n_ss_in = n_ss; a.gamma = mod; a.beta = mod + D;
       } else {
         VLA_CK(launch_modnorm(d, h->h, h->ss2, n_ss, mod, mod + D, act, st));
       }
-      VLA_CK(run_lin(&h->tm_wqkv, &tm_uq, &tmH, a, pq, st));
+      VLA_CK(run_lin(&h->tm_wqkv, fn ? &tm_xq : &tm_uq, &tmH, a, pq, st));
       // attention
       VLA_ST(enqueue_attention(h, ap, l, tls(1), st));
       // O projection + residual
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
+      if (fn) { a.xt_out = h->xt; a.xt_gamma = mod + 2 * D; }
       VLA_CK(run_lin(&h->tm_wo, &tm_o, &tmH, a, po, st));
       // MLP up + GeLU
       a = lin_args(h, pu, F, T, l);
       a.epi = EPI_GELU; a.g = (bf16*)h->gbuf; a.ldg = F; a.tl = tls(3);
-      if (pu.bmode == 1) {
+      if (fn) {
+        a.fn_c = h->cup + ((size_t)k * L + l) * F; a.fn_ss = h->ss1; a.fn_nss = po.tiles_n;
+      } else if (pu.bmode == 1) {
         a.h_in = h->h; a.ss_in = h->ss1; a.n_ss_in = po.tiles_n; a.gamma = mod + 2 * D; a.beta = mod + 3 * D;
       } else {
         VLA_CK(launch_modnorm(d, h->h, h->ss1, po.tiles_n, mod + 2 * D, mod + 3 * D, act, st));
       }
-      VLA_CK(run_lin(&h->tm_wup, &tm_uu, &tmH, a, pu, st));
+      VLA_CK(run_lin(&h->tm_wup, fn ? &tm_xu : &tm_uu, &tmH, a, pu, st));
       // MLP down + residual
       a = lin_args(h, pd, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.tl = tls(4);
+      if (fn && l + 1 < L) { a.xt_out = h->xt; a.xt_gamma = mod + 4 * D; }  // the next layer's gamma_a
       VLA_CK(run_lin(&h->tm_wdown, &tm_g, &tmH, a, pd, st));
       n_ss = pd.tiles_n;
     }
@@ -974,7 +999,32 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
       if (tc_encode_2d_bf16(&h->tm_wdown, h->wdown, c.mlp_width, (uint64_t)L * D, 64, 128)) return VLA_ERR_CUDA;
     }
   }
-  // persistent few-token solver: W beta vectors, accumulators, attention partials
+  // W beta for every (step, layer): the beta half of the factored modulated
+  // norm, used by the many-token linears and by the persistent solver
+  auto wbeta_tables = [&]() -> vla_status {
+    if (h->cqkv) return VLA_OK;
+    const int F = c.mlp_width;
+    vla_status s2;
+    if ((s2 = dalloc(&h->cqkv, (size_t)S * L * h->qkvdim * 4)) != VLA_OK) return s2;
+    if ((s2 = dalloc(&h->cup, (size_t)S * L * F * 4)) != VLA_OK) return s2;
+    cudaError_t e2 = cudaSuccess;
+    for (int l = 0; l < L && e2 == cudaSuccess; ++l) {
+      e2 = launch_gemm_simt(0, h->modtab + ((size_t)l * 4 + 1) * D, L * 4 * D, 1,
+                            (const char*)h->wqkv + (size_t)l * h->qkvdim * D * 2, D, S, h->qkvdim, D, 1,
+                            h->cqkv + (size_t)l * h->qkvdim, 0, L * h->qkvdim, nullptr, st);
+      if (e2 == cudaSuccess)
+        e2 = launch_gemm_simt(0, h->modtab + ((size_t)l * 4 + 3) * D, L * 4 * D, 1,
+                              (const char*)h->wup + (size_t)l * F * D * 2, D, S, F, D, 1, h->cup + (size_t)l * F, 0,
+                              L * F, nullptr, st);
+    }
+    VLA_CK(e2);
+    return VLA_OK;
+  };
+  if (h->fused && !h->w2a8 && !h->f32 && wide_applies(c.flags, h->num_sms, D, h->qdim, Tm)) {
+    if ((s = wbeta_tables()) != VLA_OK) return s;
+    if ((s = dalloc(&h->xt, (size_t)Tm * D * 2)) != VLA_OK) return s;
+  }
+  // persistent few-token solver: accumulators, attention partials
   const int dh = c.head_dim;
   if (h->fused && !h->w2a8 && !h->f32 && (c.flags & VLA_FLAG_PERSIST) && (dh == 64 || dh == 128 || dh == 256) &&
       D % 128 == 0 && c.mlp_width % 128 == 0 && h->qkvdim % 128 == 0 && h->qdim % 64 == 0 && c.action_dim <= 64 &&
@@ -990,8 +1040,7 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
       const int group = c.n_q_heads / c.n_kv_heads;
       h->p_units = (size_t)Bmax * c.n_kv_heads * cdiv(group * c.horizon, 128) *
                    (cdiv(c.max_prefix, 128) + cdiv(c.horizon, 128));
-      if ((s = dalloc(&h->cqkv, (size_t)S * L * h->qkvdim * 4)) != VLA_OK) return s;
-      if ((s = dalloc(&h->cup, (size_t)S * L * F * 4)) != VLA_OK) return s;
+      if ((s = wbeta_tables()) != VLA_OK) return s;
       if ((s = dalloc(&h->p_accq, (size_t)Tp * h->qkvdim * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_accu, (size_t)Tp * F * 4)) != VLA_OK) return s;
       if ((s = dalloc(&h->p_rms, (size_t)2 * Tp * 4)) != VLA_OK) return s;
@@ -1000,17 +1049,6 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
       if ((s = dalloc(&h->p_oml, h->p_units * 128 * sizeof(float2))) != VLA_OK) return s;
       if ((s = dalloc(&h->p_bar, 64)) != VLA_OK) return s;
       VLA_CK(cudaMemset(h->p_bar, 0, 64));
-      // W beta for every (step, layer): the beta half of the factored modulated norm
-      for (int l = 0; l < L && err == cudaSuccess; ++l) {
-        err = launch_gemm_simt(0, h->modtab + ((size_t)l * 4 + 1) * D, L * 4 * D, 1,
-                               (const char*)h->wqkv + (size_t)l * h->qkvdim * D * 2, D, S, h->qkvdim, D, 1,
-                               h->cqkv + (size_t)l * h->qkvdim, 0, L * h->qkvdim, nullptr, st);
-        if (err == cudaSuccess)
-          err = launch_gemm_simt(0, h->modtab + ((size_t)l * 4 + 3) * D, L * 4 * D, 1,
-                                 (const char*)h->wup + (size_t)l * F * D * 2, D, S, F, D, 1, h->cup + (size_t)l * F, 0,
-                                 L * F, nullptr, st);
-      }
-      VLA_CK(err);
       h->persist_ok = true;
     }
   }
@@ -1069,7 +1107,7 @@ void vla_expert_destroy(vla_expert* h) {
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
                   h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf,
                   h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar, h->noise_buf,
-                  h->beta_rows, h->beta_pre_rows, h->zcodes, h->zalpha, h->wup_sel, h->wdown_sel};
+                  h->beta_rows, h->beta_pre_rows, h->zcodes, h->zalpha, h->wup_sel, h->wdown_sel, h->xt};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_abort) cudaFreeHost(h->h_abort);
@@ -1464,11 +1502,14 @@ vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kerne
     // per step: embed, head; per layer: 4 quantisers, 4 GEMMs, attention
     *kernels = h->S * (2 + 9 * h->cfg.n_layers);
   } else if (h->fused) {
-    const int T = B * h->cfg.horizon;
-    const int extra = (plan_linear(h, h->qkvdim, h->cfg.width, T, true).bmode == 0) +
-                      (plan_linear(h, h->F_eff, h->cfg.width, T, true).bmode == 0);
+    const int T = B * h->cfg.horizon, D = h->cfg.width;
+    const LinPlan pq = plan_linear(h, h->qkvdim, D, T, true), pu = plan_linear(h, h->F_eff, D, T, true);
+    const LinPlan po = plan_linear(h, D, h->qdim, T, false), pd = plan_linear(h, D, h->F_eff, T, false);
+    const bool fn = factored_norm(h, pq, po, pu, pd);
+    const int extra = fn ? 0 : (pq.bmode == 0) + (pu.bmode == 0);
     // per step: embed, head; per layer: 4 GEMMs and the attention, plus the
-    // standalone norms when the in-GEMM prologue does not fit
+    // standalone norms when neither the in-GEMM prologue nor the factored
+    // form applies
     *kernels = h->S * (2 + (5 + extra) * h->cfg.n_layers);
   } else {
     *kernels = h->S * (1 + 10 * h->cfg.n_layers);

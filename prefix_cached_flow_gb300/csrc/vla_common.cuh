@@ -607,6 +607,17 @@ struct LinArgs {
   float* xss;
   int* status;
   unsigned long long* tl;  // event trace (VLA_TIMELINE builds), else unused
+  // Factored modulated RMSNorm (many-token kernel only).  With
+  // u = h r (1 + gamma) + beta and r = 1 / rms(h):  W u = r W ((1 + gamma) h) + W beta.
+  // EPI_RESID: xt_out (nullable) [T][D] bf16 receives (1 + xt_gamma[n]) h_new,
+  // the operand of the next normed map.  EPI_QKV / EPI_GELU: if fn_c is set,
+  // the B operand is that scaled h, and y = r_t acc + fn_c[n], with r_t from the
+  // fn_nss per-block sums of squares fn_ss [fn_nss][T].
+  bf16* xt_out;
+  const float* xt_gamma;  // [D]
+  const float* fn_c;      // [N]  W beta of this (step, layer)
+  const float* fn_ss;
+  int fn_nss;
 };
 size_t linear_smem_bytes(const LinArgs& g);
 cudaError_t linear_kernels_init();
@@ -775,8 +786,9 @@ cudaError_t launch_head(const ExpertDims& d, const StepBufs& b, int step, int sp
 // Fused-path helpers: h = x W_in^T with its row sums of squares (1 slot);
 // u = modulated RMSNorm of h as bf16 [T][D] (for token tiles too large for
 // the in-GEMM prologue); the velocity head reading h directly.
+// xt (nullable) also receives bf16((1 + xgam) h) (factored modulated norm).
 cudaError_t launch_embed_ss(const ExpertDims& d, const StepBufs& b, const float* x_in, float* ss_out, DevCtl ctl,
-                            cudaStream_t st);
+                            cudaStream_t st, bf16* xt = nullptr, const float* xgam = nullptr);
 // Sum-of-squares slots k_embed_ss / k_embed_ss_multi write for this shape.
 int embed_ss_slots(const ExpertDims& d);
 cudaError_t launch_modnorm(const ExpertDims& d, const float* h, const float* ss, int n_ss, const float* gamma,

@@ -110,12 +110,14 @@ def test_prefix_mask_w2a8():
 
 
 @pytest.mark.parametrize("name,flags", [("small_bf16", 0), ("full_bf16_b1", 0), ("small_bf16", "persist"),
-                                        ("tiny_f32", 0)])
+                                        ("small_bf16", "wide"), ("tiny_f32", 0)])
 def test_reverse_schedule(name, flags):
+    """flags "wide": the many-token linears with the factored norm, whose
+    W beta tables follow the reversed time."""
     import torch
     import prefix_cached_flow_gb300 as V
     cfg = CONFIGS[name].replace(reverse=True)
-    fl = V.FLAG_PERSIST if flags == "persist" else 0
+    fl = {0: 0, "persist": V.FLAG_PERSIST, "wide": V.FLAG_LINEAR_WIDE}[flags]
     Z, noise = make_observations(cfg, cfg.B)
     ex, w = _expert(cfg, cfg.B, cfg.P, fl)
     Kc, Vc = _cache(ex, cfg, Z)
