@@ -630,8 +630,8 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
 
 // Persistent many-token linear kernel (k_linear_wide.cu): same LinArgs and
 // epilogues (EPI_QKV, EPI_RESID, EPI_GELU, and EPI_KV for the prefix K/V
-// build; bf16 weights, TMA'd tokens with a 64 x BN box, KS = K), BN in
-// {64, 128, 192, 256}, N a multiple of 128.
+// build; bf16 weights, TMA'd tokens with a 64 x BN box, KS = K), BN a
+// multiple of 16 in [64, 256], N a multiple of 128.
 size_t linear_wide_smem_bytes(int BN);
 // GeLU by erff and by the many-token epilogue's approximation, elementwise.
 cudaError_t launch_gelu_forms(const float* x, int n, float* exact, float* fast, cudaStream_t st);
