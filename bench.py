@@ -310,6 +310,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = CONFIGS[args.workload]
+    if args.solver_steps:
+        cfg = cfg.replace(S=args.solver_steps)
     w = make_weights(cfg)
     if cfg.w2a8:
         import oracle as O
@@ -397,6 +399,8 @@ def run_ours(args):
         import __graft_entry__
         __graft_entry__.build()
     cfg = CONFIGS[args.workload]
+    if args.solver_steps:
+        cfg = cfg.replace(S=args.solver_steps)
     B = cfg.B
     w = make_weights(cfg)
     Z, noise = make_observations(cfg.replace(seed=replica_seed(cfg.seed, rank)), B)
@@ -505,6 +509,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", action="store_true",
                     help="time the chosen workload alone (no Eq. (3) sweep, no other workloads)")
+    ap.add_argument("--solver-steps", type=int, default=0,
+                    help="override the workload's number of Euler steps S (0: the workload's own)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -376,7 +376,12 @@ bool wide_applies(unsigned flags, int num_sms, int N, int K, int T) {
 
 // Cluster split-K plan: the smallest power-of-two cluster (<= 16) that puts
 // about one CTA on every SM, with the modulated-norm prologue fused when the
-// CTA's B slice fits in shared memory.
+// CTA's B slice fits in shared memory.  Packed ternary weights: clusters of
+// at most 8 and a ring of at most 90 KB, so that two CTAs (and the next
+// kernel's early CTAs) fit on an SM and every grid runs as one wave (with
+// 160 KB rings and clusters of 16 the batch-1 W2A8 O, up and down
+// projections ran as two waves each; measured per solve: 16.45 -> 12.02 ms
+// at B = 1, 23.48 -> 16.62 ms at B = 16; a 110 KB ring gave 12.16 / 16.93).
 LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool packed) {
   LinPlan p;
   p.BN = T >= 256 ? 256 : round_up(T < 16 ? 16 : T, 16);
@@ -384,7 +389,8 @@ LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool p
   p.tiles_t = cdiv(T, p.BN);
   const int tiles = p.tiles_n * p.tiles_t;
   p.C = 1;
-  while (p.C < 16 && tiles * p.C < num_sms && K % (p.C * 2 * 64) == 0) p.C *= 2;
+  const int cmax = packed ? 8 : 16;
+  while (p.C < cmax && tiles * p.C < num_sms && K % (p.C * 2 * 64) == 0) p.C *= 2;
   p.KS = K / p.C;
   const int nkb = p.KS / 64;
   const int b_tile = p.BN * 128;
@@ -393,7 +399,7 @@ LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool p
   // KS / 8 must divide 128
   const int kcs = p.KS / 8;
   p.bmode = (want_norm && b_res <= 96 * 1024 && kcs <= 128 && 128 % kcs == 0) ? 1 : 0;
-  const int budget = 200 * 1024 - (p.bmode ? b_res : 0);
+  const int budget = (packed ? 90 * 1024 : 200 * 1024) - (p.bmode ? b_res : 0);
   const int per_stage = 128 * 128 + (p.bmode ? 0 : b_tile) + (packed ? 128 * 16 : 0);
   int st = budget / per_stage;
   if (st > 8) st = 8;
