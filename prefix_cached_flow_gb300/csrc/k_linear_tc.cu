@@ -47,7 +47,7 @@ __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   const uint32_t nkb = (uint32_t)(g.KS / 64);
   s.a = 0;
   s.b = (uint32_t)g.stages * kA;
-  s.hs = s.b + (g.bmode == 0 ? (uint32_t)g.stages * b_tile : nkb * b_tile);
+  s.hs = s.b + (g.bmode != 1 ? (uint32_t)g.stages * b_tile : nkb * b_tile);
   s.pk = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
   const uint32_t end = s.pk + (g.amode == 1 ? (uint32_t)g.stages * kPk : 0u);
   s.region = end;
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(BMODE == 0 ? (const void*)&tmB : (const void*)&tmH);
+    tma_prefetch_desc(BMODE != 1 ? (const void*)&tmB : (const void*)&tmH);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, ncols);
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(128, 1)
   // B stage); packed ternary stages put their B tile on aready[s] (with the
   // decoders' arrivals) instead, so the codes can be decoded before the
   // previous kernel has finished.
-  const uint32_t stage_tx = AMODE == 1 ? kPk : kA + (BMODE == 0 ? b_tile : 0u);
+  const uint32_t stage_tx = AMODE == 1 ? kPk : kA + (BMODE != 1 ? b_tile : 0u);
   // A stage i: bf16 tile by TMA, or its 2-bit codes (16 bytes per row per 64 K)
   auto load_a = [&](int i, int s, uint64_t pol) {
     if (AMODE == 1)
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(128, 1)
       if (AMODE == 1) {
         mbar_arrive_expect_tx(&aready[s], b_tile);
         tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &aready[s], k0 + i * 64, t0);
-      } else if (BMODE == 0) {
+      } else if (BMODE != 1) {
         tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &full[s], k0 + i * 64, t0);
       }
       issued = i + 1;
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(128, 1)
       if (i == nkb - 1) VLA_TL(g.tl, 32, 15);
       tc_fence_after();
       const uint32_t a_addr = smem_u32(Abase + (size_t)s * kA);
-      const uint32_t b_addr = smem_u32(Bbase + (size_t)(BMODE == 0 ? s : i) * b_tile);
+      const uint32_t b_addr = smem_u32(Bbase + (size_t)(BMODE != 1 ? s : i) * b_tile);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_bf16(tmem, sdesc_k128(a_addr + k * 32), sdesc_k128(b_addr + k * 32), idesc, (i > 0 || k > 0) ? 1u : 0u);
@@ -317,6 +317,40 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
 
+  // Factored modulated norm (BMODE 2), fetched while the MMAs run: the row
+  // scales r_t of this tile's tokens into rstat (QKV / GeLU maps), and the
+  // thread's W beta values (QKV / GeLU) or next-norm scales 1 + gamma
+  // (residual map, which writes (1 + gamma) h_new for the next normed map).
+  // Split path: the thread's rows are the same quad in every iteration.
+  constexpr bool FN_IN = BMODE == 2 && (EPI == EPI_QKV || EPI == EPI_GELU);
+  constexpr bool FN_OUT = BMODE == 2 && EPI == EPI_RESID;
+  float4 fn4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (FN_IN && threadIdx.x >= 64) {  // warps 2-3 (the producer and MMA threads are still busy)
+    for (int t = threadIdx.x - 64; t < BN; t += 64) {
+      float v[kMaxC];  // every slot's load in flight at once
+#pragma unroll
+      for (int sl = 0; sl < kMaxC; ++sl)
+        v[sl] = (sl < g.fn_nss && t0 + t < g.T) ? g.fn_ss[(size_t)sl * g.T + t0 + t] : 0.f;
+      float ssum = 0.f;
+#pragma unroll
+      for (int sl = 0; sl < kMaxC; ++sl) ssum += v[sl];
+      rstat[t] = rsqrtf(ssum / (float)g.D + g.eps);
+    }
+  }
+  if (FN_IN || FN_OUT) {
+    const float* src = FN_IN ? g.fn_c : g.xt_gamma;
+    const float add = FN_IN ? 0.f : 1.f;
+    if (SPLIT) {
+      const int n = m0 + rank * RPR + (threadIdx.x % qpc) * 4;
+      if (n < g.N) {
+        fn4 = *(const float4*)(src + n);
+        fn4.x += add; fn4.y += add; fn4.z += add; fn4.w += add;
+      }
+    } else {
+      const int n = m0 + threadIdx.x;
+      if (n < g.N) fn4.x = src[n] + add;
+    }
+  }
   // W2A8 scales, fetched while the MMAs run: the thread's weight-scale quad
   // (the same rows in every epilogue iteration of the split path, since its
   // quads per column divide 128) and the token scales of its first two
@@ -373,12 +407,14 @@ __global__ void __launch_bounds__(128, 1)
           if (EPI != EPI_W2A8_OUT && g.accout) g.accout[(size_t)t * g.N + n] = (int32_t)y;  // diagnostic tap
           y = w2a8_scale(y, g.alpha[t], be);
         }
+        if (FN_IN) y = fmaf(rstat[c0 + j], y, fn4.x);
         float sq = 0.f;
         if (valid) {
           if (EPI == EPI_RESID) {
             float* hp = g.h + (size_t)t * g.D + n;
             const float hv = *hp + y;
             *hp = hv;
+            if (FN_OUT) g.xt_out[(size_t)t * g.D + n] = __float2bfloat16_rn(fn4.x * hv);
             sq = hv * hv;
           } else if (EPI == EPI_GELU) {
             if (g.g32)
@@ -473,6 +509,13 @@ __global__ void __launch_bounds__(128, 1)
       if (EPI != EPI_W2A8_OUT && g.accout)  // diagnostic tap of the exact accumulators
         *(int4*)(g.accout + (size_t)t * g.N + n) = make_int4((int)raw.x, (int)raw.y, (int)raw.z, (int)raw.w);
     }
+    if (FN_IN && valid) {
+      const float rr = rstat[col];
+      acc.x = fmaf(rr, acc.x, fn4.x);
+      acc.y = fmaf(rr, acc.y, fn4.y);
+      acc.z = fmaf(rr, acc.z, fn4.z);
+      acc.w = fmaf(rr, acc.w, fn4.w);
+    }
     if (EPI == EPI_RESID) {
       float ss = 0.f;
       if (valid) {
@@ -480,6 +523,12 @@ __global__ void __launch_bounds__(128, 1)
         float4 hv = have_prev ? hprev : *hp;
         hv.x += acc.x; hv.y += acc.y; hv.z += acc.z; hv.w += acc.w;
         *hp = hv;
+        if (FN_OUT) {
+          uint2 xk;
+          xk.x = pack_bf16x2(fn4.x * hv.x, fn4.y * hv.y);
+          xk.y = pack_bf16x2(fn4.z * hv.z, fn4.w * hv.w);
+          *(uint2*)(g.xt_out + (size_t)t * g.D + n) = xk;
+        }
         ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
       }
       for (int o = qpc >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -638,6 +687,10 @@ cudaError_t linear_kernels_init() {
   if (e == cudaSuccess) e = init_one<EPI_RESID, 0, 0>();
   if (e == cudaSuccess) e = init_one<EPI_GELU, 0, 0>();
   if (e == cudaSuccess) e = init_one<EPI_GELU, 0, 1>();
+  // factored modulated norm (bmode 2)
+  if (e == cudaSuccess) e = init_one<EPI_QKV, 0, 2>();
+  if (e == cudaSuccess) e = init_one<EPI_RESID, 0, 2>();
+  if (e == cudaSuccess) e = init_one<EPI_GELU, 0, 2>();
   // packed ternary weights (W2A8)
   if (e == cudaSuccess) e = init_one<EPI_QKV, 1, 0>();
   if (e == cudaSuccess) e = init_one<EPI_RESID, 1, 0>();
@@ -651,7 +704,10 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
                           int tiles_n, int tiles_t, int C, cudaStream_t st) {
   if (g.BN < 16 || g.BN > 256 || g.BN % 16 || g.KS % 64 || g.KS < 64 || g.stages < 1 || C < 1 || C > kMaxC ||
       (C & (C - 1)) || g.N % 4 || (g.bmode == 1 && (g.n_ss_in < 1 || g.n_ss_in > kMaxC)) ||
-      (g.amode == 1 && g.bmode != 0) || (g.amode == 1) != (g.w2a8 == 1))
+      (g.amode == 1 && g.bmode != 0) || (g.amode == 1) != (g.w2a8 == 1) ||
+      (g.bmode == 2 && g.epi == EPI_RESID && (!g.xt_out || !g.xt_gamma)) ||
+      (g.bmode == 2 && (g.epi == EPI_QKV || g.epi == EPI_GELU) &&
+       (!g.fn_c || !g.fn_ss || g.fn_nss < 1 || g.fn_nss > kMaxC)))
     return cudaErrorInvalidValue;
   const size_t smem = linear_smem_bytes(g);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -665,6 +721,9 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
   VLA_LIN_CASE(EPI_RESID, 0, 0)
   VLA_LIN_CASE(EPI_GELU, 0, 0)
   VLA_LIN_CASE(EPI_GELU, 0, 1)
+  VLA_LIN_CASE(EPI_QKV, 0, 2)
+  VLA_LIN_CASE(EPI_RESID, 0, 2)
+  VLA_LIN_CASE(EPI_GELU, 0, 2)
   VLA_LIN_CASE(EPI_QKV, 1, 0)
   VLA_LIN_CASE(EPI_RESID, 1, 0)
   VLA_LIN_CASE(EPI_GELU, 1, 0)

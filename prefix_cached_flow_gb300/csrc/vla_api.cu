@@ -414,12 +414,10 @@ LinPlan plan_linear(const vla_expert* h, int N, int K, int T, bool want_norm) {
   return plan_linear_sms(h->num_sms, N, K, T, want_norm && !h->w2a8, h->w2a8);
 }
 
-// The many-token solver folds its modulated norms into the linears when all
-// four maps of a layer run on the many-token kernel (see
-// enqueue_denoise_fused).
-bool factored_norm(const vla_expert* h, const LinPlan& pq, const LinPlan& po, const LinPlan& pu, const LinPlan& pd) {
-  return h->xt && pq.wide && po.wide && pu.wide && pd.wide && h->F_eff == h->cfg.mlp_width;
-}
+// The bf16 solver folds its modulated norms into the linears (see
+// enqueue_denoise_fused) whenever the handle holds the W beta tables for its
+// MLP width.
+bool factored_norm(const vla_expert* h) { return h->xt && h->F_eff == h->cfg.mlp_width; }
 
 // One linear layer on the kernel its plan names.
 cudaError_t run_lin(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmH, const LinArgs& a,
@@ -565,9 +563,15 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   const ExpertDims d = make_dims(h, B, P);
   const StepBufs sb = make_bufs(h, P);
   const int T = B * c.horizon, D = c.width, F = h->F_eff, L = c.n_layers;
-  const LinPlan pq = plan_linear(h, h->qkvdim, D, T, true);
+  // Factored modulated norm: W u = r W((1 + gamma) h) + W beta.  Every
+  // residual epilogue (and the input projection) writes (1 + gamma) h in
+  // bf16 for the next normed map, whose epilogue applies the row scale r and
+  // adds W beta (a per-(step, layer) table): no separate norm pass and no
+  // norm prologue on the critical path of the next map.
+  const bool fn = factored_norm(h);
+  const LinPlan pq = plan_linear(h, h->qkvdim, D, T, !fn);
   const LinPlan po = plan_linear(h, D, h->qdim, T, false);
-  const LinPlan pu = plan_linear(h, F, D, T, true);
+  const LinPlan pu = plan_linear(h, F, D, T, !fn);
   const LinPlan pd = plan_linear(h, D, F, T, false);
   bf16* act = (bf16*)h->act;
   CUtensorMap tm_uq, tm_uu, tm_o, tm_g;  // activations as B operands (box: 64 x the plan's BN)
@@ -578,11 +582,6 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
   VLA_ST(plan_attention(h, B, P, kc, vc, act, nullptr, &ap));
   CUtensorMap tmH;
   if (tc_encode_2d_f32(&tmH, h->h, D, T, 64, pq.BN)) return VLA_ERR_CUDA;
-  // Many tokens: the modulated norms are factored into the linears
-  // (W u = r W((1 + gamma) h) + W beta): each residual epilogue writes
-  // (1 + gamma) h for the next normed map, whose epilogue applies r and adds
-  // W beta, so no separate norm pass re-reads h.
-  const bool fn = factored_norm(h, pq, po, pu, pd);
   CUtensorMap tm_xq, tm_xu;
   if (fn && (tc_encode_2d_bf16(&tm_xq, h->xt, D, T, 64, pq.BN) || tc_encode_2d_bf16(&tm_xu, h->xt, D, T, 64, pu.BN)))
     return VLA_ERR_CUDA;
@@ -609,6 +608,7 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       a.epi = EPI_QKV; a.q = (bf16*)h->q; a.ks = (bf16*)h->ks; a.vst = (bf16*)h->vs;
       if (fn) {
         a.fn_c = h->cqkv + ((size_t)k * L + l) * h->qkvdim; a.fn_ss = h->ss2; a.fn_nss = n_ss;
+        if (!pq.wide) a.bmode = 2;
       } else if (pq.bmode == 1) {
         a.h_in = h->h; a.ss_in = h->ss2; a.n_ss_in = n_ss; a.gamma = mod; a.beta = mod + D;
       } else {
@@ -620,13 +620,17 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       // O projection + residual
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
-      if (fn) { a.xt_out = h->xt; a.xt_gamma = mod + 2 * D; }
+      if (fn) {
+        a.xt_out = h->xt; a.xt_gamma = mod + 2 * D;
+        if (!po.wide) a.bmode = 2;
+      }
       VLA_CK(run_lin(&h->tm_wo, &tm_o, &tmH, a, po, st));
       // MLP up + GeLU
       a = lin_args(h, pu, F, T, l);
       a.epi = EPI_GELU; a.g = (bf16*)h->gbuf; a.ldg = F; a.tl = tls(3);
       if (fn) {
         a.fn_c = h->cup + ((size_t)k * L + l) * F; a.fn_ss = h->ss1; a.fn_nss = po.tiles_n;
+        if (!pu.wide) a.bmode = 2;
       } else if (pu.bmode == 1) {
         a.h_in = h->h; a.ss_in = h->ss1; a.n_ss_in = po.tiles_n; a.gamma = mod + 2 * D; a.beta = mod + 3 * D;
       } else {
@@ -636,7 +640,10 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       // MLP down + residual
       a = lin_args(h, pd, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.tl = tls(4);
-      if (fn && l + 1 < L) { a.xt_out = h->xt; a.xt_gamma = mod + 4 * D; }  // the next layer's gamma_a
+      if (fn && l + 1 < L) {  // the next layer's gamma_a
+        a.xt_out = h->xt; a.xt_gamma = mod + 4 * D;
+        if (!pd.wide) a.bmode = 2;
+      }
       VLA_CK(run_lin(&h->tm_wdown, &tm_g, &tmH, a, pd, st));
       n_ss = pd.tiles_n;
     }
@@ -1026,7 +1033,7 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
     VLA_CK(e2);
     return VLA_OK;
   };
-  if (h->fused && !h->w2a8 && !h->f32 && wide_applies(c.flags, h->num_sms, D, h->qdim, Tm)) {
+  if (h->fused && !h->w2a8 && !h->f32) {
     if ((s = wbeta_tables()) != VLA_OK) return s;
     if ((s = dalloc(&h->xt, (size_t)Tm * D * 2)) != VLA_OK) return s;
   }
@@ -1509,9 +1516,8 @@ vla_status vla_expert_launch_count(const vla_expert* h, int B, int P, int* kerne
     *kernels = h->S * (2 + 9 * h->cfg.n_layers);
   } else if (h->fused) {
     const int T = B * h->cfg.horizon, D = h->cfg.width;
-    const LinPlan pq = plan_linear(h, h->qkvdim, D, T, true), pu = plan_linear(h, h->F_eff, D, T, true);
-    const LinPlan po = plan_linear(h, D, h->qdim, T, false), pd = plan_linear(h, D, h->F_eff, T, false);
-    const bool fn = factored_norm(h, pq, po, pu, pd);
+    const bool fn = factored_norm(h);
+    const LinPlan pq = plan_linear(h, h->qkvdim, D, T, !fn), pu = plan_linear(h, h->F_eff, D, T, !fn);
     const int extra = fn ? 0 : (pq.bmode == 0) + (pu.bmode == 0);
     // per step: embed, head; per layer: 4 GEMMs and the attention, plus the
     // standalone norms when neither the in-GEMM prologue nor the factored
