@@ -384,6 +384,10 @@ __global__ void k_head(ExpertDims d, StepBufs b, int step, int splits, float dt,
 // factored modulated norm (many-token linears).
 __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl, bf16* xt,
                            const float* xgam) {
+  // The first kernel of a solver step waits before it lets the next kernel
+  // start: the attention kernels load the prefix cache before their own
+  // grid-dependency wait, so no early launch may reach back past the cache
+  // build that precedes the solve.
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
@@ -414,6 +418,10 @@ __global__ void k_embed_ss(ExpertDims d, StepBufs b, const float* x_in, float* s
 constexpr int kMT = 16;
 __global__ void k_embed_ss_multi(ExpertDims d, StepBufs b, const float* x_in, float* ss_out, DevCtl ctl, bf16* xt,
                                  const float* xgam) {
+  // The first kernel of a solver step waits before it lets the next kernel
+  // start: the attention kernels load the prefix cache before their own
+  // grid-dependency wait, so no early launch may reach back past the cache
+  // build that precedes the solve.
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
@@ -576,8 +584,13 @@ __global__ void k_head_multi(ExpertDims d, StepBufs b, int step, float dt, const
 // and the codes (as exact bf16 carriers).
 __global__ void k_quant_norm(int D, float eps, const float* h, const float* gamma, const float* beta, bf16* codes,
                              float* alpha, float* u_out) {
+  // A few rows (batch 1): let the next kernel (a ternary linear) start its
+  // weight prologue now, under this one; with many rows its early CTAs
+  // would compete with this kernel's for the SMs.
+  const bool early = gridDim.x <= 32;
+  if (early && threadIdx.x == 0) griddep_launch_dependents();
   griddep_wait();
-  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (!early && threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
@@ -602,8 +615,13 @@ __global__ void k_quant_norm(int D, float eps, const float* h, const float* gamm
 // Eq. (4) on fp32 rows x [T][K]; codes as bf16 carriers (I8 false) or int8.
 template <bool I8>
 __global__ void k_quant_rows(int K, const float* x, void* codes, float* alpha) {
+  // A few rows (batch 1): let the next kernel (a ternary linear) start its
+  // weight prologue now, under this one; with many rows its early CTAs
+  // would compete with this kernel's for the SMs.
+  const bool early = gridDim.x <= 32;
+  if (early && threadIdx.x == 0) griddep_launch_dependents();
   griddep_wait();
-  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (!early && threadIdx.x == 0) griddep_launch_dependents();
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + K;
@@ -680,8 +698,13 @@ __global__ void k_modnorm_v(int T, int D, float eps, const float* h, const float
 template <int RV>
 __global__ void k_quant_norm_v(int D, float eps, const float* h, const float* gamma, const float* beta, bf16* codes,
                                float* alpha, float* u_out) {
+  // A few rows (batch 1): let the next kernel (a ternary linear) start its
+  // weight prologue now, under this one; with many rows its early CTAs
+  // would compete with this kernel's for the SMs.
+  const bool early = gridDim.x <= 32;
+  if (early && threadIdx.x == 0) griddep_launch_dependents();
   griddep_wait();
-  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (!early && threadIdx.x == 0) griddep_launch_dependents();
   __shared__ float red[32];
   const int t = blockIdx.x, nc = D >> 2;
   float4 v[RV], g[RV], b[RV];
@@ -716,8 +739,13 @@ __global__ void k_quant_norm_v(int D, float eps, const float* h, const float* ga
 // Eq. (4) on fp32 rows x [T][K]; codes as bf16 carriers (I8 false) or int8.
 template <int RV, bool I8>
 __global__ void k_quant_rows_v(int K, const float* x, void* codes, float* alpha) {
+  // A few rows (batch 1): let the next kernel (a ternary linear) start its
+  // weight prologue now, under this one; with many rows its early CTAs
+  // would compete with this kernel's for the SMs.
+  const bool early = gridDim.x <= 32;
+  if (early && threadIdx.x == 0) griddep_launch_dependents();
   griddep_wait();
-  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (!early && threadIdx.x == 0) griddep_launch_dependents();
   __shared__ float red[32];
   const int t = blockIdx.x, nc = K >> 2;
   float4 v[RV];
