@@ -34,6 +34,8 @@ namespace {
 constexpr uint32_t kA = 128 * 128;  // bytes of one 128 x 64 bf16 weight stage
 constexpr int kMaxC = 16;           // largest cluster
 constexpr int kPre = 2;             // residual quads prefetched per thread
+constexpr int kSlotRound = 32;      // sums-of-squares slots loaded per round (factored norm)
+constexpr int kMaxSlots = 256;      // slots a factored-norm map may read (16 ranks x 16 row blocks)
 
 
 struct LinSmem {
@@ -327,13 +329,15 @@ __global__ void __launch_bounds__(128, 1)
   float4 fn4 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (FN_IN && threadIdx.x >= 64) {  // warps 2-3 (the producer and MMA threads are still busy)
     for (int t = threadIdx.x - 64; t < BN; t += 64) {
-      float v[kMaxC];  // every slot's load in flight at once
-#pragma unroll
-      for (int sl = 0; sl < kMaxC; ++sl)
-        v[sl] = (sl < g.fn_nss && t0 + t < g.T) ? g.fn_ss[(size_t)sl * g.T + t0 + t] : 0.f;
       float ssum = 0.f;
+      for (int s0 = 0; s0 < g.fn_nss; s0 += kSlotRound) {
+        float v[kSlotRound];  // a round of slot loads in flight at once; fixed summation order
 #pragma unroll
-      for (int sl = 0; sl < kMaxC; ++sl) ssum += v[sl];
+        for (int sl = 0; sl < kSlotRound; ++sl)
+          v[sl] = (s0 + sl < g.fn_nss && t0 + t < g.T) ? g.fn_ss[(size_t)(s0 + sl) * g.T + t0 + t] : 0.f;
+#pragma unroll
+        for (int sl = 0; sl < kSlotRound; ++sl) ssum += v[sl];
+      }
       rstat[t] = rsqrtf(ssum / (float)g.D + g.eps);
     }
   }
@@ -623,7 +627,13 @@ __global__ void __launch_bounds__(128, 1)
     epilogue(acc, live, col, quad, make_float4(0.f, 0.f, 0.f, 0.f), false, it);
   }
   VLA_TL(g.tl, 0, 11);
-  if (EPI == EPI_RESID && g.ss_out) {
+  if (EPI == EPI_RESID && g.ss_out && g.ss_per_rank) {
+    // Each rank's own slot; the consumer sums them.
+    __syncthreads();
+    if (ok)
+      for (int col = threadIdx.x; col < tcols; col += 128)
+        g.ss_out[((size_t)blockIdx.x * C + rank) * g.T + t0 + col] = rstat[col];
+  } else if (EPI == EPI_RESID && g.ss_out) {
     // Rank 0 combines the ranks' per-token sums of squares (fixed order).
     __syncthreads();
     float* myss = g.xss + ((size_t)tile * C + rank) * BN;
@@ -707,7 +717,7 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
       (g.amode == 1 && g.bmode != 0) || (g.amode == 1) != (g.w2a8 == 1) ||
       (g.bmode == 2 && g.epi == EPI_RESID && (!g.xt_out || !g.xt_gamma)) ||
       (g.bmode == 2 && (g.epi == EPI_QKV || g.epi == EPI_GELU) &&
-       (!g.fn_c || !g.fn_ss || g.fn_nss < 1 || g.fn_nss > kMaxC)))
+       (!g.fn_c || !g.fn_ss || g.fn_nss < 1 || g.fn_nss > kMaxSlots)))
     return cudaErrorInvalidValue;
   const size_t smem = linear_smem_bytes(g);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;

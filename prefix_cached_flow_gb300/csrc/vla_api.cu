@@ -620,16 +620,19 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       // O projection + residual
       a = lin_args(h, po, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss1; a.tl = tls(2);
+      // split O feeding a split up map: one statistics slot per rank
+      const int nss_o = (fn && !po.wide && !pu.wide) ? po.tiles_n * po.C : po.tiles_n;
       if (fn) {
         a.xt_out = h->xt; a.xt_gamma = mod + 2 * D;
         if (!po.wide) a.bmode = 2;
+        a.ss_per_rank = nss_o != po.tiles_n;
       }
       VLA_CK(run_lin(&h->tm_wo, &tm_o, &tmH, a, po, st));
       // MLP up + GeLU
       a = lin_args(h, pu, F, T, l);
       a.epi = EPI_GELU; a.g = (bf16*)h->gbuf; a.ldg = F; a.tl = tls(3);
       if (fn) {
-        a.fn_c = h->cup + ((size_t)k * L + l) * F; a.fn_ss = h->ss1; a.fn_nss = po.tiles_n;
+        a.fn_c = h->cup + ((size_t)k * L + l) * F; a.fn_ss = h->ss1; a.fn_nss = nss_o;
         if (!pu.wide) a.bmode = 2;
       } else if (pu.bmode == 1) {
         a.h_in = h->h; a.ss_in = h->ss1; a.n_ss_in = po.tiles_n; a.gamma = mod + 2 * D; a.beta = mod + 3 * D;
@@ -640,12 +643,15 @@ vla_status enqueue_denoise_fused(vla_expert* h, const void* kc, const void* vc, 
       // MLP down + residual
       a = lin_args(h, pd, D, T, l);
       a.epi = EPI_RESID; a.h = h->h; a.ss_out = h->ss2; a.tl = tls(4);
+      // split down feeding the next layer's split QKV map: one slot per rank
+      const int nss_d = (fn && !pd.wide && !pq.wide) ? pd.tiles_n * pd.C : pd.tiles_n;
       if (fn && l + 1 < L) {  // the next layer's gamma_a
         a.xt_out = h->xt; a.xt_gamma = mod + 4 * D;
         if (!pd.wide) a.bmode = 2;
+        a.ss_per_rank = nss_d != pd.tiles_n;
       }
       VLA_CK(run_lin(&h->tm_wdown, &tm_g, &tmH, a, pd, st));
-      n_ss = pd.tiles_n;
+      n_ss = a.ss_per_rank ? nss_d : pd.tiles_n;
     }
     VLA_CK(launch_head_fused(d, sb, k, dt, x_in, actions, tap, st));
   }
@@ -954,8 +960,8 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
   if ((s = dalloc(&h->ks, (size_t)Tm * h->kvdim * ae)) != VLA_OK) return s;
   if ((s = dalloc(&h->vs, (size_t)c.max_batch * h->kvdim * h->Hp * ae)) != VLA_OK) return s;
   if (h->fused) {
-    // sums of squares: at most one slot per 128-row tile of D, or 1 (embed)
-    h->ss_elems = (size_t)(D / 128 + 1) * Tm;
+    // sums of squares: at most one slot per (128-row tile of D, split rank)
+    h->ss_elems = (size_t)(D / 128 * 16 + 8) * Tm;
     if ((s = dalloc(&h->ss1, h->ss_elems * 4)) != VLA_OK) return s;
     if ((s = dalloc(&h->ss2, h->ss_elems * 4)) != VLA_OK) return s;
     if ((s = dalloc(&h->gbuf, (size_t)Tm * c.mlp_width * 2)) != VLA_OK) return s;

@@ -615,6 +615,11 @@ struct LinArgs {
   // fn_nss per-block sums of squares fn_ss [fn_nss][T].
   bf16* xt_out;
   const float* xt_gamma;  // [D]
+  // EPI_RESID, cluster split: each rank writes its own rows' per-token sums of
+  // squares to slot (tile_n * C + rank) of ss_out instead of combining the
+  // ranks' sums behind a second cluster barrier (the consumer sums the
+  // slots, in fixed order)
+  int ss_per_rank;
   const float* fn_c;      // [N]  W beta of this (step, layer)
   const float* fn_ss;
   int fn_nss;
