@@ -36,6 +36,7 @@ constexpr int kMaxC = 16;           // largest cluster
 constexpr int kPre = 2;             // residual quads prefetched per thread
 constexpr int kSlotRound = 32;      // sums-of-squares slots loaded per round (factored norm)
 constexpr int kMaxSlots = 256;      // slots a factored-norm map may read (16 ranks x 16 row blocks)
+constexpr int kMaxResident = 16;    // k-blocks whose packed codes a CTA holds at once (amode 2)
 
 
 struct LinSmem {
@@ -51,7 +52,8 @@ __host__ __device__ __forceinline__ LinSmem lin_layout(const LinArgs& g) {
   s.b = (uint32_t)g.stages * kA;
   s.hs = s.b + (g.bmode != 1 ? (uint32_t)g.stages * b_tile : nkb * b_tile);
   s.pk = s.hs + (g.bmode == 1 ? nkb * (uint32_t)g.BN * 256u : 0u);
-  const uint32_t end = s.pk + (g.amode == 1 ? (uint32_t)g.stages * kPk : 0u);
+  // packed codes: a ring of `stages` (amode 1) or every k-block of the CTA (amode 2)
+  const uint32_t end = s.pk + (g.amode == 1 ? (uint32_t)g.stages * kPk : (g.amode == 2 ? nkb * kPk : 0u));
   s.region = end;
   s.bars = s.region;                                  // full, empty, done, hbar, aready (+ spare)
   s.slot = s.bars + (4u * (uint32_t)g.stages + 2u) * 8u;
@@ -144,25 +146,39 @@ __global__ void __launch_bounds__(128, 1)
   };
   if (warp == 0 && lane == 0) {
     const uint64_t pol = l2_policy_evict_first();
-    for (int i = 0; i < pre; ++i) {
-      mbar_arrive_expect_tx(&full[i], stage_tx);
-      load_a(i, i, pol);
+    if (AMODE == 2) {
+      // every k-block's codes at once (one barrier): the decode is then
+      // paced by the decoders and the MMAs, not by a load per stage
+      mbar_arrive_expect_tx(&full[0], (uint32_t)nkb * kPk);
+      for (int i = 0; i < nkb; ++i)
+        tma_load_2d_hint(Pk + (size_t)i * kPk, &tmA, &full[0], (k0 + i * 64) / 4, g.a_row0 + m0, pol);
+    } else {
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], stage_tx);
+        load_a(i, i, pol);
+      }
     }
   }
   if (threadIdx.x == 0) griddep_launch_dependents();
-  const bool decoder = AMODE == 1 && warp >= 2;
+  const bool decoder = AMODE >= 1 && warp >= 2;
   if (decoder) {
     // Warps 2-3: decode each stage's 2-bit codes (code q+1, little-endian
     // fields) into the bf16 A tile with the 128-byte swizzle the MMA reads.
     // Weights only: this starts before griddepcontrol.wait.
     const int dt = threadIdx.x - 64;
-    for (int i = 0; i < nkb; ++i) {
+    bool okd = AMODE != 2 || mbar_wait(&full[0], 0, g.status);  // amode 2: every k-block's codes
+    if (!okd) s_fail = 1;
+    for (int i = 0; okd && i < nkb; ++i) {
       const int s = i % NS;
-      if (!mbar_wait(&full[s], (i / NS) & 1, g.status)) {
+      // amode 1: stage s's codes have landed; amode 2: the MMAs have
+      // released decoded stage s (a stage's first use needs no wait)
+      const bool oks = AMODE == 2 ? (i < NS || mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, g.status))
+                                  : mbar_wait(&full[s], (i / NS) & 1, g.status);
+      if (!oks) {
         s_fail = 1;
         break;
       }
-      const uint8_t* pk = Pk + (size_t)s * kPk;
+      const uint8_t* pk = Pk + (size_t)(AMODE == 2 ? i : s) * kPk;
       const uint32_t at = smem_u32(Abase + (size_t)s * kA);
       // Rows dt and dt + 64: one 16-byte load of 64 codes each, eight
       // 16-byte chunks out (consecutive lanes cover all eight swizzle phases).
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(128, 1)
     if (BMODE == 1) {
       mbar_arrive_expect_tx(hbar, (uint32_t)nkb * (uint32_t)BN * 256u);
       for (int i = 0; i < nkb; ++i) tma_load_2d(Hs + (size_t)i * BN * 64, &tmH, hbar, k0 + i * 64, t0);
-    } else if (AMODE == 1) {
+    } else if (AMODE >= 1) {
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&aready[i], b_tile);
         tma_load_2d(Bbase + (size_t)i * b_tile, &tmB, &aready[i], k0 + i * 64, t0);
@@ -259,9 +275,11 @@ __global__ void __launch_bounds__(128, 1)
         s_fail = 1;
         break;
       }
-      mbar_arrive_expect_tx(&full[s], stage_tx);
-      load_a(i, s, pol);
-      if (AMODE == 1) {
+      if (AMODE != 2) {
+        mbar_arrive_expect_tx(&full[s], stage_tx);
+        load_a(i, s, pol);
+      }
+      if (AMODE >= 1) {
         mbar_arrive_expect_tx(&aready[s], b_tile);
         tma_load_2d(Bbase + (size_t)s * b_tile, &tmB, &aready[s], k0 + i * 64, t0);
       } else if (BMODE != 1) {
@@ -276,7 +294,7 @@ __global__ void __launch_bounds__(128, 1)
       const int s = i % NS;
       // One wait per stage: the TMA transaction of the stage (bf16 weights),
       // or the decoded tile plus its B tile (packed ternary weights).
-      if (s_fail || !mbar_wait(AMODE == 1 ? &aready[s] : &full[s], (i / NS) & 1, g.status)) {
+      if (s_fail || !mbar_wait(AMODE >= 1 ? &aready[s] : &full[s], (i / NS) & 1, g.status)) {
         s_fail = 1;
         break;
       }
@@ -361,7 +379,7 @@ __global__ void __launch_bounds__(128, 1)
   // iterations.
   float4 be_pre = make_float4(0.f, 0.f, 0.f, 0.f);
   float al_pre[2] = {0.f, 0.f};
-  if (AMODE == 1 && SPLIT) {
+  if (AMODE >= 1 && SPLIT) {
     const int quad = threadIdx.x % qpc;
     const int n = m0 + rank * RPR + quad * 4;
     if (n < g.N)
@@ -391,7 +409,7 @@ __global__ void __launch_bounds__(128, 1)
     float* wss = (float*)(smem + Ls.wss);
     int slot = 0;
     if (EPI == EPI_QKV) slot = n < g.qdim ? 0 : (n < g.qdim + g.kvdim ? 1 : 2);
-    const float be = (AMODE == 1 && n < g.N)
+    const float be = (AMODE >= 1 && n < g.N)
                          ? (g.wbeta ? g.wbeta[(size_t)g.layer * g.beta_stride + g.beta_off + n] : g.beta_val)
                          : 0.f;
     for (int c0 = 0; c0 < tcols; c0 += 16) {
@@ -407,7 +425,7 @@ __global__ void __launch_bounds__(128, 1)
         const int t = t0 + c0 + j;
         const bool valid = ok && c0 + j < tcols && n < g.N;
         float y = v[j];
-        if (AMODE == 1 && valid) {
+        if (AMODE >= 1 && valid) {
           if (EPI != EPI_W2A8_OUT && g.accout) g.accout[(size_t)t * g.N + n] = (int32_t)y;  // diagnostic tap
           y = w2a8_scale(y, g.alpha[t], be);
         }
@@ -502,7 +520,7 @@ __global__ void __launch_bounds__(128, 1)
     const int n = m0 + rloc, t = t0 + col;
     const bool valid = live && t < g.T && n < g.N;
     const float4 raw = acc;
-    if (AMODE == 1 && valid) {
+    if (AMODE >= 1 && valid) {
       // Eq. (4): exact integer accumulators scaled to bf16
       const float al = it < 2 ? al_pre[it] : g.alpha[t];
       const float4 be = be_pre;
@@ -658,9 +676,10 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0 && lane == 0) {
     const int first = issued > NS ? issued - NS : 0;
     for (int i = first; i < issued; ++i) {
-      mbar_drain(&full[i % NS], (i / NS) & 1);
-      if (AMODE == 1) mbar_drain(&aready[i % NS], (i / NS) & 1);
+      if (AMODE != 2) mbar_drain(&full[i % NS], (i / NS) & 1);
+      if (AMODE >= 1) mbar_drain(&aready[i % NS], (i / NS) & 1);
     }
+    if (AMODE == 2) mbar_drain(&full[0], 0);
     if (BMODE == 1) mbar_drain(hbar, 0);
     mbar_drain(done, 0);  // the MMA warp always commits `done`
   }
@@ -706,6 +725,11 @@ cudaError_t linear_kernels_init() {
   if (e == cudaSuccess) e = init_one<EPI_RESID, 1, 0>();
   if (e == cudaSuccess) e = init_one<EPI_GELU, 1, 0>();
   if (e == cudaSuccess) e = init_one<EPI_W2A8_OUT, 1, 0>();
+  // packed ternary weights, every k-block's codes resident
+  if (e == cudaSuccess) e = init_one<EPI_QKV, 2, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_RESID, 2, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_GELU, 2, 0>();
+  if (e == cudaSuccess) e = init_one<EPI_W2A8_OUT, 2, 0>();
   if (e == cudaSuccess) e = set_max_dyn_smem(k_linear<EPI_KV, 1, 0, 1>);
   return e;
 }
@@ -714,7 +738,8 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
                           int tiles_n, int tiles_t, int C, cudaStream_t st) {
   if (g.BN < 16 || g.BN > 256 || g.BN % 16 || g.KS % 64 || g.KS < 64 || g.stages < 1 || C < 1 || C > kMaxC ||
       (C & (C - 1)) || g.N % 4 || (g.bmode == 1 && (g.n_ss_in < 1 || g.n_ss_in > kMaxC)) ||
-      (g.amode == 1 && g.bmode != 0) || (g.amode == 1) != (g.w2a8 == 1) ||
+      (g.amode >= 1 && g.bmode != 0) || (g.amode >= 1) != (g.w2a8 == 1) || g.amode > 2 ||
+      (g.amode == 2 && g.KS / 64 > kMaxResident) ||
       (g.bmode == 2 && g.epi == EPI_RESID && (!g.xt_out || !g.xt_gamma)) ||
       (g.bmode == 2 && (g.epi == EPI_QKV || g.epi == EPI_GELU) &&
        (!g.fn_c || !g.fn_ss || g.fn_nss < 1 || g.fn_nss > kMaxSlots)))
@@ -738,6 +763,10 @@ cudaError_t launch_linear(const CUtensorMap* tmA, const CUtensorMap* tmB, const 
   VLA_LIN_CASE(EPI_RESID, 1, 0)
   VLA_LIN_CASE(EPI_GELU, 1, 0)
   VLA_LIN_CASE(EPI_W2A8_OUT, 1, 0)
+  VLA_LIN_CASE(EPI_QKV, 2, 0)
+  VLA_LIN_CASE(EPI_RESID, 2, 0)
+  VLA_LIN_CASE(EPI_GELU, 2, 0)
+  VLA_LIN_CASE(EPI_W2A8_OUT, 2, 0)
 #undef VLA_LIN_CASE
   if (g.epi == EPI_KV) fn = (g.amode == 1 && C == 1) ? k_linear<EPI_KV, 1, 0, 1> : nullptr;
   if (!fn) return cudaErrorInvalidValue;

@@ -335,6 +335,7 @@ vla_status enqueue_denoise(vla_expert* h, const void* kc, const void* vc, int B,
 
 struct LinPlan {
   int C = 1, KS = 64, BN = 16, tiles_n = 1, tiles_t = 1, stages = 1, bmode = 0;
+  int amode = 0;      // packed ternary weights: 1 (code ring) or 2 (every k-block's codes resident)
   bool wide = false;  // persistent many-token kernel (k_linear_wide.cu)
   int grid = 0;       // its CTA count
 };
@@ -399,8 +400,13 @@ LinPlan plan_linear_sms(int num_sms, int N, int K, int T, bool want_norm, bool p
   // KS / 8 must divide 128
   const int kcs = p.KS / 8;
   p.bmode = (want_norm && b_res <= 96 * 1024 && kcs <= 128 && 128 % kcs == 0) ? 1 : 0;
-  const int budget = (packed ? 90 * 1024 : 200 * 1024) - (p.bmode ? b_res : 0);
-  const int per_stage = 128 * 128 + (p.bmode ? 0 : b_tile) + (packed ? 128 * 16 : 0);
+  // packed codes: all of the CTA's k-blocks at once when they are few
+  // (loaded together before the grid-dependency wait; the decode is then
+  // paced by the decoders and the MMAs), else a ring beside the decoded tiles
+  p.amode = packed ? (nkb <= 16 ? 2 : 1) : 0;
+  const int resident = p.amode == 2 ? nkb * 128 * 16 : 0;
+  const int budget = (packed ? 90 * 1024 : 200 * 1024) - (p.bmode ? b_res : 0) - resident;
+  const int per_stage = 128 * 128 + (p.bmode ? 0 : b_tile) + (p.amode == 1 ? 128 * 16 : 0);
   int st = budget / per_stage;
   if (st > 8) st = 8;
   if (st > nkb) st = nkb;
@@ -435,7 +441,7 @@ LinArgs lin_args(const vla_expert* h, const LinPlan& p, int N, int T, int layer)
   a.xpart = h->xpart; a.xss = h->xss;
   a.layer = layer;
   if (h->w2a8) {
-    a.amode = 1; a.w2a8 = 1; a.alpha = h->alpha; a.wbeta = h->beta_rows; a.beta_stride = h->beta_stride;
+    a.amode = p.amode; a.w2a8 = 1; a.alpha = h->alpha; a.wbeta = h->beta_rows; a.beta_stride = h->beta_stride;
   }
   return a;
 }
@@ -1650,7 +1656,7 @@ vla_status vla_w2a8_ternary_gemm(const int8_t* a, const float* alpha, const uint
     e = cudaErrorInvalidValue;
   if (e == cudaSuccess) {
     LinArgs g{};
-    g.N = N; g.T = M; g.a_row0 = 0; g.KS = p.KS; g.BN = p.BN; g.stages = p.stages; g.bmode = 0; g.amode = 1;
+    g.N = N; g.T = M; g.a_row0 = 0; g.KS = p.KS; g.BN = p.BN; g.stages = p.stages; g.bmode = 0; g.amode = p.amode;
     g.epi = EPI_W2A8_OUT; g.w2a8 = 1; g.alpha = alpha; g.wbeta = nullptr; g.beta_val = beta;
     g.yout = y; g.accout = acc; g.xpart = xpart; g.xss = xss; g.D = K;
     e = launch_linear(&tmA, &tmB, &tmB, g, p.tiles_n, p.tiles_t, p.C, st);

@@ -566,6 +566,8 @@ struct LinArgs {
   int stages;   // weight ring depth
   int bmode;    // 0: B tiles by TMA (tmB over [T][K] bf16); 1: B = modulated RMSNorm of h
   int amode;    // 0: A (weights) bf16 by TMA; 1: packed 2-bit ternary codes by TMA, decoded to bf16 in smem
+                // (a ring of `stages` code stages); 2: the same with every k-block's codes loaded at once
+                // (KS / 64 <= 16)
   int epi;      // EPI_*
   // W2A8 (Eq. 4): the accumulators are exact integers; y = bf16((acc * alpha_t) * beta)
   int w2a8;
