@@ -12,13 +12,21 @@
 //             v_s^T [B][n_kv][d_h][Hp] (bf16) for the attention kernel;
 //   EPI_RESID h[t][n] += y, and per-(128-row block, token) sums of squares of
 //             the new h for the next modulated RMSNorm (the cluster combines
-//             its ranks' partial sums on chip, rank 0 writes them);
+//             its ranks' partial sums, rank 0 writes them; or every rank
+//             writes its own slot);
 //   EPI_GELU  g[t][n] = bf16(GeLU(y)).
 // The B operand (tokens) is either TMA-loaded from an activation tensor
 // (bmode 0) or built in shared memory from the fp32 residual stream as the
 // time-modulated RMSNorm  h / rms(h) * (1 + gamma) + beta  (bmode 1): one
 // TMA brings the CTA's h tile while the threads fetch the sums of squares
-// and the modulation slices in parallel.
+// and the modulation slices in parallel.  Bmode 2 factors the norm out of
+// the product, W u = r W((1 + gamma) h) + W beta: the B operand is the bf16
+// (1 + gamma) h that the previous residual epilogue wrote (bmode 2 on
+// EPI_RESID), and the QKV / GeLU epilogues apply the row scale r and add
+// W beta.
+// Packed ternary weights (amode 1 and 2, the W2A8 variant): the 2-bit codes
+// arrive by TMA (a ring of stages, or with amode 2 every k-block of the CTA
+// at once) and two decoder warps expand them to the bf16 tile the MMA reads.
 //
 // The weights do not depend on the previous kernel, so their TMA loads are
 // issued before griddepcontrol.wait: under programmatic dependent launch the
