@@ -248,30 +248,11 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
   }
   VLA_TL(a.tl, 0, 9);
-  cluster_sync_all();  // every rank's (m, l) is visible
-  VLA_TL(a.tl, 0, 4);
 
-  // Merge factors for this row: M = max_c m_c, den = sum_c exp2(m_c - M) l_c.
-  const uint32_t mloc = smem_u32(&sm_m[row]), lloc = smem_u32(&sm_l[row]);
-  float mc[CS], lc[CS];
-#pragma unroll
-  for (int c = 0; c < CS; ++c) {
-    mc[c] = ld_dsmem_f32(mapa_shared(mloc, (uint32_t)c));
-    lc[c] = ld_dsmem_f32(mapa_shared(lloc, (uint32_t)c));
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < CS; ++c) M = fmaxf(M, mc[c]);
-  float den = 0.f;
-#pragma unroll
-  for (int c = 0; c < CS; ++c)
-    if (lc[c] > 0.f) den += fast_exp2(mc[c] - M) * lc[c];
-  const float f = (nk > 0 && l > 0.f) ? fast_exp2(m - M) / den : 0.f;
-  VLA_TL(a.tl, 0, 10);
-
-  // Publish f * O_rank (bf16; each rank holds roughly 1/CS of the sum) for the
-  // valid query rows through L2, interleaved as [d_h/8][128 rows][8] so that
-  // a warp's 32 rows form one 512-byte run.
+  // Publish this rank's unnormalised O (bf16) and each row's (m, l) through
+  // L2; O is interleaved as [d_h/8][128 rows][8] so that a warp's 32 rows
+  // form one 512-byte run.  One cluster barrier (release/acquire) then makes
+  // every rank's part visible to the merge.
   const int nrows = (a.group * a.H - qt * 128) < 128 ? (a.group * a.H - qt * 128) : 128;
   const size_t cl = (size_t)bg * a.n_qt + qt;  // this cluster's query tile
   if (s_fail == 0 && nk > 0) {
@@ -287,14 +268,15 @@ __global__ void __launch_bounds__(128, 1)
         for (int q = 0; q < 8; ++q) {
           const uint32_t* w = r + q * 8;
           uint4 u;
-          u.x = pack_bf16x2(f * __uint_as_float(w[0]), f * __uint_as_float(w[1]));
-          u.y = pack_bf16x2(f * __uint_as_float(w[2]), f * __uint_as_float(w[3]));
-          u.z = pack_bf16x2(f * __uint_as_float(w[4]), f * __uint_as_float(w[5]));
-          u.w = pack_bf16x2(f * __uint_as_float(w[6]), f * __uint_as_float(w[7]));
+          u.x = pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+          u.y = pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+          u.z = pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5]));
+          u.w = pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7]));
           __stcg(dst + (size_t)(c0 / 8 + q) * 128, u);
         }
       }
     }
+    if (row < nrows) __stcg(&a.xml[(cl * CS + rank) * 128 + row], make_float2(m, l));
   }
   cluster_sync_all();
   VLA_TL(a.tl, 0, 5);
@@ -304,6 +286,32 @@ __global__ void __launch_bounds__(128, 1)
   const int cols = dh / CS;
   const int q8 = cols / 8;  // 8-column groups in this slice
   if (s_fail == 0 && row < nrows) {
+    // ranks that held keys: the prefix ranks with keys, the action-key rank
+    // unless this is a cross-attention layer
+    auto held_rank = [&](int c) { return c == CS - 1 ? a.no_suffix == 0 : c * a.kc < a.P; };
+    // merge weights of this row: w_c = 2^(m_c - M) / sum_c 2^(m_c - M) l_c,
+    // M = max_c m_c over the ranks with visible keys (a rank whose keys are
+    // all hidden has l_c = 0 and weight 0)
+    float mrow[CS], lrow[CS], wgt[CS];
+#pragma unroll
+    for (int c = 0; c < CS; ++c) {
+      const float2 ml = held_rank(c) ? __ldcg(&a.xml[(cl * CS + c) * 128 + row]) : make_float2(-INFINITY, 0.f);
+      mrow[c] = ml.x;
+      lrow[c] = ml.y;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CS; ++c)
+      if (lrow[c] > 0.f) M = fmaxf(M, mrow[c]);
+    float den = 0.f;
+#pragma unroll
+    for (int c = 0; c < CS; ++c) {
+      wgt[c] = lrow[c] > 0.f ? fast_exp2(mrow[c] - M) : 0.f;
+      den += wgt[c] * lrow[c];
+    }
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int c = 0; c < CS; ++c) wgt[c] *= inv;
     const int rg = qt * 128 + row;  // row within the group: (head, token)
     const int jj = rg / a.H, i = rg - jj * a.H;
     const int j = gk * a.group + jj;
@@ -314,9 +322,7 @@ __global__ void __launch_bounds__(128, 1)
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < CS; ++c) {
-          // ranks that held keys: the prefix ranks with keys, the action-key rank
-          // unless this is a cross-attention layer
-          const bool held = (c8 + h) < q8 && (c == CS - 1 ? a.no_suffix == 0 : c * a.kc < a.P);
+          const bool held = (c8 + h) < q8 && held_rank(c);
           v[h][c] = held ? __ldcg((const uint4*)(a.xo + (cl * CS + c) * 128 * (size_t)dh) +
                                   (size_t)(rank * q8 + c8 + h) * 128 + row)
                          : make_uint4(0u, 0u, 0u, 0u);
@@ -330,8 +336,8 @@ __global__ void __launch_bounds__(128, 1)
           const uint32_t w[4] = {v[h][c].x, v[h][c].y, v[h][c].z, v[h][c].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            sum[2 * u] += __uint_as_float(w[u] << 16);
-            sum[2 * u + 1] += __uint_as_float(w[u] & 0xFFFF0000u);
+            sum[2 * u] = fmaf(wgt[c], __uint_as_float(w[u] << 16), sum[2 * u]);
+            sum[2 * u + 1] = fmaf(wgt[c], __uint_as_float(w[u] & 0xFFFF0000u), sum[2 * u + 1]);
           }
         }
         if (O32) {
@@ -386,7 +392,8 @@ cudaError_t attn_kernels_init() {
 cudaError_t launch_attn_tc(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmVt,
                            const CUtensorMap* tmKs, const CUtensorMap* tmVs, const AttnArgs& a, cudaStream_t st) {
   if (a.d_h % 64 || a.d_h > 256 || a.d_h < 64 || (a.cs != 8 && a.cs != 16) || a.kc < 16 ||
-      a.kc > 128 || a.kc % 16 || a.kc_s < 16 || a.kc_s > 128 || a.kc_s % 16 || (a.d_h / a.cs) % 8)
+      a.kc > 128 || a.kc % 16 || a.kc_s < 16 || a.kc_s > 128 || a.kc_s % 16 || (a.d_h / a.cs) % 8 || !a.xo ||
+      !a.xml)
     return cudaErrorInvalidValue;
   const int kmax = a.kc > a.kc_s ? a.kc : a.kc_s;
   const size_t smem = attn_tc_smem_bytes(a.d_h, kmax);

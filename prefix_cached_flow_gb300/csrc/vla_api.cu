@@ -105,6 +105,7 @@ struct vla_expert {
   float* xpart = nullptr;  // split-K partial tiles exchanged through L2
   float* xss = nullptr;    // per-rank sums of squares exchanged through L2
   bf16* xo = nullptr;      // attention partial outputs exchanged through L2
+  float2* xml = nullptr;   // and their row maxima and sums
   size_t xpart_elems = 0, xss_elems = 0;
   int* d_status = nullptr;
   int* h_abort = nullptr;
@@ -523,7 +524,7 @@ vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, con
   aa.kc = attn_kc(P, aa.cs);
   aa.kc_s = round_up(c.horizon, 16);
   aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)dh));
-  aa.o = (bf16*)o; aa.o32 = o32; aa.xo = h->xo; aa.status = h->d_status;
+  aa.o = (bf16*)o; aa.o32 = o32; aa.xo = h->xo; aa.xml = h->xml; aa.status = h->d_status;
   aa.pmask = h->pmask; aa.pmw = h->pmw;
   const unsigned fl = c.flags;
   const bool stream_ok = dh == 64 || dh == 128 || dh == 256;
@@ -992,6 +993,7 @@ vla_status finish_create(vla_expert* h, const void* wt1, const void* wt2, const 
     const int cs = attn_cluster(c.max_prefix);
     const size_t qtiles = (size_t)c.max_batch * c.n_kv_heads * cdiv(c.n_q_heads / c.n_kv_heads * c.horizon, 128);
     if ((s = dalloc(&h->xo, qtiles * cs * 128 * c.head_dim * 2)) != VLA_OK) return s;
+    if ((s = dalloc(&h->xml, qtiles * cs * 128 * sizeof(float2))) != VLA_OK) return s;
   }
   // attention key-chunk size: largest multiple of 16 (<= 128) whose staging fits
   ExpertDims dd = make_dims(h, 1, c.max_prefix);
@@ -1130,7 +1132,7 @@ void vla_expert_destroy(vla_expert* h) {
   void* ptrs[] = {h->wkv_pre, h->wqkv, h->wo,   h->wup,   h->wdown, h->beta,  h->win,     h->wout,
                   h->modtab,  h->modf, h->h,    h->act,   h->codes, h->alpha, h->part,    h->q,
                   h->ks,      h->vs,   h->opart, h->ml,   h->d_status, h->req_z, h->req_kc, h->req_vc,
-                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->f32buf,
+                  h->req_noise, h->req_act, h->ss1, h->ss2, h->aopart, h->aml, h->gbuf, h->tl, h->xpart, h->xss, h->xo, h->xml, h->f32buf,
                   h->cqkv, h->cup, h->p_accq, h->p_accu, h->p_rms, h->p_opart, h->p_oml, h->p_bar, h->noise_buf,
                   h->beta_rows, h->beta_pre_rows, h->zcodes, h->zalpha, h->wup_sel, h->wdown_sel, h->xt};
   for (void* p : ptrs)

@@ -661,7 +661,8 @@ struct AttnArgs {
   const uint32_t* pmask;  // prefix visibility bits [B][pmw] (null: every prefix key visible)
   int pmw;                // mask words per observation, (P + 31) / 32
   int no_suffix;          // a cross-attention layer: the cached keys only, no action keys
-  bf16* xo;          // L2 exchange of scaled partial O: [tile][rank][d_h/8][128][8] bf16
+  bf16* xo;          // L2 exchange of unnormalised partial O: [tile][rank][d_h/8][128][8] bf16
+  float2* xml;       // and of each partial's row maximum and sum (m, l): [tile][rank][128]
   float* o32;        // when set, o is written in fp32 here instead of bf16 (W2A8 quantises it next)
   int* status;
   unsigned long long* tl;  // event trace (VLA_TIMELINE builds), else unused
