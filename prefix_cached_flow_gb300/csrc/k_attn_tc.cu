@@ -13,11 +13,13 @@
 //                                       a 128-byte-swizzled tile in smem
 //   O = P V        tcgen05, A = P [128][KC], B = V^T chunk [d_h][KC] -> TMEM
 // V is stored transposed so that both MMAs read K-major operands.  The ranks
-// then merge: row maxima and sums are exchanged through distributed shared
-// memory, every rank scales its O by exp2(m_r - M) / sum_c exp2(m_c - M) l_c
-// and publishes it in bf16 through L2 (cluster barrier with release/acquire),
-// and rank r sums a d_h/CS-column slice over the ranks in fp32 (fixed order,
-// deterministic) and writes bf16 o [B*H][n_q*d_h].
+// then merge: every rank publishes its unnormalised O in bf16 and each row's
+// running maximum m_r and sum l_r through L2, one cluster barrier
+// (release/acquire) makes them visible, and rank r weights the ranks' O by
+// w_c = exp2(m_c - M) / sum_c' exp2(m_c' - M) l_c' (M the largest m over
+// ranks with visible keys), sums a d_h/CS-column slice over the ranks in fp32
+// (fixed order, deterministic) and writes bf16 o [B*H][n_q*d_h] (fp32 for the
+// W2A8 quantiser).
 // The prefix tiles are loaded before griddepcontrol.wait (they do not
 // depend on the previous kernel); Q and the action keys/values after it.
 #include "vla_common.cuh"
