@@ -1,7 +1,18 @@
 // Per-token kernels of the action expert's solver step.
 //
 // One velocity evaluation v(X^k, tau_k, C) ("vla.cpp: A Unified Inference
-// Runtime for Vision-Language-Action Models", §III-A Eq. (1)) runs, per layer:
+// Runtime for Vision-Language-Action Models", §III-A Eq. (1)).
+//
+// Default (fused) path: the linear maps and the attention run in
+// k_linear_tc.cu / k_linear_wide.cu / k_attn_*.cu with their epilogues fused;
+// this file supplies the per-step input projection with its row statistics
+// (k_embed_ss*), the velocity head with the Euler update (k_head_*), the
+// standalone modulated RMSNorm (k_modnorm*), the Eq. (4) row quantisers of
+// the W2A8 variant (k_quant_*), the time-conditioning table, the seeded
+// noise, the selected-neuron gathers and the bounded-wait self-test.
+//
+// Unfused path (the fp32 configuration and the CUDA-core diagnostic), per
+// layer:
 //   GEMM qkv -> reduce_qkv -> attention (split over key chunks) -> combine
 //   GEMM o   -> reduce_norm (residual, MLP norm)
 //   GEMM up  -> reduce_gelu
@@ -29,7 +40,8 @@ int embed_split(const ExpertDims& d) {
 }
 
 // ---------------------------------------------------------------------------
-// Time conditioning table (built once per handle; tau_k = k / S)
+// Time conditioning table (built once per handle; tau_k = k / S, or
+// 1 - k / S for the reverse schedule)
 // ---------------------------------------------------------------------------
 __global__ void k_time_embed(float* e, int S, int d_t, int reverse) {
   const int k = blockIdx.x;
