@@ -142,6 +142,8 @@ def _lib_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "prefix_cached_flow_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not f.endswith((".cu", ".cuh", ".h", ".cpp", ".c")):
+            continue  # sources only: stray files (editor backups, caches) do not count
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)

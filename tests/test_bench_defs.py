@@ -71,3 +71,25 @@ def test_roofline_picks_the_longer_roof(bench):
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-12
     roof64 = bench.roofline(CONFIGS["full_bf16_b64"], 26.0)
     assert roof64["bound"] == "tensor" and roof64["unit"] == "TFLOP/s"
+
+
+def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(bench, tmp_path, monkeypatch):
+    # A DRAM-traffic record names the hash of the library sources it was
+    # captured on; the bench reports it only while the sources hash the same.
+    csrc = tmp_path / "prefix_cached_flow_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "k.cu").write_text("// a kernel\n__global__ void k() { int x = 1; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = tmp_path / "profiles" / "solver_w_traffic.txt"
+    rec.write_text(f"dram_bytes_per_solver_launch: 123456\nlibrary_sources_sha256_16: {bench._lib_hash()}\n")
+    assert bench._traffic_from_profile("w") == 123456.0
+    # comments, blank lines and stray non-source files do not change the hash
+    (csrc / "k.cu").write_text("// the same kernel, reworded comment\n\n__global__ void k() { int x = 1; }  // x\n")
+    (csrc / "k.cu~").write_bytes(b"\xff\xfe binary backup")
+    assert bench._traffic_from_profile("w") == 123456.0
+    # a code change does
+    (csrc / "k.cu").write_text("__global__ void k() { int x = 2; }\n")
+    assert bench._traffic_from_profile("w") is None
+    # no record: None
+    assert bench._traffic_from_profile("other") is None
