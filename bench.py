@@ -27,6 +27,7 @@ import hashlib
 import re
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -289,6 +290,39 @@ def cpu_oracle_chunk(cfg, w, Z, noise):
     return O.denoise(noise.astype(np.float64), Kc, Vc, w, cfg)[0]
 
 
+def _host_threads() -> int:
+    """Threads the oracle's BLAS uses: its thread variable if set, else the
+    cores this process may run on."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _cpu_model(info: str | None = None) -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer / part codes), else the machine type."""
+    try:
+        if info is None:
+            with open("/proc/cpuinfo") as f:
+                info = f.read()
+        for key in ("model name", "Model name"):
+            m = re.search(rf"^{key}\s*:\s*(.+)$", info, flags=re.M)
+            if m:
+                return m.group(1).strip()
+        imp = re.search(r"^CPU implementer\s*:\s*(\S+)", info, flags=re.M)
+        part = re.search(r"^CPU part\s*:\s*(\S+)", info, flags=re.M)
+        if imp and part:
+            return f"{platform.machine()} implementer {imp.group(1)} part {part.group(1)}"
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(cfg, w, Z, noise, budget_s=10.0):
     """Oracle throughput on the host cores on a bounded sample: whole chunks
     of observation 0, repeated until ~budget_s of CPU work."""
@@ -302,7 +336,7 @@ def cpu_baseline(cfg, w, Z, noise, budget_s=10.0):
         if time.perf_counter() - t_all > budget_s:
             break
     mean = sum(times) / len(times)
-    return {"value": 1.0 / mean, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": 1.0 / mean, "unit": "chunks/s", "cores": _host_threads(), "cpu": _cpu_model(), "kind": "oracle",
             "sample": f"{len(times)} whole chunk(s) (prefix K/V + {cfg.S} Euler steps) of observation 0 of "
                       f"{cfg.name}, fp64 numpy/OpenBLAS, {mean * 1e3:.0f} ms per chunk"}
 
@@ -332,7 +366,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(config_dict(cfg.replace(B=1)), note="one observation per step"),
-        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "chunks/s", "cores": _host_threads(), "cpu": _cpu_model(),
+                         "kind": "oracle",
                          "sample": f"{args.steps} whole chunks of observation 0 of {cfg.name} (prefix K/V + "
                                    f"{cfg.S} Euler steps), fp64 numpy/OpenBLAS"},
         "e2e": {"value": value, "unit": "chunks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -93,3 +93,11 @@ def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(bench, tmp_
     assert bench._traffic_from_profile("w") is None
     # no record: None
     assert bench._traffic_from_profile("other") is None
+
+
+def test_cpu_model_reads_x86_and_arm_cpuinfo(bench):
+    assert bench._cpu_model("processor\t: 0\nmodel name\t: Some Xeon @ 2.70GHz\n") == "Some Xeon @ 2.70GHz"
+    arm = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n"
+    assert bench._cpu_model(arm).endswith("implementer 0x41 part 0xd4f")
+    assert bench._cpu_model("") == bench.platform.machine()
+    assert bench._host_threads() >= 1
