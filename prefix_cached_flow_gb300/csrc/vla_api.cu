@@ -528,8 +528,13 @@ vla_status plan_attention(const vla_expert* h, int B, int P, const void* kc, con
   aa.pmask = h->pmask; aa.pmw = h->pmw;
   const unsigned fl = c.flags;
   const bool stream_ok = dh == 64 || dh == 128 || dh == 256;
+  // The clustered form holds at most 128 keys per rank (prefix keys over
+  // cs - 1 ranks, the action keys on the last) and gives each rank d_h / cs
+  // output columns in whole 8-column groups; a longer prefix or horizon, or
+  // too narrow a head for the cluster, takes the streaming form.
+  const bool split_ok = aa.kc <= 128 && aa.kc_s <= 128 && (dh / aa.cs) % 8 == 0;
   ap->stream = stream_ok && ((fl & VLA_FLAG_ATTN_STREAM) ||
-                             (!(fl & VLA_FLAG_ATTN_SPLIT) && B * nkv * aa.n_qt * 5 >= h->num_sms));
+                             (!(fl & VLA_FLAG_ATTN_SPLIT) && (!split_ok || B * nkv * aa.n_qt * 5 >= h->num_sms)));
   const uint32_t krows = ap->stream ? 128u : (uint32_t)aa.kc, ksrows = ap->stream ? 128u : (uint32_t)aa.kc_s;
   if (tc_encode_2d_bf16(&ap->tmQ, h->q, dh, (uint64_t)B * c.n_q_heads * c.horizon, 64, 128) ||
       tc_encode_3d_bf16(&ap->tmK, kc, dh, P, (uint64_t)L * B * nkv, (uint64_t)dh * 2, (uint64_t)P * dh * 2, 64,

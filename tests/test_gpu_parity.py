@@ -207,6 +207,20 @@ def test_full_bf16_b1_solver_lengths(S):
     _check(gpu_run(CONFIGS["full_bf16_b1"].replace(S=S)), obs=[0], chunk_gate=gate)
 
 
+def test_small_bf16_long_prefix_batch1():
+    """A prefix too long for the clustered attention at batch 1 (with d_h = 64
+    a 16-rank cluster cannot split the head's columns in 8-column groups, and
+    more than 1920 keys do not fit 15 ranks of 128): the library takes the
+    streaming form by itself."""
+    _check(gpu_run(CONFIGS["small_bf16"], B=1, P=1000), obs=[0])
+
+
+def test_w2a8_long_prefix_batch1():
+    """2000 cached keys at batch 1 (more than 15 ranks x 128 keys), W2A8 with
+    two layers so that the oracle stays quick."""
+    _check(gpu_run(CONFIGS["w2a8_b1"].replace(L=2), B=1, P=2000), obs=[0])
+
+
 def test_w2a8_b16_free_running_chunk():
     _check(gpu_run(CONFIGS["w2a8_b16"]), obs=[7], free_running=True)
 
