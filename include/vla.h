@@ -67,9 +67,9 @@ typedef enum { VLA_SCHEDULE_FORWARD = 0, VLA_SCHEDULE_REVERSE = 1 } vla_schedule
 #define VLA_FLAG_SIMT_GEMM 1u  /* run bf16 GEMMs on the CUDA-core kernel instead of tcgen05 */
 #define VLA_FLAG_NO_GRAPH 2u   /* enqueue the solver kernels directly instead of one graph launch */
 #define VLA_FLAG_ATTN_SPLIT 4u  /* attention: always the clustered form (a query tile's keys split over SMs;
-                                   it holds at most 1920 prefix keys, and at most 896 when d_h = 64: beyond
+                                   it holds at most 1920 prefix keys, and at most 896 when d_h is 64 or 192: beyond
                                    that the call fails, while without this flag such prefixes take the
-                                   streaming form) */
+                                   streaming form where d_h is 64, 128 or 256) */
 #define VLA_FLAG_ATTN_STREAM 8u /* attention: the streaming form (one CTA per query tile, all keys) where d_h is 64, 128 or 256 */
 #define VLA_FLAG_LINEAR_SPLIT 16u /* bf16 linear layers: always the cluster split-K kernel */
 #define VLA_FLAG_LINEAR_WIDE 32u  /* bf16 linear layers: the persistent many-token kernel wherever N % 128 == 0 */
