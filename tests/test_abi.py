@@ -92,3 +92,30 @@ def test_bad_solver_length_and_misaligned_pointer(lib):
     assert lib.vla_expert_create(ctypes.byref(c), ctypes.byref(w), 0, None, ctypes.byref(out)) == 1
     w.wq = w.wq + 1
     assert lib.vla_expert_create(ctypes.byref(c), ctypes.byref(w), 4, None, ctypes.byref(out)) == 1
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/vla.h is a C header (no C++ or torch types): a C99 program that
+    includes it and takes the address of every declared entry point compiles
+    with -Wall -Werror and links against the built library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = _declared()
+    src = tmp_path / "abi_check.c"
+    body = "\n".join(f"  p[{i}] = (fn){n};" for i, n in enumerate(names))
+    src.write_text('#include "vla.h"\n#include <stdio.h>\n'
+                   f"typedef void (*fn)(void);\nint main(void) {{\n  fn p[{len(names)}];\n{body}\n"
+                   f"  for (int i = 0; i < {len(names)}; ++i) if (!p[i]) return 1;\n"
+                   '  printf("%s\\n", vla_status_string(VLA_OK));\n  return 0;\n}\n')
+    libdir = os.path.dirname(V.LIB_PATH)
+    exe = tmp_path / "abi_check"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lvla", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    # the program runs without a GPU: it only resolves symbols and reads a string
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip(), r.stderr
